@@ -1,0 +1,289 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against a hand derivation, a closed form, brute
+force with numpy on tiny inputs, or an invariant of the definition
+y[n,m] = scale[m] * sum_k w[m,k] * x[n,k]  ("state times scale",
+"Neutrino-1: quantization is a training decision", "What's actually ternary").
+"""
+import numpy as np
+import pytest
+
+from bit_matvec_ternary_b300 import synth
+from tests.conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+SHAPES = [(16, 128), (32, 256), (5, 37), (17, 129), (1, 1), (48, 300), (128, 128), (3, 260)]
+
+
+def _rand_case(M, K, seed, p0=0.626):
+    W = synth.ternary(M, K, p0, seed)
+    scale = synth.scales(M, seed)
+    return W, scale
+
+
+# ---------------------------------------------------------------- format
+
+def test_layout_hand_derived_positions(oracle_mod):
+    """Single non-zero weights land on the hand-derived word and bits."""
+    for M, K, m, k, w, wi, val in read_golden("tl2p_layout.txt"):
+        M, K, m, k, w, wi = map(int, (M, K, m, k, w, wi))
+        W = np.zeros((M, K), dtype=np.int8)
+        W[m, k] = w
+        P = oracle_mod.pack(W)
+        assert P.size == ((M + 15) // 16 * 16) * ((K + 127) // 128 * 128) // 16
+        nz = np.flatnonzero(P)
+        assert list(nz) == [wi], (M, K, m, k, nz)
+        assert int(P[wi]) == int(val, 16), (M, K, m, k, hex(int(P[wi])))
+        back, bad = oracle_mod.unpack(P, M, K)
+        assert bad == 0 and np.array_equal(back, W)
+
+
+def test_layout_is_a_bijection(oracle_mod):
+    """Every (row, column) of a full tile owns a distinct 2-bit field."""
+    M, K = 16, 128
+    seen = set()
+    for m in range(M):
+        for k in range(K):
+            W = np.zeros((M, K), dtype=np.int8)
+            W[m, k] = -1
+            P = oracle_mod.pack(W)
+            (wi,) = np.flatnonzero(P)
+            bits = int(P[wi])
+            assert bin(bits).count("1") == 2
+            lo = (bits & -bits).bit_length() - 1
+            assert lo % 2 == 0 and bits == (3 << lo)
+            seen.add((int(wi), lo))
+    assert len(seen) == M * K
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_pack_unpack_roundtrip(oracle_mod, M, K):
+    W, _ = _rand_case(M, K, seed=M * 1000 + K)
+    P = oracle_mod.pack(W)
+    back, bad = oracle_mod.unpack(P, M, K)
+    assert bad == 0
+    assert np.array_equal(back, W)
+
+
+def test_pack_rejects_values_outside_ternary(oracle_mod):
+    W = np.zeros((4, 8), dtype=np.int8)
+    W[2, 3] = 2
+    with pytest.raises(ValueError):
+        oracle_mod.pack(W)
+    W[2, 3] = -2
+    with pytest.raises(ValueError):
+        oracle_mod.pack(W)
+
+
+def test_invalid_code_decodes_to_zero_and_is_counted(oracle_mod):
+    W = np.zeros((16, 128), dtype=np.int8)
+    P = oracle_mod.pack(W)
+    P[0] |= np.uint32(0x8000)          # sign bit without the non-zero bit
+    back, bad = oracle_mod.unpack(P, 16, 128)
+    assert bad == 1 and not back.any()
+
+
+def test_padding_must_stay_zero(oracle_mod):
+    W = np.ones((5, 37), dtype=np.int8)
+    P = oracle_mod.pack(W)
+    _, bad = oracle_mod.unpack(P, 5, 37)
+    assert bad == 0
+    P2 = P.copy()
+    P2[-1] |= np.uint32(0x4000)        # row 15 / far column: padding
+    _, bad = oracle_mod.unpack(P2, 5, 37)
+    assert bad == 1
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_rowsum_three_ways(oracle_mod, M, K):
+    W, _ = _rand_case(M, K, seed=7 + M + K)
+    P = oracle_mod.pack(W)
+    rs = oracle_mod.rowsum(P, M, K)
+    assert np.array_equal(rs, W.astype(np.int64).sum(axis=1))
+    # position-free popcount identity over the whole matrix: each field is
+    # (sign, nz) with nz on even bits; +1 = nz & ~sign, -1 = nz & sign.
+    words = P.astype(np.uint64)
+    nz = words & 0x55555555
+    sg = (words >> 1) & 0x55555555
+    plus = sum(bin(int(v)).count("1") for v in (nz & ~sg & 0x55555555))
+    minus = sum(bin(int(v)).count("1") for v in (nz & sg))
+    assert plus - minus == int(rs.sum())
+    assert plus == int((W == 1).sum()) and minus == int((W == -1).sum())
+
+
+# ---------------------------------------------------------------- mode A
+
+def _x(N, K, seed, **kw):
+    return synth.activations(N, K, seed, **kw)
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("N", [1, 3, 8])
+def test_linear_a_matches_dense_bruteforce(oracle_mod, M, K, N):
+    """Mode A equals numpy's float64 dense product on the unpacked weights."""
+    W, scale = _rand_case(M, K, seed=11 * M + K)
+    X = _x(N, K, seed=M + 3 * K + N)
+    P = oracle_mod.pack(W)
+    Y, S = oracle_mod.linear_a(P, scale, M, K, X, return_sums=True)
+    xf = synth.bf16_bits_to_f32(X).astype(np.float64)
+    dense = xf @ W.astype(np.float64).T          # [N, M], exact at these sizes
+    assert np.array_equal(S, dense)
+    ref = (dense * scale.astype(np.float64)[None, :]).astype(np.float32)
+    assert np.array_equal(Y, ref)
+
+
+def test_linear_a_closed_forms(oracle_mod):
+    M, K = 37, 300
+    W, scale = _rand_case(M, K, seed=5)
+    W[3, :] = 0                                     # an all-zero row
+    P = oracle_mod.pack(W)
+    # one-hot activations: y = scale * w[m, k] * v (a single term)
+    k, v = 201, 1.5
+    X = np.zeros((1, K), dtype=np.float32)
+    X[0, k] = v
+    Y = oracle_mod.linear_a(P, scale, M, K, synth.to_bf16_bits(X))
+    expect = (scale.astype(np.float64) * W[:, k] * v).astype(np.float32)
+    assert np.array_equal(Y[0], expect)
+    # all-ones activations: y = scale * rowsum
+    X1 = synth.to_bf16_bits(np.ones((1, K), dtype=np.float32))
+    Y1 = oracle_mod.linear_a(P, scale, M, K, X1)
+    rs = W.astype(np.int64).sum(axis=1)
+    assert np.array_equal(Y1[0], (scale.astype(np.float64) * rs).astype(np.float32))
+    # the zero row gives exactly 0 for any input
+    Xr = _x(4, K, seed=9)
+    Yr = oracle_mod.linear_a(P, scale, M, K, Xr)
+    assert np.all(Yr[:, 3] == 0.0)
+
+
+def test_linear_a_is_linear(oracle_mod):
+    """Exact sums are additive: S(x1 + x2) = S(x1) + S(x2) for exact inputs."""
+    M, K = 40, 256
+    W, scale = _rand_case(M, K, seed=21)
+    P = oracle_mod.pack(W)
+    rng = np.random.default_rng(3)
+    a = rng.integers(-64, 64, size=(2, K)).astype(np.float32)
+    b = rng.integers(-64, 64, size=(2, K)).astype(np.float32)
+    _, Sa = oracle_mod.linear_a(P, scale, M, K, synth.to_bf16_bits(a), return_sums=True)
+    _, Sb = oracle_mod.linear_a(P, scale, M, K, synth.to_bf16_bits(b), return_sums=True)
+    _, Sab = oracle_mod.linear_a(P, scale, M, K, synth.to_bf16_bits(a + b), return_sums=True)
+    assert np.array_equal(Sab, Sa + Sb)
+
+
+def test_linear_a_row_independence(oracle_mod):
+    """Rows of a 16-row panel computed alone equal the same rows in the whole."""
+    M, K = 64, 384
+    W, scale = _rand_case(M, K, seed=33)
+    X = _x(2, K, seed=4)
+    Y = oracle_mod.linear_a(oracle_mod.pack(W), scale, M, K, X)
+    P = oracle_mod.pack(W)
+    words_per_panel = (K + 127) // 128 * 128
+    panel = 2
+    Pp = P[panel * words_per_panel:(panel + 1) * words_per_panel]
+    Yp = oracle_mod.linear_a(Pp, scale[32:48], 16, K, X)
+    assert np.array_equal(Yp, Y[:, 32:48])
+
+
+# ---------------------------------------------------------------- quant
+
+def test_quant_one_hot_closed_form(oracle_mod):
+    K = 512
+    for v in (0.75, 3.0, 20.0, 1e-3):
+        X = np.zeros((1, K), dtype=np.float32)
+        X[0, 17] = v
+        Q, s, z = oracle_mod.quant(synth.to_bf16_bits(X))
+        assert z[0] == -128
+        assert Q[0, 17] == 127
+        assert np.all(np.delete(Q[0], 17) == -128)
+        vb = float(synth.bf16_bits_to_f32(synth.to_bf16_bits(np.float32([v])))[0])
+        assert abs(float(s[0]) * 255.0 - vb) <= 2 * np.spacing(np.float32(vb))
+
+
+def test_quant_degenerate_zero_token(oracle_mod):
+    Q, s, z = oracle_mod.quant(np.zeros((2, 64), dtype=np.uint16))
+    assert np.all(Q == 0) and np.all(s == 1.0) and np.all(z == 0)
+    Q, s, z = oracle_mod.quant(np.zeros((2, 64), dtype=np.uint16), symmetric=True)
+    assert np.all(Q == 0) and np.all(s == 1.0) and np.all(z == 0)
+
+
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_quant_properties(oracle_mod, symmetric):
+    X = _x(8, 1000, seed=2, outlier_frac=0.01)
+    Q, s, z = oracle_mod.quant(X, symmetric=symmetric)
+    xf = synth.bf16_bits_to_f32(X).astype(np.float64)
+    deq = (Q.astype(np.float64) - z[:, None]) * s[:, None].astype(np.float64)
+    err = np.abs(deq - xf)
+    # unclamped entries are within half a step, up to fp32 rounding of x/s
+    assert np.all(err <= 0.5 * s[:, None] * (1 + 1e-5) + 1e-30)
+    if symmetric:
+        assert np.all(z == 0)
+        amax = np.abs(xf).max(axis=1)
+        assert np.allclose(s, amax / 127.0, rtol=1e-6)
+        assert np.all(np.abs(Q).max(axis=1) == 127)
+        assert Q.min() >= -127
+    else:
+        # zero is exact: x = 0 maps to q = z; the minimum maps to -128
+        lo = xf.min(axis=1)
+        for n in range(8):
+            assert Q[n, np.argmin(xf[n])] == -128 or lo[n] == 0
+        assert np.all((z >= -128) & (z <= 127))
+        Xz = X.copy()
+        Xz[:, 5] = 0
+        Qz, _, zz = oracle_mod.quant(Xz)
+        assert np.all(Qz[:, 5] == zz)
+
+
+# ---------------------------------------------------------------- mode B
+
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_linear_b_integer_sums_match_numpy(oracle_mod, M, K):
+    W, scale = _rand_case(M, K, seed=M + 99 * K)
+    X = _x(5, K, seed=K)
+    Q, s, z = oracle_mod.quant(X)
+    P = oracle_mod.pack(W)
+    rs = oracle_mod.rowsum(P, M, K)
+    acc, Y = oracle_mod.linear_b(P, scale, rs, M, K, Q, s, z)
+    assert np.array_equal(acc, Q.astype(np.int64) @ W.astype(np.int64).T)
+
+
+def test_linear_b_one_hot_identity(oracle_mod):
+    """One-hot x: acc - z*rowsum = 255*w[m,k] (q = 127 there, -128 elsewhere)."""
+    M, K = 50, 256
+    W, scale = _rand_case(M, K, seed=8)
+    P = oracle_mod.pack(W)
+    rs = oracle_mod.rowsum(P, M, K)
+    X = np.zeros((1, K), dtype=np.float32)
+    X[0, 77] = 2.5
+    Q, s, z = oracle_mod.quant(synth.to_bf16_bits(X))
+    acc, Y = oracle_mod.linear_b(P, scale, rs, M, K, Q, s, z)
+    corrected = acc[0].astype(np.int64) - int(z[0]) * rs.astype(np.int64)
+    assert np.array_equal(corrected, 255 * W[:, 77].astype(np.int64))
+    # and y is within two fp32 roundings of scale * w * v
+    ref = scale.astype(np.float64) * W[:, 77] * 2.5
+    assert np.all(np.abs(Y[0] - ref) <= 4 * np.spacing(np.abs(ref).astype(np.float32)) + 0)
+
+
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_linear_b_tracks_linear_a_within_quant_error(oracle_mod, symmetric):
+    """|y_B - y_A| <= scale * sum_k |w| * s / 2 (+ fp32 rounding): pins the
+    sign of the zero-point correction and the order of the epilogue."""
+    M, K = 64, 1024
+    W, scale = _rand_case(M, K, seed=17)
+    X = _x(6, K, seed=18, outlier_frac=0.01)
+    P = oracle_mod.pack(W)
+    rs = oracle_mod.rowsum(P, M, K)
+    Q, s, z = oracle_mod.quant(X, symmetric=symmetric)
+    _, YB = oracle_mod.linear_b(P, scale, rs, M, K, Q, s, z)
+    YA = oracle_mod.linear_a(P, scale, M, K, X)
+    absw = np.abs(W).sum(axis=1).astype(np.float64)
+    bound = scale[None, :].astype(np.float64) * absw[None, :] * (s[:, None] / 2) * (1 + 1e-4)
+    bound += 1e-6 * np.abs(YA)
+    assert np.all(np.abs(YB.astype(np.float64) - YA) <= bound)
+
+
+def test_bf16_rne_matches_hand_values(oracle_mod):
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even mantissa (1.0) wins;
+    # 1 + 3*2^-8 ties between 1+2^-7 and 1+2^-6: even (1 + 2^-6) wins.
+    vals = np.array([1.0, 1 + 2**-8, 1 + 3 * 2**-8, -2.0, 0.0, 65504.0], dtype=np.float32)
+    out = oracle_mod.bf16_rne(vals)
+    assert list(out) == [0x3F80, 0x3F80, 0x3F82, 0xC000, 0x0000, 0x4780]

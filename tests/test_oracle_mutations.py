@@ -1,0 +1,96 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each case copies tl_oracle.c, plants one plausible mistake (a wrong index, a
+flipped sign, a dropped term, a wrong rounding), compiles the copy with the
+same flags on the CPU, swaps it in, and runs the pins of test_oracle.py; at
+least one pin must fail.  Every planted mistake keeps memory accesses in
+bounds, so a mutant fails by value, never by crashing the test process.
+"""
+import os
+import subprocess
+
+import pytest
+
+from oracle import build as obuild
+from oracle import oracle as omod
+from tests import test_oracle as T
+
+MUTATIONS = {
+    "lane_index": ("int lane = 4 * g + t;", "int lane = 4 * t + g;"),
+    "fragment_index": ("int f = 2 * u + h;", "int f = 2 * h + u;"),
+    "hi_lo_columns": ("if (e == 0) { *sign_bit", "if (e == 1) { *sign_bit"),
+    "word_of_step": ("int j = s / 2;", "int j = s % 4;"),
+    "slot_of_step": ("int q = 4 * (s % 2) + f;", "int q = 4 * (s / 4) + f;"),
+    "sign_map": ("return sign ? -1 : 1;", "return sign ? 1 : -1;"),
+    "dropped_term": ("acc += (double)w[k] * (double)bf16_to_float(X[n * K + k]);",
+                     "if (k) acc += (double)w[k] * (double)bf16_to_float(X[n * K + k]);"),
+    "transposed_x": ("(double)bf16_to_float(X[n * K + k])", "(double)bf16_to_float(X[k * N + n])"),
+    "wrong_scale_row": ("Y[n * M + m] = (float)(acc * (double)scale[m]);",
+                        "Y[n * M + m] = (float)(acc * (double)scale[0]);"),
+    "scale_rounded_early": ("Y[n * M + m] = (float)(acc * (double)scale[m]);",
+                            "Y[n * M + m] = (float)acc * scale[m];"),
+    "zero_point_sign": ("acc - (int64_t)z[n] * (int64_t)rowsum[m]",
+                        "acc + (int64_t)z[n] * (int64_t)rowsum[m]"),
+    "epilogue_drops_s": ("float t = (float)corrected * s[n];", "float t = (float)corrected;"),
+    "zero_point_truncated": ("z = -128 - (int32_t)rintf(lo / s);", "z = -128 - (int32_t)(lo / s);"),
+    "quant_step_256": ("s = (hi - lo) / 255.0f;", "s = (hi - lo) / 256.0f;"),
+    "quant_clamp_low": ("if (r < -128.0f) r = -128.0f;", "if (r < -127.0f) r = -127.0f;"),
+    "sym_divisor": ("s = (a == 0.0f) ? 1.0f : a / 127.0f;", "s = (a == 0.0f) ? 1.0f : a / 128.0f;"),
+    "rowsum_dropped": ("for (int64_t k = 0; k < K; ++k) acc += oracle_weight(P, m, k, Kp, NULL);",
+                       "for (int64_t k = 1; k < K; ++k) acc += oracle_weight(P, m, k, Kp, NULL);"),
+    "int_acc_dropped_term": ("for (int64_t k = 0; k < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];",
+                             "for (int64_t k = 0; k + 1 < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];"),
+}
+
+
+def _pins():
+    """(name, callable) for every pin, with the oracle module bound."""
+    o = omod
+    return [
+        ("layout", lambda: T.test_layout_hand_derived_positions(o)),
+        ("roundtrip", lambda: [T.test_pack_unpack_roundtrip(o, M, K) for M, K in T.SHAPES]),
+        ("rowsum", lambda: [T.test_rowsum_three_ways(o, M, K) for M, K in T.SHAPES]),
+        ("brute_a", lambda: [T.test_linear_a_matches_dense_bruteforce(o, M, K, N)
+                             for M, K in T.SHAPES for N in (1, 3)]),
+        ("closed_a", lambda: T.test_linear_a_closed_forms(o)),
+        ("quant_onehot", lambda: T.test_quant_one_hot_closed_form(o)),
+        ("quant_props", lambda: [T.test_quant_properties(o, s) for s in (False, True)]),
+        ("int_sums", lambda: [T.test_linear_b_integer_sums_match_numpy(o, M, K) for M, K in T.SHAPES]),
+        ("onehot_b", lambda: T.test_linear_b_one_hot_identity(o)),
+        ("b_tracks_a", lambda: [T.test_linear_b_tracks_linear_a_within_quant_error(o, s)
+                                for s in (False, True)]),
+    ]
+
+
+def _compile(tmp_path, name, old, new):
+    src = open(obuild.SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib_{name}.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                           "-pthread", "-shared", "-fPIC", str(path), "-o", str(lib), "-lm"])
+    return str(lib)
+
+
+def test_unmutated_oracle_passes_every_pin():
+    for name, fn in _pins():
+        fn()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    old, new = MUTATIONS[name]
+    mutated = omod.load(_compile(tmp_path, name, old, new))
+    saved = omod.lib()
+    omod._lib = mutated
+    caught = []
+    try:
+        for pin, fn in _pins():
+            try:
+                fn()
+            except (AssertionError, ValueError):
+                caught.append(pin)
+    finally:
+        omod._lib = saved
+    assert caught, f"no pin caught the planted mistake {name}"
