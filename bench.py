@@ -1,0 +1,339 @@
+#!/usr/bin/env python
+"""Benchmark: the 8B-shaped ternary linear stack on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch: all 252
+projection linears of a 36-layer, Qwen3-8B-shaped decoder (hidden 4096,
+q/o 4096x4096, k/v 1024x4096, gate/up 12288x4096, down 4096x12288), as 144
+launches, on seeded synthetic weights with the pages' code statistics.  The
+headline is N = 1 decode in mode A (bf16 activations, fp32 accumulation);
+the N = 8 speculative-verify batch (modes A and B) is reported beside it.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an
+independent replica (the path has no exchange step); value is the sum of the
+ranks' tokens/s over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "8B-shape ternary linears: tokens/s at N=1 and N=8; HBM GB/s as % of B300 peak"
+WORKLOAD = ("8B-shaped ternary linear stack: 36 layers x 7 projections (252 matrices, "
+            "q/o 4096x4096, k/v 1024x4096, gate/up 12288x4096, down 4096x12288), N=1 decode, "
+            "mode A (bf16 activations, fp32 accumulate, fp32 out)")
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- timing
+def time_graph(stack, steps, warmup, torch):
+    g = stack.graph
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def time_e2e(stack, steps, warmup, torch):
+    """Per step: pinned host -> device copy of all inputs, the graph, and a
+    device -> host read of all outputs, inside the timed region."""
+    stream = torch.cuda.current_stream()
+    hx = torch.empty(stack.X_flat.shape, dtype=stack.X_flat.dtype, pin_memory=True)
+    hx.copy_(stack.X_flat.cpu())
+    hy = torch.empty(stack.Y_flat.shape, dtype=stack.Y_flat.dtype, pin_memory=True)
+
+    def step():
+        stack.X_flat.copy_(hx, non_blocking=True)
+        stack.graph.replay()
+        hy.copy_(stack.Y_flat, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, stack.input_bytes(), stack.output_bytes()
+
+
+# ---------------------------------------------------------------- oracle legs
+class OracleSample:
+    """Layer 0's seven linears packed for the CPU oracle; run() times passes
+    over them and extrapolates to the whole 252-linear stack."""
+
+    def __init__(self, host, shape, N):
+        from oracle import oracle as O
+        from bit_matvec_ternary_b300 import synth
+        self.O, self.shape, self.N = O, shape, N
+        self.cores = O.host_cores()
+        self.packed = {}
+        for p in synth.PROJ_ORDER:
+            W, scale = host[(0, p)]
+            P = O.pack(W)
+            self.packed[p] = (P, scale, O.rowsum(P, W.shape[0], W.shape[1]), W.shape)
+        shp = shape.linear_shapes()
+        self.xs = {p: synth.activations(N, shp[p][1], seed=424242 + i)
+                   for i, p in enumerate(synth.PROJ_ORDER)}
+        self.order = synth.PROJ_ORDER
+
+    def run(self, seconds, mode=0):
+        O = self.O
+        per_layer = self.shape.ternary_weights_per_layer()
+        done, t0 = 0, time.perf_counter()
+        while True:
+            for p in self.order:
+                P, scale, rs, (M, K) = self.packed[p]
+                if mode == 0:
+                    O.linear_a_mt(P, scale, M, K, self.xs[p], nthreads=self.cores)
+                else:
+                    Q, s, z = O.quant(self.xs[p])
+                    O.linear_b_mt(P, scale, rs, M, K, Q, s, z, nthreads=self.cores)
+            done += per_layer
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        passes = done / self.shape.ternary_weights()
+        desc = (f"layer 0's 7 linears x{done // per_layer} ({done / 1e9:.2f}e9 weights), "
+                f"N={self.N}, mode {'A' if mode == 0 else 'B'}, extrapolated to 252 linears")
+        return self.N * passes / el, desc
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    from bit_matvec_ternary_b300 import synth
+    shape = synth.NEUTRINO_8B
+    host = {}
+    for p in synth.PROJ_ORDER:
+        M, K = shape.linear_shapes()[p]
+        seed = synth.matrix_seed(0, 0, p)
+        host[(0, p)] = (synth.ternary(M, K, synth.zero_fraction(shape, 0, p), seed),
+                        synth.scales(M, seed))
+    sampler = OracleSample(host, shape, 1)
+    cores = sampler.cores
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        v, desc = sampler.run(seconds=0.0)
+        if i >= args.warmup:
+            per_step.append(1.0 / v)           # seconds per token (extrapolated)
+    sec = sum(per_step) / len(per_step)
+    value = 1.0 / sec
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 1,
+                       "parallelism": "none (host threads)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: " + desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-n8", action="store_true", help="skip the N=8 lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--layers", type=int, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from bit_matvec_ternary_b300 import build as tlbuild
+    tlbuild.build()
+    from bit_matvec_ternary_b300 import synth, tl
+    from bit_matvec_ternary_b300.stack import LinearStack
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    shape = synth.NEUTRINO_8B
+    hbm_peak, peak_kind = peaks()
+
+    # ---- N = 1, mode A: the headline
+    stack = LinearStack(shape, N=1, mode=tl.TL_MODE_BF16, out_dtype=tl.TL_OUT_F32,
+                        keep_host=(0,) if rank == 0 else (), layers=args.layers)
+    stack.capture()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = time_graph(stack, args.steps, args.warmup, torch)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    t = torch.tensor([ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    tok_s = world * 1.0 / (ms_max / 1e3)
+    alg = stack.algorithmic_bytes()
+    gbs = alg / (ms_max / 1e3) / 1e9
+    launches = stack.launches_per_step
+
+    ms_e2e, h2d, d2h = time_e2e(stack, args.steps, args.warmup, torch)
+    e2e = {"value": world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "how": "per step: one pinned H2D copy of all 144 inputs, one replay of the graph "
+                  "of C-ABI launches, one D2H copy of all 252 outputs"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        sampler = OracleSample(stack.host, shape, 1)
+        v, desc = sampler.run(seconds=10.0)
+        cpu = {"value": v, "unit": "tokens/s", "cores": sampler.cores, "kind": "oracle",
+               "sample": desc}
+    del stack
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if not args.no_n8:
+        for mode, name, outl in ((tl.TL_MODE_BF16, "n8_mode_a", 0.01), (tl.TL_MODE_I8, "n8_mode_b", 0.01)):
+            st8 = LinearStack(shape, N=8, mode=mode, out_dtype=tl.TL_OUT_F32, outlier_frac=outl,
+                              layers=args.layers)
+            st8.capture()
+            ms8 = time_graph(st8, args.steps, args.warmup, torch)
+            a8 = st8.algorithmic_bytes()
+            extra[name] = {"tokens_s": 8 / (ms8 / 1e3), "ms_per_step": ms8,
+                           "algorithmic_bytes": a8, "gbs": a8 / (ms8 / 1e3) / 1e9,
+                           "frac_of_hbm": a8 / (ms8 / 1e3) / 1e9 / hbm_peak,
+                           "launches_per_step": st8.launches_per_step}
+            del st8
+            torch.cuda.empty_cache()
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 1,
+                       "parallelism": f"replicas x{world}" if world > 1 else "none",
+                       "layers": args.layers or shape.layers,
+                       "l2": f"inputs larger than L2: {alg / 1e9:.3f} GB streamed per step vs "
+                             f"{L2_BYTES / 2**20:.0f} MiB L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak, "traffic": None,
+                         "kernel": "tl_mma_kernel",
+                         "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
+                         "algorithmic_bytes_per_step": alg, "launches_per_step": launches,
+                         "avg_launch_us": ms_max * 1e3 / launches},
+            "e2e": e2e,
+            "gpu_launches": launches * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        out.update(extra)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,73 @@
+"""Run one named launch of the hot path a few times (for profiler captures).
+
+    python -m bit_matvec_ternary_b300.cases --case gate_up --n 1 --mode a --reps 3
+
+Cases are the launch groups of one 8B-shaped decoder layer: qkv (q/k/v
+grouped, K = 4096), o, gate_up (gate/up grouped), down (K = 12288), and quant
+(the activation quantiser, K = 12288).  Each is built from the same seeded
+synthetic inputs as the benchmark and launched `reps` times back to back
+after `warmup` launches, then the process checks nothing and exits 0.
+"""
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+
+from . import synth
+from .stack import GROUPS
+
+CASE_GROUPS = {"qkv": 0, "o": 1, "gate_up": 2, "down": 3}
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant"])
+    ap.add_argument("--n", type=int, default=1)
+    ap.add_argument("--mode", default="a", choices=["a", "b"])
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--layer", type=int, default=5)
+    args = ap.parse_args()
+
+    import torch
+    from . import build as tlbuild
+    tlbuild.build()
+    from . import tl
+
+    shape = synth.NEUTRINO_8B
+    shp = shape.linear_shapes()
+    mode = tl.TL_MODE_BF16 if args.mode == "a" else tl.TL_MODE_I8
+    if args.case == "quant":
+        K = shp["down"][1]
+        x = synth.activations(args.n, K, seed=1)
+        xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        for _ in range(args.warmup + args.reps):
+            tl.tl_quantize_act(xt)
+        torch.cuda.synchronize()
+        return
+    grp = GROUPS[CASE_GROUPS[args.case]]
+    ws = []
+    for p in grp:
+        M, K = shp[p]
+        seed = synth.matrix_seed(0, args.layer, p)
+        W = synth.ternary(M, K, synth.zero_fraction(shape, args.layer, p), seed)
+        ws.append(tl.TernaryWeight.from_int8(W, synth.scales(M, seed)))
+    K = shp[grp[0]][1]
+    x = synth.activations(args.n, K, seed=2)
+    xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    work = tl.make_workspace([ws], args.n)
+    if mode == tl.TL_MODE_I8:
+        q, s, z = tl.tl_quantize_act(xt)
+        outs = tl.tl_linear_group(ws, q, s, z, mode=mode, workspace=work)
+        for _ in range(args.warmup + args.reps):
+            tl.tl_linear_group(ws, q, s, z, outs=outs, mode=mode, workspace=work)
+    else:
+        outs = tl.tl_linear_group(ws, xt, workspace=work)
+        for _ in range(args.warmup + args.reps):
+            tl.tl_linear_group(ws, xt, outs=outs, workspace=work)
+    torch.cuda.synchronize()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,609 @@
+// tl_kernels.cu -- sm_103a kernels and the device half of the C ABI.
+//
+// What runs here (Neutrino-1 pages):
+//   * ternary weights {-1, 0, +1} with one scale per output row and the
+//     signed sum "state times scale" (blog "Neutrino-1: quantization is a
+//     training decision", "What's actually ternary");
+//   * weights decoded inside the matrix kernel, never stored as fp16/fp32
+//     (model page "Neutrino-1 8B", "Overview");
+//   * single-stream decode is bound by bytes moved per token (blog, "Serving
+//     it: the Neutrino Engine"), so the N <= 8 kernel is built to stream the
+//     2-bit codes at HBM rate;
+//   * speculative verify: up to seven drafted tokens checked in one batched
+//     pass (wiki "Neutrino-1", "What is actually new"), hence N <= 8 columns
+//     of one mma.sync n8 tile.
+//
+// Kernel tl_mma_kernel (N <= 8, modes A and B):
+//   The TL2P v1 tile is laid out in mma.m16n8k16 A-fragment order, so one
+//   128-bit load gives a lane the 64 weights it needs for 8 MMA steps over
+//   rows g and g+8.  Register f of a step is (word << 2q) & 0xC000C000: a
+//   bf16x2 pair of +-2.0 / +-0.0.  Activations are staged once per CTA in
+//   shared memory in B-fragment order (mode B converts int8 to bf16, exact).
+//   Work is split "stream-K" style: the (slice, row tile, k-block) units of
+//   the launch are cut into equal contiguous ranges, one per warp, so every
+//   warp streams the same number of bytes.  A row tile whose k-range spans
+//   several warps is finished by whichever warp arrives last (counter in the
+//   workspace); it adds the partial sums in a fixed order, so results are
+//   deterministic and do not depend on N.
+
+#include "tl.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <algorithm>
+#include <cstring>
+
+namespace {
+
+constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
+constexpr int kThreads = kWarps * 32;
+constexpr int kDepth = 8;             // 128-bit weight loads in flight per lane
+constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
+constexpr int kMaxDevices = 64;
+constexpr size_t kSmemLimit = 200 * 1024;
+constexpr int kMaxSlice = 32;         // 128-column blocks per split-K slice, at most
+
+struct GroupArgs {
+    const char *packed[TL_MAX_GROUP];
+    const float *scale[TL_MAX_GROUP];
+    const int32_t *rowsum[TL_MAX_GROUP];
+    void *Y[TL_MAX_GROUP];
+    int M[TL_MAX_GROUP];
+    int rt_off[TL_MAX_GROUP + 1];   // row-tile prefix over the group
+    int G;
+    int R;          // row tiles in the launch
+    int KB;         // 128-column blocks
+    int KS;         // blocks per slice
+    int S;          // slices
+    int K;
+    long long U;    // units = R * KB
+    long long V;    // warps in the grid
+    const void *X;  // bf16 [N][K] (mode A) or int8 [N][K] (mode B)
+    const float *s;
+    const int32_t *z;
+    int N;
+    int mode;
+    int out;
+    float *part;    // split-K partials [R*S*2][N][16]
+    int *cnt;       // [R] arrival counters (units), zero between launches
+};
+
+__device__ __forceinline__ long long bnd(const GroupArgs &a, long long v) {
+    return v * a.U / a.V;
+}
+
+// Warp owning unit u: the v with bnd(v) <= u < bnd(v + 1).
+__device__ __forceinline__ long long warp_of(const GroupArgs &a, long long u) {
+    long long v = (u * a.V) / a.U;
+    while (v + 1 <= a.V && bnd(a, v + 1) <= u) ++v;
+    while (v > 0 && bnd(a, v) > u) --v;
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Position of a unit: slice s, row tile r (group-wide), block bp in the slice,
+// and the matrix gi / local row tile rl it belongs to.
+struct Cursor {
+    long long u;
+    int s, r, bp, gi, rl;
+
+    __device__ void seek(const GroupArgs &a, long long u0) {
+        u = u0;
+        const long long su = (long long)a.R * a.KS;
+        s = (int)(u0 / su);
+        const long long rem = u0 - (long long)s * su;
+        r = (int)(rem / a.KS);
+        bp = (int)(rem - (long long)r * a.KS);
+        gi = 0;
+        while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
+        rl = r - a.rt_off[gi];
+    }
+    __device__ __forceinline__ void next(const GroupArgs &a) {
+        ++u;
+        if (++bp == a.KS) {
+            bp = 0;
+            if (++r == a.R) {
+                r = 0; ++s; gi = 0; rl = 0;
+            } else if (r == a.rt_off[gi + 1]) {
+                ++gi; rl = 0;
+            } else {
+                ++rl;
+            }
+        }
+    }
+    __device__ __forceinline__ const char *ptr(const GroupArgs &a, int lane) const {
+        const long long tile = (long long)rl * a.KB + (long long)s * a.KS + bp;
+        return a.packed[gi] + tile * 512 + lane * 16;
+    }
+};
+
+__device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int n, float acc) {
+    // acc holds 2 * sum_k w*x (weights decode to +-2.0); halving is exact.
+    const int M = a.M[gi];
+    const float half = acc * 0.5f;
+    float y;
+    if (a.mode == TL_MODE_BF16) {
+        y = __fmul_rn(half, a.scale[gi][m]);
+    } else {
+        const int iacc = __float2int_rn(half);
+        if (a.out == TL_OUT_I32_RAW) {
+            reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * M + m] = iacc;
+            return;
+        }
+        const int corrected = iacc - a.z[n] * a.rowsum[gi][m];
+        y = __fmul_rn(__fmul_rn((float)corrected, a.s[n]), a.scale[gi][m]);
+    }
+    if (a.out == TL_OUT_F32)
+        reinterpret_cast<float *>(a.Y[gi])[(long long)n * M + m] = y;
+    else
+        reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * M + m] = __float2bfloat16_rn(y);
+}
+
+__device__ __forceinline__ void epilogue(const GroupArgs &a, int gi, int rl, int g, int t,
+                                         const float (&c)[4]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int m = rl * 16 + g + 8 * h;
+            const int n = 2 * t + e;
+            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, c[2 * h + e]);
+        }
+}
+
+// Emit the partial sum of one piece (row tile r, slice s, piece p, nk blocks).
+__device__ __noinline__ void flush_piece(const GroupArgs &a, int r, int s, int p, int nk, int gi,
+                                         int rl, int lane, float c0, float c1, float c2,
+                                         float c3) {
+    const int g = lane >> 2, t = lane & 3;
+    const float c[4] = {c0, c1, c2, c3};
+    if (a.S == 1 && nk == a.KB) {   // the whole k-range in one piece: final
+        epilogue(a, gi, rl, g, t, c);
+        return;
+    }
+    const long long slot = ((long long)r * a.S + s) * 2 + p;
+    float *dst = a.part + slot * a.N * 16;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = 2 * t + e;
+            if (n < a.N) __stcg(dst + n * 16 + g + 8 * h, c[2 * h + e]);
+        }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+        const int old = atomicAdd(a.cnt + r, nk);
+        last = (old + nk == a.KB);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ss = 0; ss < a.S; ++ss) {
+        const long long us = ((long long)ss * a.R + r) * a.KS;
+        const long long v0 = warp_of(a, us);
+        const bool split = bnd(a, v0 + 1) < us + a.KS;
+        for (int pp = 0; pp < (split ? 2 : 1); ++pp) {
+            const float *src = a.part + (((long long)r * a.S + ss) * 2 + pp) * a.N * 16;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int n = 2 * t + e;
+                    if (n < a.N) acc[2 * h + e] += __ldcg(src + n * 16 + g + 8 * h);
+                }
+        }
+    }
+    epilogue(a, gi, rl, g, t, acc);
+    if (lane == 0) a.cnt[r] = 0;
+}
+
+__global__ void __launch_bounds__(kThreads)
+tl_mma_kernel(const __grid_constant__ GroupArgs a) {
+    extern __shared__ uint4 xs[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+
+    const long long v = (long long)blockIdx.x * kWarps + warp;
+    const long long u0 = bnd(a, v), u1 = bnd(a, v + 1);
+    const long long cu0 = bnd(a, (long long)blockIdx.x * kWarps);
+    const long long cu1 = bnd(a, (long long)(blockIdx.x + 1) * kWarps);
+    const long long su = (long long)a.R * a.KS;
+    const int s_lo = (int)(cu0 / su);
+    const int n_sl = cu1 > cu0 ? (int)((cu1 - 1) / su) - s_lo + 1 : 0;
+
+    // Weights do not depend on the previous kernel: start streaming them
+    // before waiting for it.
+    uint4 ring[kDepth];
+    Cursor pf;
+    pf.seek(a, u0);
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i) {
+        if (pf.u < u1) ring[i] = ldg_stream(pf.ptr(a, lane));
+        pf.next(a);
+    }
+    griddep_wait();
+    griddep_launch();
+
+    // Stage X for this CTA's slices in B-fragment order:
+    // word ((((sl*KS + bp)*4 + qd)*N + n)*4 + t)*4 + w holds x[n][k], x[n][k+1]
+    // with k = ((s_lo+sl)*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
+    {
+        const int N = a.N;
+        const long long words = (long long)n_sl * a.KS * 64 * N;
+        uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
+        for (long long idx = threadIdx.x; idx < words; idx += kThreads) {
+            const int w = (int)(idx & 3), tt = (int)((idx >> 2) & 3);
+            long long rest = idx >> 4;
+            const int n = (int)(rest % N); rest /= N;
+            const int qd = (int)(rest & 3); rest >>= 2;
+            const int bp = (int)(rest % a.KS);
+            const int sl = (int)(rest / a.KS);
+            const int k = ((s_lo + sl) * a.KS + bp) * 128 + 16 * (2 * qd + (w >> 1)) + 2 * tt +
+                          8 * (w & 1);
+            uint32_t lo = 0, hi = 0;
+            if (a.mode == TL_MODE_BF16) {
+                const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
+                if (k < a.K) lo = x[k];
+                if (k + 1 < a.K) hi = x[k + 1];
+            } else {
+                const int8_t *x = reinterpret_cast<const int8_t *>(a.X) + (long long)n * a.K;
+                if (k < a.K) lo = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k]));
+                if (k + 1 < a.K) hi = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k + 1]));
+            }
+            xw[idx] = lo | (hi << 16);
+        }
+    }
+    __syncthreads();
+
+    const uint32_t M2 = 0xC000C000u;
+    const bool xlane = g < a.N;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    Cursor cc;
+    cc.seek(a, u0);
+    int piece_p = cc.bp == 0 ? 0 : 1;
+    int piece_nk = 0;
+
+    for (long long base = u0; base < u1; base += kDepth) {
+#pragma unroll
+        for (int i = 0; i < kDepth; ++i) {
+            if (base + i < u1) {
+                const uint4 w = ring[i];
+                if (pf.u < u1) ring[i] = ldg_stream(pf.ptr(a, lane));
+                pf.next(a);
+
+                const uint4 *xb = xs + ((long long)((cc.s - s_lo) * a.KS + cc.bp) * 4 * a.N + g) * 4 + t;
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                    const uint32_t word = qd == 0 ? w.x : qd == 1 ? w.y : qd == 2 ? w.z : w.w;
+                    uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                    if (xlane) b = xb[qd * a.N * 4];
+                    mma_bf16_16816(c, word & M2, (word << 2) & M2, (word << 4) & M2,
+                                   (word << 6) & M2, b.x, b.y);
+                    mma_bf16_16816(c, (word << 8) & M2, (word << 10) & M2, (word << 12) & M2,
+                                   (word << 14) & M2, b.z, b.w);
+                }
+                ++piece_nk;
+                const bool seg_end = (cc.bp == a.KS - 1) || (base + i + 1 == u1);
+                if (seg_end) {
+                    flush_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane, c[0], c[1],
+                                c[2], c[3]);
+                    c[0] = c[1] = c[2] = c[3] = 0.f;
+                    piece_p = 0;
+                    piece_nk = 0;
+                }
+                cc.next(a);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ quant
+__global__ void __launch_bounds__(256)
+tl_quant_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Q,
+                float *__restrict__ s_out, int32_t *__restrict__ z_out, int symmetric) {
+    const int n = blockIdx.x;
+    const uint16_t *x = X + (long long)n * K;
+    int8_t *q = Q + (long long)n * K;
+    float lo = 0.f, hi = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const float v = __uint_as_float((uint32_t)x[k] << 16);
+        if (symmetric) {
+            hi = fmaxf(hi, fabsf(v));
+        } else {
+            lo = fminf(lo, v);
+            hi = fmaxf(hi, v);
+        }
+    }
+    __shared__ float slo[32], shi[32];
+    __shared__ float s_sh;
+    __shared__ int z_sh;
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    const int wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    if (ln == 0) { slo[wid] = lo; shi[wid] = hi; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+            lo = fminf(lo, slo[w]);
+            hi = fmaxf(hi, shi[w]);
+        }
+        float s;
+        int z;
+        if (symmetric) {
+            s = hi == 0.f ? 1.f : __fdiv_rn(hi, 127.f);
+            z = 0;
+        } else if (hi == lo) {
+            s = 1.f;
+            z = 0;
+        } else {
+            s = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
+            z = -128 - (int)rintf(__fdiv_rn(lo, s));
+        }
+        s_sh = s;
+        z_sh = z;
+        s_out[n] = s;
+        z_out[n] = z;
+    }
+    __syncthreads();
+    const float s = s_sh;
+    const float zf = (float)z_sh;
+    const float qlo = symmetric ? -127.f : -128.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const float v = __uint_as_float((uint32_t)x[k] << 16);
+        float r = __fadd_rn(rintf(__fdiv_rn(v, s)), zf);
+        r = fminf(fmaxf(r, qlo), 127.f);
+        q[k] = (int8_t)(int)r;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+struct DeviceInfo {
+    int init;     // 0 = unknown, 1 = ok, -1 = unsupported
+    int sms;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+tl_status device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TL_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TL_ERR_UNSUPPORTED;
+    DeviceInfo &d = g_dev[dev];
+    if (d.init == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TL_ERR_CUDA;
+        if (major != 10 || minor != 3) {
+            d.init = -1;
+        } else {
+            if (cudaFuncSetAttribute(tl_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemLimit) != cudaSuccess)
+                return TL_ERR_CUDA;
+            d.sms = sms;
+            d.init = 1;
+        }
+    }
+    if (d.init < 0) return TL_ERR_UNSUPPORTED;
+    *out = &d;
+    return TL_OK;
+}
+
+struct Plan {
+    int R, KB, KS, S, P;
+    long long U, V;
+    size_t smem;       // for the given N
+    size_t ws_bytes;   // workspace for the given N
+};
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// The plan depends on the shapes and the SM count only, never on N, so every
+// token is summed in the same order whatever the batch.
+void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
+    p->R = 0;
+    for (int g = 0; g < G; ++g) p->R += (int)ceil_div(Ms[g], 16);
+    p->KB = (int)ceil_div(K, 128);
+    p->U = (long long)p->R * p->KB;
+    long long ctas = sms;                       // one CTA of 8 warps per SM
+    ctas = std::min<long long>(ctas, ceil_div(p->U, (long long)kWarps * 2));
+    if (ctas < 1) ctas = 1;
+    p->P = (int)ctas;
+    p->V = ctas * kWarps;
+    const long long avg = p->U / p->V;
+    // Largest slice (in 128-column blocks) that divides KB, keeps every
+    // slice segment within two warps (min warp range >= KS - 1) and keeps
+    // the staged activations of one CTA within the shared-memory budget at
+    // N = 8.  Chosen without looking at N.
+    const long long cta_units = ceil_div(p->U, p->P);
+    p->KS = 1;
+    for (int d = 1; d <= p->KB && d <= kMaxSlice; ++d) {
+        if (p->KB % d != 0 || d > avg + 1) continue;
+        const long long su = (long long)p->R * d;
+        const long long n_sl = std::min<long long>(p->KB / d, ceil_div(cta_units, su) + 1);
+        if ((size_t)n_sl * d * 128 * kNMax * 2 <= kSmemLimit) p->KS = d;
+    }
+    p->S = p->KB / p->KS;
+    const long long su = (long long)p->R * p->KS;
+    const long long n_sl = std::min<long long>(p->S, ceil_div(cta_units, su) + 1);
+    const int n = std::min(std::max(N, 1), kNMax);
+    p->smem = (size_t)n_sl * p->KS * 128 * n * 2;
+    const size_t cnt_bytes = ((size_t)p->R * 4 + 255) / 256 * 256;
+    p->ws_bytes = cnt_bytes + (size_t)p->R * p->S * 2 * 16 * n * 4;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+tl_status check_weights(const tl_weight *Ws, int G, int mode) {
+    if (!Ws) return TL_ERR_NULL;
+    if (G < 1 || G > TL_MAX_GROUP) return TL_ERR_SHAPE;
+    for (int g = 0; g < G; ++g) {
+        const tl_weight &w = Ws[g];
+        if (!w.packed || !w.scale) return TL_ERR_NULL;
+        if (mode == TL_MODE_I8 && !w.rowsum) return TL_ERR_NULL;
+        if (w.layout != TL_LAYOUT_TL2P_V1) return TL_ERR_UNSUPPORTED;
+        if (w.M < 1 || w.K < 1 || w.M > TL_MAX_M || w.K > TL_MAX_K) return TL_ERR_SHAPE;
+        if (w.K != Ws[0].K) return TL_ERR_SHAPE;
+        if (!aligned(w.packed, 16) || !aligned(w.scale, 4)) return TL_ERR_ALIGN;
+        if (mode == TL_MODE_I8 && !aligned(w.rowsum, 4)) return TL_ERR_ALIGN;
+    }
+    return TL_OK;
+}
+
+size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
+    int Ms[TL_MAX_GROUP];
+    for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
+    Plan p;
+    make_plan(Ms, G, Ws[0].K, N, sms, &p);
+    return p.ws_bytes;
+}
+
+tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s,
+                       const int32_t *z, void *const *Ys, int n0, int n, int mode, int out,
+                       void *ws, size_t ws_bytes, unsigned flags, cudaStream_t stream,
+                       const DeviceInfo &dev) {
+    GroupArgs a;
+    std::memset(&a, 0, sizeof a);
+    int Ms[TL_MAX_GROUP];
+    a.G = G;
+    a.rt_off[0] = 0;
+    const int K = Ws[0].K;
+    for (int g = 0; g < G; ++g) {
+        a.packed[g] = reinterpret_cast<const char *>(Ws[g].packed);
+        a.scale[g] = Ws[g].scale;
+        a.rowsum[g] = Ws[g].rowsum;
+        a.M[g] = Ms[g] = Ws[g].M;
+        const size_t esz = out == TL_OUT_BF16 ? 2 : 4;
+        a.Y[g] = static_cast<char *>(Ys[g]) + (size_t)n0 * Ws[g].M * esz;
+        a.rt_off[g + 1] = a.rt_off[g] + (int)ceil_div(Ws[g].M, 16);
+    }
+    Plan p;
+    make_plan(Ms, G, K, n, dev.sms, &p);
+    if (p.smem > kSmemLimit) return TL_ERR_SHAPE;
+    if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
+    a.R = p.R; a.KB = p.KB; a.KS = p.KS; a.S = p.S; a.K = K; a.U = p.U; a.V = p.V;
+    const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
+    a.X = static_cast<const char *>(X) + (size_t)n0 * K * xsz;
+    a.s = s ? s + n0 : nullptr;
+    a.z = z ? z + n0 : nullptr;
+    a.N = n; a.mode = mode; a.out = out;
+    const size_t cnt_bytes = ((size_t)p.R * 4 + 255) / 256 * 256;
+    a.cnt = static_cast<int *>(ws);
+    a.part = reinterpret_cast<float *>(static_cast<char *>(ws) + cnt_bytes);
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)p.P);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, tl_mma_kernel, a) != cudaSuccess) return TL_ERR_CUDA;
+    return TL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N) {
+    if (!Ws || G < 1 || G > TL_MAX_GROUP || N < 1) return 0;
+    DeviceInfo *dev = nullptr;
+    int sms = 148;
+    if (device_info(&dev) == TL_OK) sms = dev->sms;
+    for (int g = 0; g < G; ++g)
+        if (Ws[g].M < 1 || Ws[g].K < 1 || Ws[g].K != Ws[0].K) return 0;
+    return workspace_bytes_for(Ws, G, N, sms);
+}
+
+tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, float *s, int32_t *z,
+                          int symmetric, void *stream) {
+    if (!X_bf16 || !Q || !s || !z) return TL_ERR_NULL;
+    if (N < 1 || K < 1 || K > TL_MAX_K) return TL_ERR_SHAPE;
+    if (!aligned(X_bf16, 2) || !aligned(s, 4) || !aligned(z, 4)) return TL_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    const tl_status st = device_info(&dev);
+    if (st != TL_OK) return st;
+    tl_quant_kernel<<<N, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(X_bf16), K, Q, s, z, symmetric ? 1 : 0);
+    return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+}
+
+tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float *s,
+                          const int32_t *z, void *const *Ys, int N, int mode, int out_dtype,
+                          void *workspace, size_t workspace_bytes, unsigned flags,
+                          void *stream) {
+    tl_status st = check_weights(Ws, G, mode);
+    if (st != TL_OK) return st;
+    if (mode != TL_MODE_BF16 && mode != TL_MODE_I8) return TL_ERR_MODE;
+    if (out_dtype != TL_OUT_F32 && out_dtype != TL_OUT_BF16 && out_dtype != TL_OUT_I32_RAW)
+        return TL_ERR_MODE;
+    if (out_dtype == TL_OUT_I32_RAW && mode != TL_MODE_I8) return TL_ERR_MODE;
+    if (!X || !Ys) return TL_ERR_NULL;
+    if (N < 1) return TL_ERR_SHAPE;
+    if (mode == TL_MODE_I8 && (!s || !z)) return TL_ERR_NULL;
+    if (mode == TL_MODE_BF16 && !aligned(X, 2)) return TL_ERR_ALIGN;
+    if (mode == TL_MODE_I8 && (!aligned(s, 4) || !aligned(z, 4))) return TL_ERR_ALIGN;
+    for (int g = 0; g < G; ++g) {
+        if (!Ys[g]) return TL_ERR_NULL;
+        if (!aligned(Ys[g], out_dtype == TL_OUT_BF16 ? 2 : 4)) return TL_ERR_ALIGN;
+    }
+    if (!workspace) return TL_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TL_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != TL_OK) return st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    for (int n0 = 0; n0 < N; n0 += kNMax) {
+        const int n = N - n0 < kNMax ? N - n0 : kNMax;
+        st = launch_chunk(Ws, G, X, s, z, Ys, n0, n, mode, out_dtype, workspace,
+                          workspace_bytes, flags, cs, *dev);
+        if (st != TL_OK) return st;
+    }
+    return TL_OK;
+}
+
+tl_status tl_linear(const tl_weight *W, const void *X, const float *s, const int32_t *z, void *Y,
+                    int N, int mode, int out_dtype, void *workspace, size_t workspace_bytes,
+                    unsigned flags, void *stream) {
+    void *Ys[1] = {Y};
+    return tl_linear_group(W, 1, X, s, z, Ys, N, mode, out_dtype, workspace, workspace_bytes,
+                           flags, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+"""A decoder's stack of ternary projection linears, run through the C ABI.
+
+Per layer the seven projections run in dependency order, as four launches:
+[q, k, v] (one grouped launch sharing X) -> o -> [gate, up] (grouped) ->
+down (model page "Neutrino-1 8B", "Architecture": seven linears per layer,
+36 layers, 252 in all).  The attention and SwiGLU between them are not part
+of this path, so each launch reads its own resident input; launches still
+follow one another on one stream, and with ``TL_FLAG_PDL`` each one starts
+streaming its weights while the previous one drains.  ``capture()`` records
+one pass as a CUDA graph.
+
+Mode B adds one activation-quantisation launch in front of every linear
+launch (four per layer).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import synth
+from . import tl
+
+GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
+class LinearStack:
+    def __init__(self, shape: synth.ModelShape, N: int, mode: int = tl.TL_MODE_BF16,
+                 out_dtype: int = tl.TL_OUT_F32, base_seed: int = 0, outlier_frac: float = 0.0,
+                 unit_rms: bool = False, layers: int | None = None, keep_host=(),
+                 device: str = "cuda", symmetric: bool = False):
+        import torch
+        self.torch = torch
+        self.shape = shape
+        self.N, self.mode, self.out_dtype = N, mode, out_dtype
+        self.symmetric = symmetric
+        self.layers = shape.layers if layers is None else layers
+        self.device = device
+        self.host = {}            # (layer, proj) -> (W int8, scale) for kept layers
+        shp = shape.linear_shapes()
+        self.weights = []         # per layer: dict proj -> TernaryWeight
+        for l in range(self.layers):
+            d = {}
+            for p in synth.PROJ_ORDER:
+                M, K = shp[p]
+                seed = synth.matrix_seed(base_seed, l, p)
+                W = synth.ternary(M, K, synth.zero_fraction(shape, l, p), seed)
+                scale = synth.scales(M, seed)
+                d[p] = tl.TernaryWeight.from_int8(W, scale, device=device)
+                if l in keep_host:
+                    self.host[(l, p)] = (W, scale)
+                del W
+            self.weights.append(d)
+        # Inputs (one per launch group and layer) live in one flat bf16 buffer
+        # and outputs in one flat buffer, so a host round trip is two copies.
+        odt = {tl.TL_OUT_F32: torch.float32, tl.TL_OUT_BF16: torch.bfloat16}[out_dtype]
+        x_sizes = [N * shp[grp[0]][1] for _ in range(self.layers) for grp in GROUPS]
+        y_sizes = [N * shp[p][0] for _ in range(self.layers) for grp in GROUPS for p in grp]
+        self.X_flat = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=device)
+        self.Y_flat = torch.empty(sum(y_sizes), dtype=odt, device=device)
+        self.X, self.Q, self.S, self.Z, self.Y = [], [], [], [], []
+        xo = yo = 0
+        for l in range(self.layers):
+            xs, qs, ss, zs, ys = [], [], [], [], []
+            for gi, grp in enumerate(GROUPS):
+                K = shp[grp[0]][1]
+                bits = synth.activations(N, K, seed=base_seed + 100_000 + 10 * l + gi,
+                                         outlier_frac=outlier_frac, unit_rms=unit_rms)
+                xt = self.X_flat[xo:xo + N * K].view(N, K)
+                xo += N * K
+                xt.copy_(torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16))
+                xs.append(xt)
+                if mode == tl.TL_MODE_I8:
+                    qs.append(torch.empty((N, K), dtype=torch.int8, device=device))
+                    ss.append(torch.empty(N, dtype=torch.float32, device=device))
+                    zs.append(torch.empty(N, dtype=torch.int32, device=device))
+                outs = []
+                for p in grp:
+                    M = shp[p][0]
+                    outs.append(self.Y_flat[yo:yo + N * M].view(N, M))
+                    yo += N * M
+                ys.append(outs)
+            self.X.append(xs); self.Q.append(qs); self.S.append(ss); self.Z.append(zs)
+            self.Y.append(ys)
+        groups = [[self.weights[l][p] for p in grp] for l in range(self.layers) for grp in GROUPS]
+        self.workspace = tl.make_workspace(groups, N, device=device)
+        self.graph = None
+
+    # ------------------------------------------------------------------ run
+    @property
+    def launches_per_step(self) -> int:
+        per_layer = len(GROUPS) * (2 if self.mode == tl.TL_MODE_I8 else 1)
+        return per_layer * self.layers
+
+    def run(self, flags: int = tl.TL_FLAG_PDL, stream=None) -> None:
+        for l in range(self.layers):
+            for gi, grp in enumerate(GROUPS):
+                ws = [self.weights[l][p] for p in grp]
+                x = self.X[l][gi]
+                if self.mode == tl.TL_MODE_I8:
+                    q, s, z = self.Q[l][gi], self.S[l][gi], self.Z[l][gi]
+                    tl.tl_quantize_act(x, symmetric=self.symmetric, Q=q, s=s, z=z, stream=stream)
+                    tl.tl_linear_group(ws, q, s, z, outs=self.Y[l][gi], mode=self.mode,
+                                       out_dtype=self.out_dtype, workspace=self.workspace,
+                                       flags=flags, stream=stream)
+                else:
+                    tl.tl_linear_group(ws, x, outs=self.Y[l][gi], mode=self.mode,
+                                       out_dtype=self.out_dtype, workspace=self.workspace,
+                                       flags=flags, stream=stream)
+
+    def capture(self, flags: int = tl.TL_FLAG_PDL):
+        """Record one pass as a CUDA graph (kernels launched by the C ABI)."""
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run(flags=flags)          # warm: device attributes cached before capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(flags=flags)
+        torch.cuda.synchronize()
+        self.graph = g
+        return g
+
+    # ------------------------------------------------------------ accounting
+    def algorithmic_bytes(self) -> int:
+        """Bytes the method must move per pass: packed codes, per-row scales
+        (and row sums in mode B), each input once, each output once."""
+        shp = self.shape.linear_shapes()
+        per_layer = 0
+        xb = 2                                         # bf16 inputs, read once
+        yb = 4 if self.out_dtype == tl.TL_OUT_F32 else 2
+        for grp in GROUPS:
+            K = shp[grp[0]][1]
+            per_layer += self.N * K * xb
+            for p in grp:
+                M = shp[p][0]
+                per_layer += tl.tl_packed_bytes(M, K) + 4 * M + self.N * M * yb
+                if self.mode == tl.TL_MODE_I8:
+                    per_layer += 4 * M
+        if self.mode == tl.TL_MODE_I8:
+            per_layer += len(GROUPS) * self.N * 8      # s and z
+        return per_layer * self.layers
+
+    def weight_count(self) -> int:
+        return self.shape.ternary_weights_per_layer() * self.layers
+
+    def output_bytes(self) -> int:
+        return self.Y_flat.numel() * self.Y_flat.element_size()
+
+    def input_bytes(self) -> int:
+        return self.X_flat.numel() * self.X_flat.element_size()

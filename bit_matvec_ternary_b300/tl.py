@@ -1,0 +1,245 @@
+"""Python binding of the C ABI in include/tl.h (ctypes over libtl.so).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels (or, for ``tl_pack``, its host packer).  PyTorch
+supplies device memory and the current CUDA stream.  Importing this module
+fails loudly when libtl.so has not been built -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtl.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m bit_matvec_ternary_b300.build` "
+        "(the ternary linears have no non-CUDA implementation)")
+
+_lib = C.CDLL(LIB_PATH)
+
+TL_OK = 0
+TL_ERR_NULL, TL_ERR_SHAPE, TL_ERR_ALIGN, TL_ERR_BAD_VALUE = 1, 2, 3, 4
+TL_ERR_MODE, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_WORKSPACE = 5, 6, 7, 8, 9
+TL_MODE_BF16, TL_MODE_I8 = 0, 1
+TL_OUT_F32, TL_OUT_BF16, TL_OUT_I32_RAW = 0, 1, 2
+TL_FLAG_PDL = 1
+TL_LAYOUT_TL2P_V1 = 1
+TL_MAX_GROUP = 4
+
+# Every symbol include/tl.h declares.
+EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
+           "tl_quantize_act", "tl_linear", "tl_linear_group", "tl_status_string",
+           "tl_version")
+
+
+class tl_weight(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("scale", C.c_void_p), ("rowsum", C.c_void_p),
+                ("M", C.c_int32), ("K", C.c_int32), ("layout", C.c_uint32)]
+
+
+_p, _i64, _int, _sz = C.c_void_p, C.c_int64, C.c_int, C.c_size_t
+_lib.tl_packed_bytes.argtypes = [_i64, _i64]
+_lib.tl_packed_bytes.restype = _sz
+_lib.tl_pack.argtypes = [_p, _i64, _i64, _p, _p, _p, _p]
+_lib.tl_pack.restype = _int
+_lib.tl_validate_packed.argtypes = [_p, _i64, _i64, C.POINTER(C.c_int64)]
+_lib.tl_validate_packed.restype = _int
+_lib.tl_workspace_bytes.argtypes = [C.POINTER(tl_weight), _int, _int]
+_lib.tl_workspace_bytes.restype = _sz
+_lib.tl_quantize_act.argtypes = [_p, _int, _int, _p, _p, _p, _int, _p]
+_lib.tl_quantize_act.restype = _int
+_lib.tl_linear.argtypes = [C.POINTER(tl_weight), _p, _p, _p, _p, _int, _int, _int, _p, _sz,
+                           C.c_uint, _p]
+_lib.tl_linear.restype = _int
+_lib.tl_linear_group.argtypes = [C.POINTER(tl_weight), _int, _p, _p, _p, C.POINTER(_p), _int,
+                                 _int, _int, _p, _sz, C.c_uint, _p]
+_lib.tl_linear_group.restype = _int
+_lib.tl_status_string.argtypes = [_int]
+_lib.tl_status_string.restype = C.c_char_p
+_lib.tl_version.argtypes = []
+_lib.tl_version.restype = _int
+
+
+class TLError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tl_status_string(status)} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != TL_OK:
+        raise TLError(status, where)
+
+
+def tl_status_string(status: int) -> str:
+    return _lib.tl_status_string(int(status)).decode()
+
+
+def tl_version() -> int:
+    return int(_lib.tl_version())
+
+
+def tl_packed_bytes(M: int, K: int) -> int:
+    return int(_lib.tl_packed_bytes(M, K))
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def tl_pack(W: np.ndarray, scale: np.ndarray | None = None):
+    """Host packer: int8 W[M, K] -> (uint32 words, fp32 scale copy, int32 rowsum)."""
+    W = np.ascontiguousarray(W, dtype=np.int8)
+    M, K = W.shape
+    packed = np.zeros(max(tl_packed_bytes(M, K), 4) // 4, dtype=np.uint32)
+    rowsum = np.zeros(M, dtype=np.int32)
+    if scale is not None:
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+        scale_out = np.empty(M, dtype=np.float32)
+        st = _lib.tl_pack(_np_ptr(W), M, K, _np_ptr(scale), _np_ptr(packed),
+                          _np_ptr(scale_out), _np_ptr(rowsum))
+    else:
+        scale_out = None
+        st = _lib.tl_pack(_np_ptr(W), M, K, None, _np_ptr(packed), None, _np_ptr(rowsum))
+    _check(st, "tl_pack")
+    return packed[: tl_packed_bytes(M, K) // 4], scale_out, rowsum
+
+
+def tl_validate_packed(packed: np.ndarray, M: int, K: int) -> int:
+    """Host validator: number of invalid codes / non-zero padding weights."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint32)
+    bad = C.c_int64(0)
+    st = _lib.tl_validate_packed(_np_ptr(packed), M, K, C.byref(bad))
+    if st not in (TL_OK, TL_ERR_BAD_VALUE):
+        _check(st, "tl_validate_packed")
+    return int(bad.value)
+
+
+# ---------------------------------------------------------------- device side
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> int | None:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class TernaryWeight:
+    """A packed matrix resident on the device (caller-owned torch tensors)."""
+    packed: "object"   # torch.int32 tensor, tl_packed_bytes(M, K) bytes
+    scale: "object"    # torch.float32 [M]
+    rowsum: "object"   # torch.int32 [M]
+    M: int
+    K: int
+
+    @classmethod
+    def from_host(cls, packed: np.ndarray, scale: np.ndarray, rowsum: np.ndarray, M: int, K: int,
+                  device="cuda") -> "TernaryWeight":
+        torch = _torch()
+        p = torch.from_numpy(np.ascontiguousarray(packed).view(np.int32)).to(device)
+        s = torch.from_numpy(np.ascontiguousarray(scale, dtype=np.float32)).to(device)
+        r = torch.from_numpy(np.ascontiguousarray(rowsum, dtype=np.int32)).to(device)
+        return cls(p, s, r, M, K)
+
+    @classmethod
+    def from_int8(cls, W: np.ndarray, scale: np.ndarray, device="cuda") -> "TernaryWeight":
+        packed, sc, rs = tl_pack(W, scale)
+        return cls.from_host(packed, sc, rs, W.shape[0], W.shape[1], device)
+
+    def struct(self) -> tl_weight:
+        return tl_weight(self.packed.data_ptr(), self.scale.data_ptr(), self.rowsum.data_ptr(),
+                         self.M, self.K, TL_LAYOUT_TL2P_V1)
+
+
+def _structs(ws):
+    arr = (tl_weight * len(ws))()
+    for i, w in enumerate(ws):
+        arr[i] = w.struct() if isinstance(w, TernaryWeight) else w
+    return arr
+
+
+def tl_workspace_bytes(weights, N: int) -> int:
+    ws = weights if isinstance(weights, (list, tuple)) else [weights]
+    return int(_lib.tl_workspace_bytes(_structs(ws), len(ws), N))
+
+
+def make_workspace(weights_lists, N: int, device="cuda"):
+    """Zero-filled workspace large enough for every group in weights_lists."""
+    torch = _torch()
+    need = max(tl_workspace_bytes(w, N) for w in weights_lists)
+    return torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
+
+
+def tl_quantize_act(X, symmetric: bool = False, Q=None, s=None, z=None, stream=None):
+    """bf16 X[N, K] (cuda) -> (int8 Q[N, K], fp32 s[N], int32 z[N])."""
+    torch = _torch()
+    N, K = X.shape
+    if Q is None:
+        Q = torch.empty((N, K), dtype=torch.int8, device=X.device)
+    if s is None:
+        s = torch.empty(N, dtype=torch.float32, device=X.device)
+    if z is None:
+        z = torch.empty(N, dtype=torch.int32, device=X.device)
+    st = _lib.tl_quantize_act(X.data_ptr(), N, K, Q.data_ptr(), s.data_ptr(), z.data_ptr(),
+                              int(bool(symmetric)), _stream_ptr(stream))
+    _check(st, "tl_quantize_act")
+    return Q, s, z
+
+
+_OUT_TORCH = {TL_OUT_F32: "float32", TL_OUT_BF16: "bfloat16", TL_OUT_I32_RAW: "int32"}
+
+
+def tl_linear_group(weights, X, s=None, z=None, outs=None, mode: int = TL_MODE_BF16,
+                    out_dtype: int = TL_OUT_F32, workspace=None, flags: int = 0, stream=None):
+    """Y_g = linear(W_g, X) for matrices sharing X; returns the list of Y_g."""
+    torch = _torch()
+    ws = list(weights)
+    N = X.shape[0]
+    if outs is None:
+        dt = getattr(torch, _OUT_TORCH[out_dtype])
+        outs = [torch.empty((N, w.M), dtype=dt, device=X.device) for w in ws]
+    if workspace is None:
+        workspace = make_workspace([ws], N, device=X.device)
+    ys = (C.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
+    st = _lib.tl_linear_group(_structs(ws), len(ws), X.data_ptr(),
+                              None if s is None else s.data_ptr(),
+                              None if z is None else z.data_ptr(), ys, N, mode, out_dtype,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              flags, _stream_ptr(stream))
+    _check(st, "tl_linear_group")
+    return outs
+
+
+def tl_linear(weight, X, s=None, z=None, out=None, mode: int = TL_MODE_BF16,
+              out_dtype: int = TL_OUT_F32, workspace=None, flags: int = 0, stream=None):
+    """Y = linear(W, X) for one matrix."""
+    torch = _torch()
+    N = X.shape[0]
+    if out is None:
+        dt = getattr(torch, _OUT_TORCH[out_dtype])
+        out = torch.empty((N, weight.M), dtype=dt, device=X.device)
+    if workspace is None:
+        workspace = make_workspace([[weight]], N, device=X.device)
+    w = _structs([weight])
+    st = _lib.tl_linear(w, X.data_ptr(), None if s is None else s.data_ptr(),
+                        None if z is None else z.data_ptr(), out.data_ptr(), N, mode, out_dtype,
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), flags,
+                        _stream_ptr(stream))
+    _check(st, "tl_linear")
+    return out
+
+
+def raw_call(name: str):
+    """The ctypes function of one ABI symbol (for tests of argument checks)."""
+    return getattr(_lib, name)

@@ -1,0 +1,176 @@
+/*
+ * tl.h -- C ABI of the ternary projection linears for B300 (sm_103a).
+ *
+ * The operation (Neutrino-1 pages):
+ *   every projection weight is one of {-1, 0, +1} (blog "Neutrino-1:
+ *   quantization is a training decision", "What's actually ternary"), a
+ *   linear multiplies the signed sum of its inputs by a scale ("state times
+ *   scale", same section), there is one scale and one row sum per output row
+ *   ("Neutrino-1 8B" model page, "Architecture": per-row metadata holds "row
+ *   dimensions, scales, and row sums"), and the weights stay packed at rest
+ *   and are decoded inside the matrix kernel (model page, "Overview").
+ *
+ *       y[n, m] = scale[m] * sum_k w[m, k] * x[n, k]
+ *
+ *   TL_MODE_BF16 (mode A): x is bf16, products are exact, sums are fp32.
+ *   TL_MODE_I8   (mode B): x was quantised per token by tl_quantize_act into
+ *       int8 q with step s[n] and zero point z[n]; acc = sum_k w*q is exact
+ *       (int32) and y = ((float)(acc - z[n]*rowsum[m]) * s[n]) * scale[m].
+ *
+ * Batch sizes: 1 <= N <= 8 is the decode / speculative-verify path (one
+ * token plus up to seven drafted ones verified "in one batched pass", wiki
+ * "Neutrino-1", "What is actually new"); every token's result is bitwise
+ * independent of N.  9 <= N < 256 runs as chunks of 8.  N >= 256 is the
+ * prefill-sized dense contraction on the tensor cores (tcgen05).
+ *
+ * Conventions for every call:
+ *   - The caller owns all buffers.  The library never allocates or frees
+ *     device memory and keeps no state except cached device attributes.
+ *   - "device" pointers are CUDA global memory of the current device; "host"
+ *     pointers are ordinary process memory.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Argument errors are returned before anything
+ *     is launched; a failed launch returns TL_ERR_CUDA.  Faults inside a
+ *     kernel surface at the caller's next synchronisation.
+ *   - Nothing aborts or throws across the ABI.
+ *   - Row-major everywhere: X is [N][K], Y is [N][M].
+ *
+ * Packed weight format "TL2P v1" (the pages' own format is unpublished; this
+ * is the library's own):
+ *   W[M][K] is padded with zero weights to Mp = ceil(M/16)*16 rows and
+ *   Kp = ceil(K/128)*128 columns and cut into 16 x 128 tiles of 512 bytes;
+ *   tile (r, b) starts at byte (r * Kp/128 + b) * 512.  In a tile, lane
+ *   L = 4g + t (g < 8, t < 4) owns the 16 bytes at 16L.  Weight (i, c) of the
+ *   tile (row i < 16, column c < 128) has g = i%8, h = i/8, s = c/16,
+ *   cc = c%16, u = cc/8, t = (cc%8)/2, e = cc%2, f = 2u+h; it lives in word
+ *   j = s/2 of lane 4g+t, slot q = 4*(s%2)+f, at bits (15-2q, 14-2q) when
+ *   e == 0 and (31-2q, 30-2q) when e == 1.  The high bit of the pair is the
+ *   sign, the low bit marks non-zero: 00 -> 0, 01 -> +1, 11 -> -1; 10 is
+ *   never written.  Size: tl_packed_bytes(M, K) = Mp * Kp / 4 bytes.
+ */
+#ifndef TL_H
+#define TL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TL_API __attribute__((visibility("default")))
+#else
+#define TL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TL_OK = 0,
+    TL_ERR_NULL = 1,        /* a required pointer is NULL */
+    TL_ERR_SHAPE = 2,       /* M, K, N, G out of range */
+    TL_ERR_ALIGN = 3,       /* packed not 16-byte aligned, or an element pointer misaligned */
+    TL_ERR_BAD_VALUE = 4,   /* tl_pack: a weight outside {-1, 0, 1}; tl_validate: bad codes */
+    TL_ERR_MODE = 5,        /* unknown mode / output type, or a combination that does not exist */
+    TL_ERR_UNSUPPORTED = 6, /* layout tag not TL2P v1, or no device of compute capability 10.3 */
+    TL_ERR_CUDA = 7,        /* a CUDA runtime call failed */
+    TL_ERR_TIMEOUT = 8,     /* a bounded device-side wait gave up */
+    TL_ERR_WORKSPACE = 9    /* workspace NULL or smaller than tl_workspace_bytes() */
+} tl_status;
+
+enum { TL_MODE_BF16 = 0, TL_MODE_I8 = 1 };
+enum { TL_OUT_F32 = 0, TL_OUT_BF16 = 1, TL_OUT_I32_RAW = 2 };
+
+/* tl_linear flags */
+#define TL_FLAG_PDL 1u  /* launch with programmatic dependent launch: the kernel
+                           may start, and begin streaming weights, before the
+                           previous kernel on the stream has finished.  Only set
+                           it when that previous kernel does not write this call's
+                           weights, scales or row sums (it may write X). */
+
+#define TL_LAYOUT_TL2P_V1 1u
+#define TL_MAX_GROUP 4
+#define TL_MAX_K (1 << 20)
+#define TL_MAX_M (1 << 24)
+
+/* One packed ternary matrix, all pointers device memory owned by the caller. */
+typedef struct {
+    const uint32_t *packed; /* TL2P v1 words, tl_packed_bytes(M, K) bytes, 16-byte aligned */
+    const float *scale;     /* [M] fp32 per-row scale */
+    const int32_t *rowsum;  /* [M] int32 sum_k w[m,k]; required in mode B, ignored in mode A */
+    int32_t M, K;           /* logical rows (outputs) and columns (inputs) */
+    uint32_t layout;        /* TL_LAYOUT_TL2P_V1 */
+} tl_weight;
+
+/* Bytes of the TL2P v1 image of an M x K matrix (0 if M or K < 1). */
+TL_API size_t tl_packed_bytes(int64_t M, int64_t K);
+
+/* HOST.  Pack int8 W[M][K] (row-major, values in {-1, 0, 1}) into `packed`
+ * (tl_packed_bytes(M, K) bytes, written completely, padding zero), compute
+ * rowsum[m] = sum_k W[m][k] and copy scale_in[M] to scale_out[M] (either
+ * scale pointer may be NULL to skip the copy).  Returns TL_ERR_BAD_VALUE,
+ * and leaves the outputs unspecified, if any weight lies outside {-1, 0, 1}.
+ * Cite: model page "Architecture" (per-row scales and row sums).  Uses all
+ * host cores for large matrices. */
+TL_API tl_status tl_pack(const int8_t *W, int64_t M, int64_t K, const float *scale_in,
+                  uint32_t *packed, float *scale_out, int32_t *rowsum);
+
+/* HOST.  Check a TL2P v1 image: *bad_codes receives the number of 10 codes
+ * plus non-zero padding weights (NULL allowed).  TL_OK iff that is 0. */
+TL_API tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K,
+                             int64_t *bad_codes);
+
+/* Device workspace needed by tl_linear / tl_linear_group for these shapes
+ * and this N (all matrices in Ws share K).  The workspace holds split-K
+ * partial sums and per-row-tile counters.  It must be zero-filled before its
+ * first use; every call leaves it zero-filled again when it completes.  One
+ * workspace may serve any sequence of calls on one stream, but calls that
+ * overlap on the GPU must not share it. */
+TL_API size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N);
+
+/* DEVICE.  Per-token activation quantisation (bf16 -> int8).  X_bf16 [N][K]
+ * (2-byte aligned), Q [N][K] int8, s [N] fp32, z [N] int32.
+ *   symmetric == 0: lo = min(0, min x), hi = max(0, max x),
+ *       s = (hi - lo) / 255, z = -128 - rint(lo / s),
+ *       q = clamp(rint(x / s) + z, -128, 127); an all-zero token gets s = 1,
+ *       z = 0, q = 0.
+ *   symmetric != 0: s = max|x| / 127 (1 if that is 0), z = 0,
+ *       q = clamp(rint(x / s), -127, 127).
+ * fp32 arithmetic with IEEE division and round-half-to-even.  The pages are
+ * silent on activation quantisation; this is the library's reading. */
+TL_API tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, float *s,
+                          int32_t *z, int symmetric, void *stream);
+
+/* DEVICE.  Y = linear(W, X) for one matrix.
+ *   mode TL_MODE_BF16: X is bf16 [N][K]; s, z ignored (may be NULL).
+ *   mode TL_MODE_I8:   X is int8 [N][K] from tl_quantize_act; s, z [N] required;
+ *                      W->rowsum required.
+ *   out_dtype: TL_OUT_F32 (fp32 Y), TL_OUT_BF16 (bf16 Y, round to nearest
+ *              even of the fp32 result), TL_OUT_I32_RAW (mode B only: the
+ *              exact int32 acc = sum_k w*q, before any correction).
+ *   workspace: device, >= tl_workspace_bytes(W, 1, N) bytes, 256-byte aligned.
+ *   flags: 0 or TL_FLAG_PDL.
+ * Y must not alias X.  Deterministic: the same call gives the same bits. */
+TL_API tl_status tl_linear(const tl_weight *W, const void *X, const float *s, const int32_t *z,
+                    void *Y, int N, int mode, int out_dtype, void *workspace,
+                    size_t workspace_bytes, unsigned flags, void *stream);
+
+/* DEVICE.  G (1..TL_MAX_GROUP) matrices that read the same X (q/k/v, or
+ * gate/up) in one launch; Ys[g] is [N][Ws[g].M].  Every Ws[g].K must be
+ * equal.  Each Ys[g] equals what tl_linear(&Ws[g], ...) would write.
+ * `Ws` and `Ys` are host arrays of G entries. */
+TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float *s,
+                          const int32_t *z, void *const *Ys, int N, int mode,
+                          int out_dtype, void *workspace, size_t workspace_bytes,
+                          unsigned flags, void *stream);
+
+/* Static, never NULL. */
+TL_API const char *tl_status_string(tl_status status);
+
+/* Library version, e.g. 100 for 0.1.0. */
+TL_API int tl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_H */

@@ -1,0 +1,259 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Mode B (int8 activations) must match bit for bit; mode A (bf16 activations,
+fp32 sums) within 1e-3 of the oracle, relative to max(|y_ref|, 1e-2 * rms of
+the token's outputs).  Every token's result must not depend on the batch.
+"""
+import numpy as np
+import pytest
+
+from bit_matvec_ternary_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU machine
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from bit_matvec_ternary_b300 import tl  # noqa: E402
+
+TOL_A = 1e-3
+
+
+def rel_err(y, ref):
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    den = np.maximum(np.abs(ref), 1e-2 * np.maximum(rms, 1e-30))
+    return float(np.max(np.abs(y - ref) / den)) if y.size else 0.0
+
+
+def bf16_tensor(bits: np.ndarray):
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def case(M, K, seed, p0=0.626):
+    W = synth.ternary(M, K, p0, seed)
+    scale = synth.scales(M, seed)
+    return W, scale
+
+
+class Mat:
+    def __init__(self, oracle_mod, M, K, seed, p0=0.626, W=None):
+        if W is None:
+            W, scale = case(M, K, seed, p0)
+        else:
+            scale = synth.scales(M, seed)
+        self.W, self.scale, self.M, self.K = W, scale, M, K
+        self.P = oracle_mod.pack(W)
+        self.rowsum = oracle_mod.rowsum(self.P, M, K)
+        self.dev = tl.TernaryWeight.from_int8(W, scale)
+
+
+def oracle_b(oracle_mod, m, X):
+    Q, s, z = oracle_mod.quant(X)
+    acc, Y = oracle_mod.linear_b(m.P, m.scale, m.rowsum, m.M, m.K, Q, s, z)
+    return Q, s, z, acc, Y
+
+
+def gpu_b(m, X, out_dtype=tl.TL_OUT_F32, symmetric=False):
+    Q, s, z = tl.tl_quantize_act(bf16_tensor(X), symmetric=symmetric)
+    Y = tl.tl_linear(m.dev, Q, s, z, mode=tl.TL_MODE_I8, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return Q, s, z, Y
+
+
+CONFIG_SHAPES = [(2048, 1024), (1024, 1024), (1024, 2048), (3072, 1024), (1024, 3072),
+                 (4096, 4096), (1024, 4096), (4096, 12288)]
+RAGGED = [(5, 37), (17, 129), (100, 1000), (33, 4099), (1, 1), (16, 128), (777, 333)]
+
+
+@pytest.mark.parametrize("M,K", CONFIG_SHAPES + RAGGED)
+@pytest.mark.parametrize("N", [1, 8])
+def test_mode_a_parity(oracle_mod, M, K, N):
+    m = Mat(oracle_mod, M, K, seed=M + 7 * K)
+    X = synth.activations(N, K, seed=N + K)
+    ref = oracle_mod.linear_a(m.P, m.scale, M, K, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert Y.shape == ref.shape
+    assert rel_err(Y, ref) <= TOL_A
+
+
+@pytest.mark.parametrize("N", [2, 3, 5, 6, 7])
+def test_mode_a_parity_other_batches(oracle_mod, N):
+    m = Mat(oracle_mod, 2048, 1024, seed=0)
+    X = synth.activations(N, 1024, seed=3, outlier_frac=0.01)
+    ref = oracle_mod.linear_a(m.P, m.scale, 2048, 1024, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert rel_err(Y, ref) <= TOL_A
+
+
+@pytest.mark.parametrize("M,K", CONFIG_SHAPES + RAGGED)
+@pytest.mark.parametrize("N", [1, 8])
+def test_mode_b_bit_exact(oracle_mod, M, K, N):
+    m = Mat(oracle_mod, M, K, seed=3 * M + K)
+    X = synth.activations(N, K, seed=2 * N + K, outlier_frac=0.01)
+    Qr, sr, zr, accr, Yr = oracle_b(oracle_mod, m, X)
+    Q, s, z, Y = gpu_b(m, X)
+    assert np.array_equal(Q.cpu().numpy(), Qr)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(z.cpu().numpy(), zr)
+    assert np.array_equal(Y.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+    acc = tl.tl_linear(m.dev, Q, s, z, mode=tl.TL_MODE_I8, out_dtype=tl.TL_OUT_I32_RAW)
+    assert np.array_equal(acc.cpu().numpy(), accr)
+
+
+def test_mode_b_bf16_output_is_rne_of_oracle(oracle_mod):
+    m = Mat(oracle_mod, 1024, 4096, seed=5)
+    X = synth.activations(8, 4096, seed=5)
+    *_, Yr = oracle_b(oracle_mod, m, X)
+    *_, Y = gpu_b(m, X, out_dtype=tl.TL_OUT_BF16)
+    got = Y.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, oracle_mod.bf16_rne(Yr))
+
+
+def test_mode_a_bf16_output(oracle_mod):
+    m = Mat(oracle_mod, 3072, 1024, seed=6)
+    X = synth.activations(4, 1024, seed=6)
+    ref = oracle_mod.linear_a(m.P, m.scale, 3072, 1024, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X), out_dtype=tl.TL_OUT_BF16).float().cpu().numpy()
+    assert rel_err(Y, ref) <= TOL_A + 2.0 ** -8
+
+
+@pytest.mark.parametrize("K", [1, 7, 128, 1000, 4096, 12288])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_quantizer_bit_exact(oracle_mod, K, symmetric):
+    X = synth.activations(8, K, seed=K, outlier_frac=0.01 if K >= 100 else 0.0)
+    X[3] = 0                                # an all-zero token
+    if K > 5:
+        X[5, :] = synth.to_bf16_bits(-np.abs(synth.bf16_bits_to_f32(X[5])))  # all <= 0
+    Qr, sr, zr = oracle_mod.quant(X, symmetric=symmetric)
+    Q, s, z = tl.tl_quantize_act(bf16_tensor(X), symmetric=symmetric)
+    torch.cuda.synchronize()
+    assert np.array_equal(Q.cpu().numpy(), Qr)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+    assert np.array_equal(z.cpu().numpy(), zr)
+
+
+@pytest.mark.parametrize("mode", [tl.TL_MODE_BF16, tl.TL_MODE_I8])
+@pytest.mark.parametrize("M,K", [(4096, 4096), (1024, 12288), (777, 333)])
+def test_batch_invariance(oracle_mod, mode, M, K):
+    """Each token's row at N=8 is bitwise the N=1 result for that token."""
+    m = Mat(oracle_mod, M, K, seed=11)
+    X = bf16_tensor(synth.activations(8, K, seed=12, outlier_frac=0.01))
+    if mode == tl.TL_MODE_BF16:
+        Y8 = tl.tl_linear(m.dev, X)
+        singles = [tl.tl_linear(m.dev, X[n:n + 1].contiguous()) for n in range(8)]
+    else:
+        Q, s, z = tl.tl_quantize_act(X)
+        Y8 = tl.tl_linear(m.dev, Q, s, z, mode=mode)
+        singles = [tl.tl_linear(m.dev, Q[n:n + 1].contiguous(), s[n:n + 1].contiguous(),
+                                z[n:n + 1].contiguous(), mode=mode) for n in range(8)]
+    torch.cuda.synchronize()
+    Y8 = Y8.cpu().numpy().view(np.uint32)
+    for n in range(8):
+        assert np.array_equal(Y8[n], singles[n].cpu().numpy().view(np.uint32)[0]), n
+
+
+def test_deterministic_across_runs(oracle_mod):
+    m = Mat(oracle_mod, 12288, 4096, seed=13)
+    X = bf16_tensor(synth.activations(8, 4096, seed=14))
+    a = tl.tl_linear(m.dev, X).cpu().numpy()
+    b = tl.tl_linear(m.dev, X).cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", [tl.TL_MODE_BF16, tl.TL_MODE_I8])
+def test_group_equals_single_calls(oracle_mod, mode):
+    mats = [Mat(oracle_mod, M, 4096, seed=20 + i) for i, M in enumerate((4096, 1024, 1024))]
+    X = bf16_tensor(synth.activations(3, 4096, seed=21))
+    if mode == tl.TL_MODE_I8:
+        Q, s, z = tl.tl_quantize_act(X)
+        ys = tl.tl_linear_group([m.dev for m in mats], Q, s, z, mode=mode)
+        singles = [tl.tl_linear(m.dev, Q, s, z, mode=mode) for m in mats]
+    else:
+        ys = tl.tl_linear_group([m.dev for m in mats], X)
+        singles = [tl.tl_linear(m.dev, X) for m in mats]
+    Xh = X.cpu().view(torch.int16).numpy().view(np.uint16)
+    for m, y, y1 in zip(mats, ys, singles):
+        ref = oracle_mod.linear_a(m.P, m.scale, m.M, m.K, Xh)
+        if mode == tl.TL_MODE_BF16:
+            assert rel_err(y.cpu().numpy(), ref) <= TOL_A
+        else:
+            *_, Yr = oracle_b(oracle_mod, m, Xh)
+            assert np.array_equal(y.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+            assert np.array_equal(y1.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+
+
+@pytest.mark.parametrize("N", [9, 12, 20])
+def test_batches_above_eight_run_in_chunks(oracle_mod, N):
+    m = Mat(oracle_mod, 1024, 3072, seed=30)
+    X = synth.activations(N, 3072, seed=31)
+    ref = oracle_mod.linear_a(m.P, m.scale, 1024, 3072, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert rel_err(Y, ref) <= TOL_A
+    *_, Yr = oracle_b(oracle_mod, m, X)
+    *_, Yb = gpu_b(m, X)
+    assert np.array_equal(Yb.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+
+
+def test_zero_rows_and_one_hot(oracle_mod):
+    M, K = 300, 2048
+    W, _ = case(M, K, 40)
+    W[17] = 0
+    W[299] = 0
+    m = Mat(oracle_mod, M, K, seed=40, W=W)
+    X = synth.activations(8, K, seed=41)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert np.all(Y[:, 17] == 0) and np.all(Y[:, 299] == 0)
+    oh = np.zeros((1, K), dtype=np.float32)
+    oh[0, 1234] = 3.0
+    Y1 = tl.tl_linear(m.dev, bf16_tensor(synth.to_bf16_bits(oh))).cpu().numpy()
+    expect = (m.scale.astype(np.float64) * W[:, 1234] * 3.0).astype(np.float32)
+    assert np.array_equal(Y1[0], expect)
+
+
+@pytest.mark.parametrize("sign", [1, -1])
+def test_adversarial_extreme_sums_stay_exact(oracle_mod, sign):
+    """All weights +-1 and activations at the quantiser's extremes: the
+    largest |acc| the path can meet (128 * K) must come out exact."""
+    M, K = 64, 12288
+    W = np.full((M, K), sign, dtype=np.int8)
+    W[1::2] = -sign
+    m = Mat(oracle_mod, M, K, seed=50, W=W)
+    x = np.full((2, K), -1.0, dtype=np.float32)
+    x[:, 0] = 1e-3                          # lo = -1, hi ~ 0: q = -128 almost everywhere
+    X = synth.to_bf16_bits(x)
+    Qr, sr, zr, accr, Yr = oracle_b(oracle_mod, m, X)
+    assert np.abs(accr).max() >= 128 * (K - 1)
+    Q, s, z, Y = gpu_b(m, X)
+    acc = tl.tl_linear(m.dev, Q, s, z, mode=tl.TL_MODE_I8, out_dtype=tl.TL_OUT_I32_RAW)
+    assert np.array_equal(acc.cpu().numpy(), accr)
+    assert np.array_equal(Y.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+    ref = oracle_mod.linear_a(m.P, m.scale, M, K, X)
+    Ya = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert rel_err(Ya, ref) <= TOL_A
+
+
+def test_workspace_is_left_zeroed(oracle_mod):
+    m = Mat(oracle_mod, 4096, 4096, seed=60)
+    X = bf16_tensor(synth.activations(8, 4096, seed=61))
+    ws = tl.make_workspace([[m.dev]], 8)
+    for _ in range(3):
+        tl.tl_linear(m.dev, X, workspace=ws)
+    torch.cuda.synchronize()
+    nbytes = tl.tl_workspace_bytes([m.dev], 8)
+    R = (4096 + 15) // 16
+    assert int(ws[: 4 * R].count_nonzero()) == 0
+    assert nbytes <= ws.numel()
+
+
+def test_pdl_flag_gives_identical_results(oracle_mod):
+    m = Mat(oracle_mod, 4096, 4096, seed=70)
+    X = bf16_tensor(synth.activations(8, 4096, seed=71))
+    a = tl.tl_linear(m.dev, X)
+    b = tl.tl_linear(m.dev, X, flags=tl.TL_FLAG_PDL)
+    c = tl.tl_linear(m.dev, X, flags=tl.TL_FLAG_PDL)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(a.view(torch.int32), c.view(torch.int32))
