@@ -27,6 +27,7 @@
 //   deterministic and do not depend on N.
 
 #include "tl.h"
+#include "tl_internal.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,7 +38,7 @@
 
 namespace {
 
-constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
+constexpr int kWarps = 16;            // warps per CTA of the N <= 8 kernel (one CTA per SM)
 constexpr int kThreads = kWarps * 32;
 constexpr int kDepth = 8;             // 128-bit weight loads in flight per lane
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
@@ -108,38 +109,40 @@ __device__ __forceinline__ void griddep_launch() {
 }
 
 // Position of a unit: slice s, row tile r (group-wide), block bp in the slice,
-// and the matrix gi / local row tile rl it belongs to.
+// and the matrix gi / local row tile rl it belongs to.  `p` is this lane's
+// 16 bytes of the unit's TL2P tile; it advances by one tile inside a slice
+// segment and is recomputed only when the segment changes.
 struct Cursor {
-    long long u;
-    int s, r, bp, gi, rl;
+    int u, s, r, bp, gi, rl;
+    const char *p;
 
-    __device__ void seek(const GroupArgs &a, long long u0) {
+    __device__ void seek(const GroupArgs &a, int u0, int lane) {
         u = u0;
-        const long long su = (long long)a.R * a.KS;
-        s = (int)(u0 / su);
-        const long long rem = u0 - (long long)s * su;
-        r = (int)(rem / a.KS);
-        bp = (int)(rem - (long long)r * a.KS);
+        const int su = a.R * a.KS;
+        s = u0 / su;
+        const int rem = u0 - s * su;
+        r = rem / a.KS;
+        bp = rem - r * a.KS;
         gi = 0;
         while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
         rl = r - a.rt_off[gi];
+        p = a.packed[gi] + ((long long)rl * a.KB + (long long)s * a.KS + bp) * 512 + lane * 16;
     }
-    __device__ __forceinline__ void next(const GroupArgs &a) {
+    __device__ __forceinline__ void next(const GroupArgs &a, int lane) {
         ++u;
-        if (++bp == a.KS) {
-            bp = 0;
-            if (++r == a.R) {
-                r = 0; ++s; gi = 0; rl = 0;
-            } else if (r == a.rt_off[gi + 1]) {
-                ++gi; rl = 0;
-            } else {
-                ++rl;
-            }
+        if (++bp < a.KS) {
+            p += 512;
+            return;
         }
-    }
-    __device__ __forceinline__ const char *ptr(const GroupArgs &a, int lane) const {
-        const long long tile = (long long)rl * a.KB + (long long)s * a.KS + bp;
-        return a.packed[gi] + tile * 512 + lane * 16;
+        bp = 0;
+        if (++r == a.R) {
+            r = 0; ++s; gi = 0; rl = 0;
+        } else if (r == a.rt_off[gi + 1]) {
+            ++gi; rl = 0;
+        } else {
+            ++rl;
+        }
+        p = a.packed[gi] + ((long long)rl * a.KB + (long long)s * a.KS) * 512 + lane * 16;
     }
 };
 
@@ -226,29 +229,29 @@ __device__ __noinline__ void flush_piece(const GroupArgs &a, int r, int s, int p
     if (lane == 0) a.cnt[r] = 0;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     extern __shared__ uint4 xs[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
 
     const long long v = (long long)blockIdx.x * kWarps + warp;
-    const long long u0 = bnd(a, v), u1 = bnd(a, v + 1);
-    const long long cu0 = bnd(a, (long long)blockIdx.x * kWarps);
-    const long long cu1 = bnd(a, (long long)(blockIdx.x + 1) * kWarps);
-    const long long su = (long long)a.R * a.KS;
-    const int s_lo = (int)(cu0 / su);
-    const int n_sl = cu1 > cu0 ? (int)((cu1 - 1) / su) - s_lo + 1 : 0;
+    const int u0 = (int)bnd(a, v), u1 = (int)bnd(a, v + 1);
+    const int cu0 = (int)bnd(a, (long long)blockIdx.x * kWarps);
+    const int cu1 = (int)bnd(a, (long long)(blockIdx.x + 1) * kWarps);
+    const int su = a.R * a.KS;
+    const int s_lo = cu0 / su;
+    const int n_sl = cu1 > cu0 ? (cu1 - 1) / su - s_lo + 1 : 0;
 
     // Weights do not depend on the previous kernel: start streaming them
     // before waiting for it.
     uint4 ring[kDepth];
     Cursor pf;
-    pf.seek(a, u0);
+    pf.seek(a, u0, lane);
 #pragma unroll
     for (int i = 0; i < kDepth; ++i) {
-        if (pf.u < u1) ring[i] = ldg_stream(pf.ptr(a, lane));
-        pf.next(a);
+        if (pf.u < u1) ring[i] = ldg_stream(pf.p);
+        pf.next(a, lane);
     }
     griddep_wait();
     griddep_launch();
@@ -258,15 +261,15 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     // with k = ((s_lo+sl)*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
     {
         const int N = a.N;
-        const long long words = (long long)n_sl * a.KS * 64 * N;
+        const int words = n_sl * a.KS * 64 * N;
         uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
-        for (long long idx = threadIdx.x; idx < words; idx += kThreads) {
-            const int w = (int)(idx & 3), tt = (int)((idx >> 2) & 3);
-            long long rest = idx >> 4;
-            const int n = (int)(rest % N); rest /= N;
-            const int qd = (int)(rest & 3); rest >>= 2;
-            const int bp = (int)(rest % a.KS);
-            const int sl = (int)(rest / a.KS);
+        for (int idx = threadIdx.x; idx < words; idx += kThreads) {
+            const int w = idx & 3, tt = (idx >> 2) & 3;
+            int rest = idx >> 4;
+            const int n = rest % N; rest /= N;
+            const int qd = rest & 3; rest >>= 2;
+            const int bp = rest % a.KS;
+            const int sl = rest / a.KS;
             const int k = ((s_lo + sl) * a.KS + bp) * 128 + 16 * (2 * qd + (w >> 1)) + 2 * tt +
                           8 * (w & 1);
             uint32_t lo = 0, hi = 0;
@@ -286,41 +289,52 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
 
     const uint32_t M2 = 0xC000C000u;
     const bool xlane = g < a.N;
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int xstride = 4 * a.N * 4;            // uint4 per 128-column block
+    // four independent accumulator chains (one per 32-column quarter)
+    float c[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
     Cursor cc;
-    cc.seek(a, u0);
+    cc.seek(a, u0, lane);
     int piece_p = cc.bp == 0 ? 0 : 1;
     int piece_nk = 0;
+    const uint4 *xb = xs + ((cc.s - s_lo) * a.KS + cc.bp) * xstride + g * 4 + t;
 
-    for (long long base = u0; base < u1; base += kDepth) {
+    for (int base = u0; base < u1; base += kDepth) {
 #pragma unroll
         for (int i = 0; i < kDepth; ++i) {
             if (base + i < u1) {
                 const uint4 w = ring[i];
-                if (pf.u < u1) ring[i] = ldg_stream(pf.ptr(a, lane));
-                pf.next(a);
-
-                const uint4 *xb = xs + ((long long)((cc.s - s_lo) * a.KS + cc.bp) * 4 * a.N + g) * 4 + t;
+                if (pf.u < u1) ring[i] = ldg_stream(pf.p);
+                pf.next(a, lane);
 #pragma unroll
                 for (int qd = 0; qd < 4; ++qd) {
                     const uint32_t word = qd == 0 ? w.x : qd == 1 ? w.y : qd == 2 ? w.z : w.w;
                     uint4 b = make_uint4(0u, 0u, 0u, 0u);
                     if (xlane) b = xb[qd * a.N * 4];
-                    mma_bf16_16816(c, word & M2, (word << 2) & M2, (word << 4) & M2,
+                    mma_bf16_16816(c[qd], word & M2, (word << 2) & M2, (word << 4) & M2,
                                    (word << 6) & M2, b.x, b.y);
-                    mma_bf16_16816(c, (word << 8) & M2, (word << 10) & M2, (word << 12) & M2,
-                                   (word << 14) & M2, b.z, b.w);
+                    mma_bf16_16816(c[qd], (word << 8) & M2, (word << 10) & M2,
+                                   (word << 12) & M2, (word << 14) & M2, b.z, b.w);
                 }
                 ++piece_nk;
                 const bool seg_end = (cc.bp == a.KS - 1) || (base + i + 1 == u1);
                 if (seg_end) {
-                    flush_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane, c[0], c[1],
-                                c[2], c[3]);
-                    c[0] = c[1] = c[2] = c[3] = 0.f;
+                    flush_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane,
+                                (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]),
+                                (c[0][1] + c[1][1]) + (c[2][1] + c[3][1]),
+                                (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]),
+                                (c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
                     piece_p = 0;
                     piece_nk = 0;
                 }
-                cc.next(a);
+                cc.next(a, lane);
+                if (cc.bp == 0)
+                    xb = xs + ((cc.s - s_lo) * a.KS) * xstride + g * 4 + t;
+                else
+                    xb += xstride;
             }
         }
     }
@@ -411,6 +425,8 @@ tl_status device_info(DeviceInfo **out) {
             if (cudaFuncSetAttribute(tl_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)kSmemLimit) != cudaSuccess)
                 return TL_ERR_CUDA;
+            const tl_status pst = tl_internal::prefill_init_device();
+            if (pst != TL_OK) return pst;
             d.sms = sms;
             d.init = 1;
         }
@@ -436,7 +452,7 @@ void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     for (int g = 0; g < G; ++g) p->R += (int)ceil_div(Ms[g], 16);
     p->KB = (int)ceil_div(K, 128);
     p->U = (long long)p->R * p->KB;
-    long long ctas = sms;                       // one CTA of 8 warps per SM
+    long long ctas = sms;                       // one CTA of kWarps warps per SM
     ctas = std::min<long long>(ctas, ceil_div(p->U, (long long)kWarps * 2));
     if (ctas < 1) ctas = 1;
     p->P = (int)ctas;
@@ -460,7 +476,7 @@ void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     const int n = std::min(std::max(N, 1), kNMax);
     p->smem = (size_t)n_sl * p->KS * 128 * n * 2;
     const size_t cnt_bytes = ((size_t)p->R * 4 + 255) / 256 * 256;
-    p->ws_bytes = cnt_bytes + (size_t)p->R * p->S * 2 * 16 * n * 4;
+    p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * p->S * 2 * 16 * n * 4;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -484,8 +500,12 @@ tl_status check_weights(const tl_weight *Ws, int G, int mode) {
 size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
     int Ms[TL_MAX_GROUP];
     for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
+    const int K = Ws[0].K;
+    if (tl_internal::prefill_supported(N, K))
+        return std::max(tl_internal::prefill_workspace_bytes(N, K, TL_MODE_BF16),
+                        tl_internal::prefill_workspace_bytes(N, K, TL_MODE_I8));
     Plan p;
-    make_plan(Ms, G, Ws[0].K, N, sms, &p);
+    make_plan(Ms, G, K, N, sms, &p);
     return p.ws_bytes;
 }
 
@@ -510,7 +530,7 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     }
     Plan p;
     make_plan(Ms, G, K, n, dev.sms, &p);
-    if (p.smem > kSmemLimit) return TL_ERR_SHAPE;
+    if (p.smem > kSmemLimit || p.U >= (1ll << 31)) return TL_ERR_SHAPE;
     if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
     a.R = p.R; a.KB = p.KB; a.KS = p.KS; a.S = p.S; a.K = K; a.U = p.U; a.V = p.V;
     const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
@@ -519,8 +539,9 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     a.z = z ? z + n0 : nullptr;
     a.N = n; a.mode = mode; a.out = out;
     const size_t cnt_bytes = ((size_t)p.R * 4 + 255) / 256 * 256;
-    a.cnt = static_cast<int *>(ws);
-    a.part = reinterpret_cast<float *>(static_cast<char *>(ws) + cnt_bytes);
+    char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
+    a.cnt = reinterpret_cast<int *>(wsb);
+    a.part = reinterpret_cast<float *>(wsb + cnt_bytes);
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -589,6 +610,11 @@ tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float
     st = device_info(&dev);
     if (st != TL_OK) return st;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (tl_internal::prefill_supported(N, Ws[0].K)) {
+        if (mode == TL_MODE_BF16 && !aligned(X, 16)) return TL_ERR_ALIGN;
+        return tl_internal::launch_prefill(Ws, G, X, s, z, Ys, N, mode, out_dtype, workspace,
+                                           workspace_bytes, flags, cs);
+    }
     for (int n0 = 0; n0 < N; n0 += kNMax) {
         const int n = N - n0 < kNMax ? N - n0 : kNMax;
         st = launch_chunk(Ws, G, X, s, z, Ys, n0, n, mode, out_dtype, workspace,

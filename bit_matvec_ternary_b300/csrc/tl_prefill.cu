@@ -1,0 +1,475 @@
+// tl_prefill.cu -- the prefill-sized dense contraction (N >= 256 tokens) on
+// the sm_103a tensor cores (tcgen05.mma, accumulator in TMEM).
+//
+// Same definition as the decode path, y[n,m] = scale[m] * sum_k w[m,k] x[n,k]
+// (blog "Neutrino-1: quantization is a training decision", "What's actually
+// ternary"), with the weights still packed at rest and decoded on chip
+// (model page "Neutrino-1 8B", "Overview"): the packed TL2P tiles are loaded
+// into registers, expanded to bf16 +-2.0 / 0 and written into shared memory
+// in the 128-byte-swizzled K-major layout the tensor core reads, so no
+// bf16 copy of a weight ever reaches global memory.
+//
+// One CTA computes a 128-row x 256-token tile of Y:
+//   warp 0      TMA producer: activation tiles X[256 tokens][64 k] (bf16)
+//   warp 1      TMEM owner and MMA issuer (one elected lane)
+//   warps 2..5  weight decoders during the K loop, then the epilogue
+//               (TMEM -> registers -> scale -> global)
+// STAGES-deep ring of (A, B) shared-memory stages guarded by mbarriers.
+// Every wait is bounded: after ~2^31 SM cycles the CTA records
+// TL_DEVERR_TIMEOUT in the workspace status word, stops issuing work, waits
+// (again bounded) for its own copies in flight, frees TMEM and exits.
+//
+// Mode B (int8 activations) feeds q as bf16, which is exact, so the fp32
+// accumulator holds the exact integer 2 * sum_k w*q (|.| < 2^24).
+
+#include "tl.h"
+#include "tl_internal.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+
+namespace tlp {
+
+constexpr int BM = 128;               // weight rows per CTA (TMEM lanes)
+constexpr int BN = 256;               // tokens per CTA (TMEM columns)
+constexpr int BK = 64;                // k per stage (one 128-byte swizzle row)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int DEC_WARPS = 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr long long WAIT_LIMIT = 1ll << 31;   // SM cycles
+
+struct PrefillArgs {
+    const char *packed[TL_MAX_GROUP];
+    const float *scale[TL_MAX_GROUP];
+    const int32_t *rowsum[TL_MAX_GROUP];
+    void *Y[TL_MAX_GROUP];
+    int M[TL_MAX_GROUP];
+    int mt_off[TL_MAX_GROUP + 1];   // 128-row tiles, prefix over the group
+    int G;
+    int KB;                          // 128-column TL2P blocks
+    int N;
+    int mode, out;
+    const float *s;
+    const int32_t *z;
+    int *status;                     // workspace status word
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait; returns false (and records the timeout) when it gives up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
+    if (mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (clock64() - t0 > WAIT_LIMIT) {
+            atomicExch(status, TL_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    // K-major operand, 128-byte swizzle: rows of 128 B, 8-row atoms of 1024 B.
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)(1024u >> 4) << 32;              // stride between 8-row atoms
+    d |= (uint64_t)1 << 46;                          // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                          // SWIZZLE_128B
+    return d;
+}
+
+// kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = 256.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(IDESC), "r"(accum));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Write the decoded half (64 columns) of one 16-row TL2P tile into the A stage.
+// The lane holds rows g, g+8 of row tile `rt`; word pair (w0, w1) covers
+// the four 16-column steps of this half.
+__device__ __forceinline__ void store_half(uint8_t *a_stage, int rt, int g, int t, uint32_t w0,
+                                           uint32_t w1) {
+    const uint32_t M2 = 0xC000C000u;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint32_t word = (s < 2) ? w0 : w1;
+        const int q0 = 4 * (s & 1);
+#pragma unroll
+        for (int f = 0; f < 4; ++f) {
+            const uint32_t v = (word << (2 * (q0 + f))) & M2;
+            const int row = rt * 16 + g + 8 * (f & 1);
+            const int chunk = 2 * s + (f >> 1);
+            const int off = (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4) + 4 * t;
+            *reinterpret_cast<uint32_t *>(a_stage + off) = v;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap xmap) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    // bars: full_a[S], full_b[S], empty[S], tmem_full; then the TMEM address
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_a = [&](int s) { return bar0 + 8u * s; };
+    auto full_b = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt_global = blockIdx.x;
+    const int nt = blockIdx.y;
+    int gi = 0;
+    while (gi + 1 < a.G && a.mt_off[gi + 1] <= mt_global) ++gi;
+    const int mt = mt_global - a.mt_off[gi];
+    const int KSTEPS = a.KB * 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_a(s), DEC_WARPS);
+            mbar_init(full_b(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"((uint32_t)BN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---------------- activation producer
+        griddep_wait();
+        if (lane == 0) {
+            for (int ks = 0; ks < KSTEPS && ok; ++ks) {
+                const int s = ks % STAGES;
+                const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+                if (!mbar_wait(empty(s), ph ^ 1u, a.status)) { ok = false; break; }
+                mbar_expect_tx(full_b(s), B_BYTES);
+                tma_load_2d(base + s * STAGE_BYTES + A_BYTES, &xmap, ks * BK, nt * BN, full_b(s));
+            }
+            // drain: every copy this lane issued must land before the CTA exits
+            const int issued = ok ? KSTEPS : 0;
+            for (int ks = (issued > STAGES ? issued - STAGES : 0); ks < issued; ++ks)
+                mbar_wait(full_b(ks % STAGES), (uint32_t)(ks / STAGES) & 1u, a.status);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            for (int ks = 0; ks < KSTEPS && ok; ++ks) {
+                const int s = ks % STAGES;
+                const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+                if (!mbar_wait(full_a(s), ph, a.status) || !mbar_wait(full_b(s), ph, a.status)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t a_addr = base + s * STAGE_BYTES;
+                const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_f16(tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                            (ks | kk) != 0);
+                mma_commit(empty(s));
+            }
+            mma_commit(tmem_full);
+        }
+    } else {
+        // ---------------- weight decoders, then the epilogue
+        const int dw = warp - 2;            // row tiles 2dw, 2dw+1 of the 8 in the CTA tile
+        const int g = lane >> 2, t = lane & 3;
+        const int rt_base = mt * 8 + 2 * dw;
+        const int rts = (a.M[gi] + 15) / 16;
+        const char *pk = a.packed[gi];
+        // two TL2P tiles (one per row tile) per 128 columns; prefetch ring of 4
+        constexpr int RING = 4;
+        uint4 ring[RING][2];
+#pragma unroll
+        for (int i = 0; i < RING; ++i)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                ring[i][r] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < a.KB && rt_base + r < rts)
+                    ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + i) * 512 + lane * 16);
+            }
+        for (int kb0 = 0; kb0 < a.KB; kb0 += RING) {
+#pragma unroll
+            for (int i = 0; i < RING; ++i) {
+                const int kb = kb0 + i;
+                if (kb < a.KB) {
+                    const uint4 cur0 = ring[i][0], cur1 = ring[i][1];
+                    const int nb = kb + RING;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+                        if (nb < a.KB && rt_base + r < rts)
+                            ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + nb) * 512 + lane * 16);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int ks = 2 * kb + h;
+                        const int s = ks % STAGES;
+                        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+                        // every lane waits; the warp continues only if all of them got through
+                        ok = __all_sync(0xffffffffu, ok && mbar_wait(empty(s), ph ^ 1u, a.status));
+                        if (ok) {
+                            uint8_t *a_stage = smem + s * STAGE_BYTES;
+                            store_half(a_stage, 2 * dw, g, t, h ? cur0.z : cur0.x, h ? cur0.w : cur0.y);
+                            store_half(a_stage, 2 * dw + 1, g, t, h ? cur1.z : cur1.x, h ? cur1.w : cur1.y);
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(full_a(s));
+                        }
+                    }
+                }
+            }
+        }
+        // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows
+        griddep_wait();
+        const bool got = __all_sync(0xffffffffu, ok && mbar_wait(tmem_full, 0u, a.status));
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (got) {
+            const int q = warp & 3;
+            const int row = mt * BM + 32 * q + lane;
+            const bool row_ok = row < a.M[gi];
+            const float sc = row_ok ? a.scale[gi][row] : 0.f;
+            const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
+            const int Mg = a.M[gi];
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+                if (!row_ok) continue;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = nt * BN + c0 + j;
+                    if (n >= a.N) break;
+                    const float half = __uint_as_float(r[j]) * 0.5f;
+                    float y;
+                    if (a.mode == TL_MODE_BF16) {
+                        y = __fmul_rn(half, sc);
+                    } else {
+                        const int iacc = __float2int_rn(half);
+                        if (a.out == TL_OUT_I32_RAW) {
+                            reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * Mg + row] = iacc;
+                            continue;
+                        }
+                        const int corr = iacc - a.z[n] * rsum;
+                        y = __fmul_rn(__fmul_rn((float)corr, a.s[n]), sc);
+                    }
+                    if (a.out == TL_OUT_F32)
+                        reinterpret_cast<float *>(a.Y[gi])[(long long)n * Mg + row] = y;
+                    else
+                        reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * Mg + row] =
+                            __float2bfloat16_rn(y);
+                }
+            }
+        }
+    }
+    if (warp == 1 && lane == 0) mbar_wait(tmem_full, 0u, a.status);  // all MMAs retired
+    griddep_launch();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"((uint32_t)BN));
+    }
+}
+
+// int8 activations -> bf16 (exact) for the TMA operand of mode B.
+__global__ void tl_i8_to_bf16_kernel(const int8_t *__restrict__ q, __nv_bfloat16 *__restrict__ out,
+                                     long long n) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long k = i; k < n; k += stride) out[k] = __float2bfloat16_rn((float)q[k]);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace tlp
+
+// ------------------------------------------------------------------ host side
+namespace tl_internal {
+
+size_t prefill_workspace_bytes(int N, int K, int mode) {
+    // status word block + bf16 copy of the int8 activations in mode B (zeroed
+    // again after use, so the workspace stays zero-filled between calls)
+    size_t b = kStatusBytes;
+    if (mode == TL_MODE_I8) b += ((size_t)N * K * 2 + 255) / 256 * 256;
+    return b;
+}
+
+bool prefill_supported(int N, int K) { return N >= kPrefillMinN && (K % 8) == 0; }
+
+tl_status prefill_init_device() {
+    if (cudaFuncSetAttribute(tlp::tl_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tlp::SMEM_BYTES) != cudaSuccess)
+        return TL_ERR_CUDA;
+    return tlp::encode_fn() ? TL_OK : TL_ERR_UNSUPPORTED;
+}
+
+tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float *s,
+                         const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,
+                         size_t ws_bytes, unsigned flags, cudaStream_t stream) {
+    const int K = Ws[0].K;
+    if (!ws || ws_bytes < prefill_workspace_bytes(N, K, mode)) return TL_ERR_WORKSPACE;
+    tlp::PrefillArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.G = G;
+    a.mt_off[0] = 0;
+    for (int g = 0; g < G; ++g) {
+        a.packed[g] = reinterpret_cast<const char *>(Ws[g].packed);
+        a.scale[g] = Ws[g].scale;
+        a.rowsum[g] = Ws[g].rowsum;
+        a.Y[g] = Ys[g];
+        a.M[g] = Ws[g].M;
+        a.mt_off[g + 1] = a.mt_off[g] + (Ws[g].M + tlp::BM - 1) / tlp::BM;
+    }
+    a.KB = (K + 127) / 128;
+    a.N = N;
+    a.mode = mode;
+    a.out = out;
+    a.s = s;
+    a.z = z;
+    a.status = static_cast<int *>(ws);
+
+    const void *xb = X;
+    __nv_bfloat16 *conv = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + kStatusBytes);
+    const long long n = (long long)N * K;
+    if (mode == TL_MODE_I8) {
+        tlp::tl_i8_to_bf16_kernel<<<592, 256, 0, stream>>>(static_cast<const int8_t *>(X), conv, n);
+        if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
+        xb = conv;
+    }
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)tlp::BK, (cuuint32_t)tlp::BN};
+    const cuuint32_t estr[2] = {1, 1};
+    auto fn = tlp::encode_fn();
+    if (!fn) return TL_ERR_UNSUPPORTED;
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(xb), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return TL_ERR_ALIGN;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)a.mt_off[G], (unsigned)((N + tlp::BN - 1) / tlp::BN));
+    cfg.blockDim = dim3(tlp::THREADS);
+    cfg.dynamicSmemBytes = tlp::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (flags & TL_FLAG_PDL) && mode != TL_MODE_I8 ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map) != cudaSuccess) return TL_ERR_CUDA;
+    if (mode == TL_MODE_I8 && cudaMemsetAsync(conv, 0, (size_t)n * 2, stream) != cudaSuccess)
+        return TL_ERR_CUDA;
+    return TL_OK;
+}
+
+}  // namespace tl_internal

@@ -14,6 +14,9 @@ launch (four per layer).
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 from . import synth
@@ -22,33 +25,65 @@ from . import tl
 GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 
 
+class StackWeights:
+    """The packed weights of every layer, resident on the device.
+
+    Matrices are drawn and packed on host threads (seeded per matrix, so the
+    result does not depend on the thread count) and copied to the device.
+    ``keep_host`` layers also keep their int8 matrices and scales on the host.
+    """
+
+    def __init__(self, shape: synth.ModelShape, base_seed: int = 0, layers: int | None = None,
+                 keep_host=(), device: str = "cuda", threads: int | None = None):
+        self.shape = shape
+        self.layers = shape.layers if layers is None else layers
+        self.base_seed = base_seed
+        self.host = {}
+        shp = shape.linear_shapes()
+        jobs = [(l, p) for l in range(self.layers) for p in synth.PROJ_ORDER]
+
+        def make(job):
+            l, p = job
+            M, K = shp[p]
+            seed = synth.matrix_seed(base_seed, l, p)
+            W = synth.ternary(M, K, synth.zero_fraction(shape, l, p), seed)
+            scale = synth.scales(M, seed)
+            packed, sc, rs = tl.tl_pack(W, scale)
+            return job, packed, sc, rs, (W if l in keep_host else None)
+
+        self.per_layer = [dict() for _ in range(self.layers)]
+        n = threads or min(16, os.cpu_count() or 1)
+        with ThreadPoolExecutor(n) as ex:
+            for (l, p), packed, sc, rs, W in ex.map(make, jobs):
+                M, K = shp[p]
+                self.per_layer[l][p] = tl.TernaryWeight.from_host(packed, sc, rs, M, K,
+                                                                  device=device)
+                if W is not None:
+                    self.host[(l, p)] = (W, sc)
+
+    def __getitem__(self, layer: int) -> dict:
+        return self.per_layer[layer]
+
+
 class LinearStack:
     def __init__(self, shape: synth.ModelShape, N: int, mode: int = tl.TL_MODE_BF16,
                  out_dtype: int = tl.TL_OUT_F32, base_seed: int = 0, outlier_frac: float = 0.0,
                  unit_rms: bool = False, layers: int | None = None, keep_host=(),
-                 device: str = "cuda", symmetric: bool = False):
+                 device: str = "cuda", symmetric: bool = False,
+                 weights: StackWeights | None = None):
         import torch
         self.torch = torch
         self.shape = shape
         self.N, self.mode, self.out_dtype = N, mode, out_dtype
         self.symmetric = symmetric
-        self.layers = shape.layers if layers is None else layers
+        if weights is None:
+            weights = StackWeights(shape, base_seed, layers, keep_host, device)
+        self.stack_weights = weights
+        self.layers = weights.layers
         self.device = device
-        self.host = {}            # (layer, proj) -> (W int8, scale) for kept layers
+        self.host = weights.host  # (layer, proj) -> (W int8, scale) for kept layers
         shp = shape.linear_shapes()
-        self.weights = []         # per layer: dict proj -> TernaryWeight
-        for l in range(self.layers):
-            d = {}
-            for p in synth.PROJ_ORDER:
-                M, K = shp[p]
-                seed = synth.matrix_seed(base_seed, l, p)
-                W = synth.ternary(M, K, synth.zero_fraction(shape, l, p), seed)
-                scale = synth.scales(M, seed)
-                d[p] = tl.TernaryWeight.from_int8(W, scale, device=device)
-                if l in keep_host:
-                    self.host[(l, p)] = (W, scale)
-                del W
-            self.weights.append(d)
+        self.weights = weights.per_layer   # per layer: dict proj -> TernaryWeight
         # Inputs (one per launch group and layer) live in one flat bf16 buffer
         # and outputs in one flat buffer, so a host round trip is two copies.
         odt = {tl.TL_OUT_F32: torch.float32, tl.TL_OUT_BF16: torch.bfloat16}[out_dtype]
