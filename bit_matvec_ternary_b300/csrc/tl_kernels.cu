@@ -45,6 +45,8 @@ constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 200 * 1024;
 constexpr int kMaxSlice = 32;         // 128-column blocks per split-K slice, at most
+constexpr int kMaxPending = 8;        // partial pieces a warp holds before publishing
+constexpr int kMaxSlices = 32;        // split-K slices per launch (one flag bit each)
 
 struct GroupArgs {
     const char *packed[TL_MAX_GROUP];
@@ -68,24 +70,17 @@ struct GroupArgs {
     int mode;
     int out;
     float *part;    // split-K partials [R*S*2][N][16]
-    int *cnt;       // [R] arrival counters (units), zero between launches
+    unsigned long long *cnt;  // [R] arrivals: low 32 bits = blocks summed so far,
+                              // bit 32+s = slice s arrived in two pieces; zero between launches
 };
 
 __device__ __forceinline__ long long bnd(const GroupArgs &a, long long v) {
     return v * a.U / a.V;
 }
 
-// Warp owning unit u: the v with bnd(v) <= u < bnd(v + 1).
-__device__ __forceinline__ long long warp_of(const GroupArgs &a, long long u) {
-    long long v = (u * a.V) / a.U;
-    while (v + 1 <= a.V && bnd(a, v + 1) <= u) ++v;
-    while (v > 0 && bnd(a, v) > u) --v;
-    return v;
-}
-
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
@@ -94,8 +89,7 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -180,41 +174,19 @@ __device__ __forceinline__ void epilogue(const GroupArgs &a, int gi, int rl, int
         }
 }
 
-// Emit the partial sum of one piece (row tile r, slice s, piece p, nk blocks).
-__device__ __noinline__ void flush_piece(const GroupArgs &a, int r, int s, int p, int nk, int gi,
-                                         int rl, int lane, float c0, float c1, float c2,
-                                         float c3) {
+// Sum every piece of row tile r in fixed (slice, piece) order and store Y.
+// Called by the warp whose arrival completed the row tile's count; `split`
+// has bit s set when slice s came in two pieces.
+__device__ __noinline__ void reduce_row_tile(const GroupArgs &a, int r, unsigned split,
+                                             int lane) {
     const int g = lane >> 2, t = lane & 3;
-    const float c[4] = {c0, c1, c2, c3};
-    if (a.S == 1 && nk == a.KB) {   // the whole k-range in one piece: final
-        epilogue(a, gi, rl, g, t, c);
-        return;
-    }
-    const long long slot = ((long long)r * a.S + s) * 2 + p;
-    float *dst = a.part + slot * a.N * 16;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = 2 * t + e;
-            if (n < a.N) __stcg(dst + n * 16 + g + 8 * h, c[2 * h + e]);
-        }
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        const int old = atomicAdd(a.cnt + r, nk);
-        last = (old + nk == a.KB);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
+    int gi = 0;
+    while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
+    const int rl = r - a.rt_off[gi];
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int ss = 0; ss < a.S; ++ss) {
-        const long long us = ((long long)ss * a.R + r) * a.KS;
-        const long long v0 = warp_of(a, us);
-        const bool split = bnd(a, v0 + 1) < us + a.KS;
-        for (int pp = 0; pp < (split ? 2 : 1); ++pp) {
+        const int pieces = ((split >> ss) & 1u) ? 2 : 1;
+        for (int pp = 0; pp < pieces; ++pp) {
             const float *src = a.part + (((long long)r * a.S + ss) * 2 + pp) * a.N * 16;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -226,7 +198,63 @@ __device__ __noinline__ void flush_piece(const GroupArgs &a, int r, int s, int p
         }
     }
     epilogue(a, gi, rl, g, t, acc);
-    if (lane == 0) a.cnt[r] = 0;
+    if (lane == 0) a.cnt[r] = 0ull;
+}
+
+// Publish this warp's pending pieces: one fence for all of them, then one
+// counter update each; the warp that completes a row tile's count reduces it.
+// Runs when the warp's weight loads have all landed (or, rarely, when its
+// pending list is full), so the fence never drains the load pipeline.
+__device__ __noinline__ void commit_pieces(const GroupArgs &a, const int *pend_r,
+                                           const unsigned long long *pend_add, int count,
+                                           int lane) {
+    __threadfence();
+    __syncwarp();
+    for (int i = 0; i < count; ++i) {
+        const int r = pend_r[i];
+        unsigned long long now = 0ull;
+        if (lane == 0) now = atomicAdd(a.cnt + r, pend_add[i]) + pend_add[i];
+        now = __shfl_sync(0xffffffffu, now, 0);
+        if ((unsigned)(now & 0xffffffffull) == (unsigned)a.KB) {
+            __threadfence();
+            reduce_row_tile(a, r, (unsigned)(now >> 32), lane);
+        }
+    }
+}
+
+// Emit one piece (row tile r, slice s, piece p, nk blocks): the final result
+// when it covers the whole k-range, else its partial sums go to the workspace
+// and the piece joins the warp's pending list.
+// Returns the new length of the pending list.
+__device__ __noinline__ int emit_piece(const GroupArgs &a, int r, int s, int p, int nk, int gi,
+                                       int rl, int lane, float c0, float c1, float c2, float c3,
+                                       int *pend_r, unsigned long long *pend_add,
+                                       int pend_count) {
+    const int g = lane >> 2, t = lane & 3;
+    const float c[4] = {c0, c1, c2, c3};
+    if (a.S == 1 && nk == a.KB) {   // the whole k-range in one piece: final
+        epilogue(a, gi, rl, g, t, c);
+        return pend_count;
+    }
+    const long long slot = ((long long)r * a.S + s) * 2 + p;
+    float *dst = a.part + slot * a.N * 16;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = 2 * t + e;
+            if (n < a.N) __stcg(dst + n * 16 + g + 8 * h, c[2 * h + e]);
+        }
+    if (lane == 0) {
+        pend_r[pend_count] = r;
+        pend_add[pend_count] = (unsigned long long)nk | ((unsigned long long)p << (32 + s));
+    }
+    __syncwarp();
+    if (++pend_count == kMaxPending) {
+        commit_pieces(a, pend_r, pend_add, pend_count, lane);
+        pend_count = 0;
+    }
+    return pend_count;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -289,11 +317,15 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
 
     const uint32_t M2 = 0xC000C000u;
     const bool xlane = g < a.N;
-    const int xstride = 4 * a.N * 4;            // uint4 per 128-column block
+    const int xq = a.N * 4;                     // uint4 per 32-column quarter
+    const int xstride = 4 * xq;                 // uint4 per 128-column block
     // four independent accumulator chains (one per 32-column quarter)
     float c[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+    __shared__ int pend_r[kWarps][kMaxPending];
+    __shared__ unsigned long long pend_add[kWarps][kMaxPending];
+    int pend_count = 0;
     Cursor cc;
     cc.seek(a, u0, lane);
     int piece_p = cc.bp == 0 ? 0 : 1;
@@ -307,24 +339,29 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 const uint4 w = ring[i];
                 if (pf.u < u1) ring[i] = ldg_stream(pf.p);
                 pf.next(a, lane);
+                uint4 b[4];
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) {
+                    b[qd] = make_uint4(0u, 0u, 0u, 0u);
+                    if (xlane) b[qd] = xb[qd * xq];
+                }
 #pragma unroll
                 for (int qd = 0; qd < 4; ++qd) {
                     const uint32_t word = qd == 0 ? w.x : qd == 1 ? w.y : qd == 2 ? w.z : w.w;
-                    uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                    if (xlane) b = xb[qd * a.N * 4];
                     mma_bf16_16816(c[qd], word & M2, (word << 2) & M2, (word << 4) & M2,
-                                   (word << 6) & M2, b.x, b.y);
+                                   (word << 6) & M2, b[qd].x, b[qd].y);
                     mma_bf16_16816(c[qd], (word << 8) & M2, (word << 10) & M2,
-                                   (word << 12) & M2, (word << 14) & M2, b.z, b.w);
+                                   (word << 12) & M2, (word << 14) & M2, b[qd].z, b[qd].w);
                 }
                 ++piece_nk;
                 const bool seg_end = (cc.bp == a.KS - 1) || (base + i + 1 == u1);
                 if (seg_end) {
-                    flush_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane,
-                                (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]),
-                                (c[0][1] + c[1][1]) + (c[2][1] + c[3][1]),
-                                (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]),
-                                (c[0][3] + c[1][3]) + (c[2][3] + c[3][3]));
+                    pend_count = emit_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane,
+                               (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]),
+                               (c[0][1] + c[1][1]) + (c[2][1] + c[3][1]),
+                               (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]),
+                               (c[0][3] + c[1][3]) + (c[2][3] + c[3][3]), pend_r[warp],
+                               pend_add[warp], pend_count);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
                     piece_p = 0;
@@ -338,6 +375,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
             }
         }
     }
+    if (pend_count) commit_pieces(a, pend_r[warp], pend_add[warp], pend_count, lane);
 }
 
 // ------------------------------------------------------------------ quant
@@ -471,11 +509,22 @@ void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
         if ((size_t)n_sl * d * 128 * kNMax * 2 <= kSmemLimit) p->KS = d;
     }
     p->S = p->KB / p->KS;
+    if (p->S > kMaxSlices) {                // fewer warps, longer slices
+        p->KS = (int)ceil_div(p->KB, kMaxSlices);
+        while (p->KB % p->KS) ++p->KS;
+        p->S = p->KB / p->KS;
+        const long long need_avg = p->KS - 1;       // min warp range >= KS - 1
+        long long V = need_avg > 0 ? p->U / need_avg : p->V;
+        V = std::max<long long>(kWarps, std::min<long long>(V, p->V)) / kWarps * kWarps;
+        p->V = V;
+        p->P = (int)(V / kWarps);
+    }
+    // the per-CTA range may have grown above; size the staging for the final plan
     const long long su = (long long)p->R * p->KS;
-    const long long n_sl = std::min<long long>(p->S, ceil_div(cta_units, su) + 1);
+    const long long n_sl = std::min<long long>(p->S, ceil_div(ceil_div(p->U, p->P), su) + 1);
     const int n = std::min(std::max(N, 1), kNMax);
     p->smem = (size_t)n_sl * p->KS * 128 * n * 2;
-    const size_t cnt_bytes = ((size_t)p->R * 4 + 255) / 256 * 256;
+    const size_t cnt_bytes = ((size_t)p->R * 8 + 255) / 256 * 256;
     p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * p->S * 2 * 16 * n * 4;
 }
 
@@ -538,9 +587,9 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     a.s = s ? s + n0 : nullptr;
     a.z = z ? z + n0 : nullptr;
     a.N = n; a.mode = mode; a.out = out;
-    const size_t cnt_bytes = ((size_t)p.R * 4 + 255) / 256 * 256;
+    const size_t cnt_bytes = ((size_t)p.R * 8 + 255) / 256 * 256;
     char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
-    a.cnt = reinterpret_cast<int *>(wsb);
+    a.cnt = reinterpret_cast<unsigned long long *>(wsb);
     a.part = reinterpret_cast<float *>(wsb + cnt_bytes);
 
     cudaLaunchConfig_t cfg;

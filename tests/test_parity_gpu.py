@@ -244,7 +244,7 @@ def test_workspace_is_left_zeroed(oracle_mod):
     torch.cuda.synchronize()
     nbytes = tl.tl_workspace_bytes([m.dev], 8)
     R = (4096 + 15) // 16
-    assert int(ws[: 4 * R].count_nonzero()) == 0
+    assert int(ws[: 256 + 8 * R].count_nonzero()) == 0     # status word + arrival counters
     assert nbytes <= ws.numel()
 
 
