@@ -24,4 +24,13 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
                          const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,
                          size_t ws_bytes, unsigned flags, cudaStream_t stream);
 
+// The N <= 8 decode / verify kernel over all N in chunks of 8, with a given
+// scratch buffer; `need` is the scratch it requires for these shapes and
+// `zeroed` the leading bytes (status word and arrival counters) that must
+// be zero when a call starts.
+tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t *zeroed);
+tl_status launch_decode(const tl_weight *Ws, int G, const void *X, const float *s,
+                        const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,
+                        size_t ws_bytes, unsigned flags, cudaStream_t stream);
+
 }  // namespace tl_internal

@@ -609,6 +609,38 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
 
 }  // namespace
 
+namespace tl_internal {
+
+tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t *zeroed) {
+    DeviceInfo *dev = nullptr;
+    const tl_status st = device_info(&dev);
+    if (st != TL_OK) return st;
+    int Ms[TL_MAX_GROUP];
+    for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
+    Plan p;
+    make_plan(Ms, G, Ws[0].K, kNMax, dev->sms, &p);   // chunks never exceed 8 tokens
+    *need = p.ws_bytes;
+    *zeroed = kStatusBytes + ((size_t)p.R * 8 + 255) / 256 * 256;
+    return TL_OK;
+}
+
+tl_status launch_decode(const tl_weight *Ws, int G, const void *X, const float *s,
+                        const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,
+                        size_t ws_bytes, unsigned flags, cudaStream_t stream) {
+    DeviceInfo *dev = nullptr;
+    tl_status st = device_info(&dev);
+    if (st != TL_OK) return st;
+    for (int n0 = 0; n0 < N; n0 += kNMax) {
+        const int n = N - n0 < kNMax ? N - n0 : kNMax;
+        st = launch_chunk(Ws, G, X, s, z, Ys, n0, n, mode, out, ws, ws_bytes, flags, stream,
+                          *dev);
+        if (st != TL_OK) return st;
+    }
+    return TL_OK;
+}
+
+}  // namespace tl_internal
+
 extern "C" {
 
 size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N) {

@@ -34,8 +34,9 @@ TL_MAX_GROUP = 4
 
 # Every symbol include/tl.h declares.
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
-           "tl_quantize_act", "tl_linear", "tl_linear_group", "tl_status_string",
-           "tl_version")
+           "tl_quantize_act", "tl_linear", "tl_linear_group", "tl_linear_noalloc",
+           "tl_status_string", "tl_version")
+TL_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class tl_weight(C.Structure):
@@ -60,6 +61,9 @@ _lib.tl_linear.restype = _int
 _lib.tl_linear_group.argtypes = [C.POINTER(tl_weight), _int, _p, _p, _p, C.POINTER(_p), _int,
                                  _int, _int, _p, _sz, C.c_uint, _p]
 _lib.tl_linear_group.restype = _int
+_lib.tl_linear_noalloc.argtypes = [C.POINTER(tl_weight), _p, _p, _p, _p, _int, _int, _int,
+                                   C.c_uint, _p]
+_lib.tl_linear_noalloc.restype = _int
 _lib.tl_status_string.argtypes = [_int]
 _lib.tl_status_string.restype = C.c_char_p
 _lib.tl_version.argtypes = []
@@ -237,6 +241,24 @@ def tl_linear(weight, X, s=None, z=None, out=None, mode: int = TL_MODE_BF16,
                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), flags,
                         _stream_ptr(stream))
     _check(st, "tl_linear")
+    return out
+
+
+def tl_linear_noalloc(weight, X, s=None, z=None, out=None, mode: int = TL_MODE_BF16,
+                      out_dtype: int = TL_OUT_F32, flags: int = 0, stream=None):
+    """Y = linear(W, X) with the library's fixed scratch array: no workspace
+    argument, nothing allocated by the library (the output is allocated
+    here only when `out` is None)."""
+    torch = _torch()
+    N = X.shape[0]
+    if out is None:
+        dt = getattr(torch, _OUT_TORCH[out_dtype])
+        out = torch.empty((N, weight.M), dtype=dt, device=X.device)
+    st = _lib.tl_linear_noalloc(_structs([weight]), X.data_ptr(),
+                                None if s is None else s.data_ptr(),
+                                None if z is None else z.data_ptr(), out.data_ptr(), N, mode,
+                                out_dtype, flags, _stream_ptr(stream))
+    _check(st, "tl_linear_noalloc")
     return out
 
 

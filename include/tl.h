@@ -163,6 +163,37 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
                           int out_dtype, void *workspace, size_t workspace_bytes,
                           unsigned flags, void *stream);
 
+/* Size of the library's fixed scratch array for tl_linear_noalloc (8 MiB):
+ * enough for every Qwen3-8B-shaped matrix at up to 8 tokens per chunk. */
+#define TL_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* DEVICE.  tl_linear for callers that cannot allocate device memory.
+ * The pages describe no such call; it exists for users of this library who
+ * may not call cudaMalloc (or any allocating routine, torch's included) when
+ * they run a linear -- code inside another runtime's memory pool, a loop
+ * that must not allocate after start-up, or a host that only hands over
+ * input and output buffers.  The caller still passes W, X, s, z and Y
+ * exactly as for tl_linear; the split-K partial sums and arrival counters
+ * that tl_linear keeps in the caller's workspace live instead in a
+ * file-scope __device__ array of TL_NOALLOC_SCRATCH_BYTES bytes, which every
+ * GPU that loads the library holds until the process exits.
+ *   - Any N >= 1 runs on the decode / verify kernel in chunks of 8 tokens
+ *     (never on the prefill kernel); results equal tl_linear's for N <= 255.
+ *   - Shapes whose scratch would exceed TL_NOALLOC_SCRATCH_BYTES return
+ *     TL_ERR_WORKSPACE before anything is launched.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.  Each call clears the array's status word and counters with
+ *     cudaMemsetAsync on `stream` before its launches.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and give wrong results; serialise
+ *     them on one stream. */
+TL_API tl_status tl_linear_noalloc(const tl_weight *W, const void *X, const float *s,
+                                   const int32_t *z, void *Y, int N, int mode, int out_dtype,
+                                   unsigned flags, void *stream);
+
 /* Static, never NULL. */
 TL_API const char *tl_status_string(tl_status status);
 
