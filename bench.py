@@ -35,13 +35,19 @@ L2_BYTES = 126 * 1024 * 1024
 
 
 def peaks():
+    """(HBM GB/s, kind, bf16 TFLOP/s sustained, kind) from MEASURED_PEAKS.json."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        hbm, hk = float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
-        return 6400.0, "fallback"
+        d, hbm, hk = {}, 6400.0, "fallback"
+    try:
+        bf, bk = float(d["bf16_tflops_sustained"]), "measured (bf16_tflops_sustained)"
+    except (KeyError, ValueError):
+        bf, bk = 1400.0, "fallback (sustained)"
+    return hbm, hk, bf, bk
 
 
 # ---------------------------------------------------------------- clocks
@@ -226,6 +232,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-n8", action="store_true", help="skip the N=8 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the N=512 prefill line")
     ap.add_argument("--layers", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -253,7 +260,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     shape = synth.NEUTRINO_8B
-    hbm_peak, peak_kind = peaks()
+    hbm_peak, peak_kind, bf16_peak, bf16_kind = peaks()
 
     # ---- N = 1, mode A: the headline
     t_gen = time.perf_counter()
@@ -309,6 +316,26 @@ def main():
                            "launches_per_step": st8.launches_per_step}
             del st8
             torch.cuda.empty_cache()
+
+    if not args.no_prefill:
+        # prefill-sized batch: 512 tokens, int8 symmetric per-token activations,
+        # bf16 out, every linear on the tcgen05 kernel
+        stp = LinearStack(shape, N=512, mode=tl.TL_MODE_I8, out_dtype=tl.TL_OUT_BF16,
+                          symmetric=True, weights=weights)
+        stp.capture()
+        msp = time_graph(stp, max(3, args.steps // 4), args.warmup, torch)
+        flops = 2.0 * shape.ternary_weights_per_layer() * stp.layers * 512
+        tflops = flops / (msp / 1e3) / 1e12
+        extra["prefill_n512"] = {
+            "tokens_s": 512 / (msp / 1e3), "ms_per_step": msp, "flops_per_step": flops,
+            "mode": "B (int8 symmetric per-token, values fed to the tensor cores as exact bf16)",
+            "out": "bf16",
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": tflops / bf16_peak,
+                         "peak_kind": bf16_kind, "kernel": "tl_prefill_kernel"},
+            "launches_per_step": stp.launches_per_step + 4 * stp.layers}
+        del stp
+        torch.cuda.empty_cache()
 
     if rank == 0:
         out = {

@@ -11,20 +11,26 @@
 //     2-bit codes at HBM rate;
 //   * speculative verify: up to seven drafted tokens checked in one batched
 //     pass (wiki "Neutrino-1", "What is actually new"), hence N <= 8 columns
-//     of one mma.sync n8 tile.
+//     of one mma n8 tile.
 //
 // Kernel tl_mma_kernel (N <= 8, modes A and B):
-//   The TL2P v1 tile is laid out in mma.m16n8k16 A-fragment order, so one
-//   128-bit load gives a lane the 64 weights it needs for 8 MMA steps over
-//   rows g and g+8.  Register f of a step is (word << 2q) & 0xC000C000: a
-//   bf16x2 pair of +-2.0 / +-0.0.  Activations are staged once per CTA in
-//   shared memory in B-fragment order (mode B converts int8 to bf16, exact).
-//   Work is split "stream-K" style: the (slice, row tile, k-block) units of
-//   the launch are cut into equal contiguous ranges, one per warp, so every
-//   warp streams the same number of bytes.  A row tile whose k-range spans
-//   several warps is finished by whichever warp arrives last (counter in the
-//   workspace); it adds the partial sums in a fixed order, so results are
-//   deterministic and do not depend on N.
+//   Weights.  Each warp owns a contiguous range of (slice, 16-row tile,
+//   128-column block) units and streams them with cp.async.bulk into its own
+//   ring of shared-memory slots (one bulk copy moves up to 4 tiles, 2 KB,
+//   and completes on the slot's mbarrier).  A TL2P v1 tile is in
+//   mma.m16n8k16 A-fragment order: a lane's 16 bytes are 4 words, each
+//   covering two 16-column steps, and register f of a step is
+//   (word << 2q) & 0xC000C000, a bf16x2 pair of +-2.0 / +-0.0 -- one shift
+//   (IMAD, FMA pipe) and one AND (LOP3, ALU pipe) per two weights.  The
+//   tensor cores do the multiply-adds (bf16 x bf16 -> fp32, products exact).
+//   Activations.  Staged once per CTA in shared memory in B-fragment order
+//   (mode B converts int8 to bf16, exact).  Token columns n >= N read token
+//   N-1 (their results are discarded), so no lane is predicated off.
+//   Split-K.  Warp v owns units [v*L, min((v+1)*L, U)), L = ceil(U / warps).
+//   A row tile whose k-range spans several warps is finished by the warp
+//   that completes its arrival count (workspace counter); it adds the pieces
+//   in a fixed order, so results are deterministic and every token's result
+//   is independent of N.
 
 #include "tl.h"
 #include "tl_internal.cuh"
@@ -40,13 +46,16 @@ namespace {
 
 constexpr int kWarps = 16;            // warps per CTA of the N <= 8 kernel (one CTA per SM)
 constexpr int kThreads = kWarps * 32;
-constexpr int kDepth = 8;             // 128-bit weight loads in flight per lane
+constexpr int kChunkTiles = 4;        // tiles (512 B each) per bulk copy
+constexpr int kSlots = 3;             // bulk copies in flight per warp
+constexpr int kRingBytes = kWarps * kSlots * kChunkTiles * 512;   // 96 KB
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
-constexpr size_t kSmemLimit = 200 * 1024;
+constexpr size_t kSmemLimit = 120 * 1024;   // activation staging budget per CTA
 constexpr int kMaxSlice = 32;         // 128-column blocks per split-K slice, at most
 constexpr int kMaxPending = 8;        // partial pieces a warp holds before publishing
 constexpr int kMaxSlices = 32;        // split-K slices per launch (one flag bit each)
+constexpr long long kWaitLimit = 1ll << 31;   // SM cycles before a wait gives up
 
 struct GroupArgs {
     const char *packed[TL_MAX_GROUP];
@@ -63,6 +72,7 @@ struct GroupArgs {
     int K;
     long long U;    // units = R * KB
     long long V;    // warps in the grid
+    int L;          // units per warp (the last warps may get fewer or none)
     const void *X;  // bf16 [N][K] (mode A) or int8 [N][K] (mode B)
     const float *s;
     const int32_t *z;
@@ -72,18 +82,15 @@ struct GroupArgs {
     float *part;    // split-K partials [R*S*2][N][16]
     unsigned long long *cnt;  // [R] arrivals: low 32 bits = blocks summed so far,
                               // bit 32+s = slice s arrived in two pieces; zero between launches
+    int *status;    // workspace status word
 };
 
-__device__ __forceinline__ long long bnd(const GroupArgs &a, long long v) {
-    return v * a.U / a.V;
+__device__ __forceinline__ int bnd(const GroupArgs &a, int v) {
+    return (int)min((long long)v * a.L, a.U);
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void *p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
@@ -102,15 +109,50 @@ __device__ __forceinline__ void griddep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Position of a unit: slice s, row tile r (group-wide), block bp in the slice,
-// and the matrix gi / local row tile rl it belongs to.  `p` is this lane's
-// 16 bytes of the unit's TL2P tile; it advances by one tile inside a slice
-// segment and is recomputed only when the segment changes.
-struct Cursor {
-    int u, s, r, bp, gi, rl;
-    const char *p;
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait; false (and the status word set) when it gives up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
+    if (mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (clock64() - t0 > kWaitLimit) {
+            atomicExch(status, TL_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+// One bulk copy global -> shared, completing `bytes` on the slot's mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
 
-    __device__ void seek(const GroupArgs &a, int u0, int lane) {
+// A run of consecutive tiles of one (slice, row tile) segment: at most
+// kChunkTiles, never across a segment or the warp's range end, so its bytes
+// are contiguous in the packed matrix.
+struct Chunk {
+    int u, s, r, bp, gi, rl, n;
+
+    __device__ void seek(const GroupArgs &a, int u0, int u1) {
         u = u0;
         const int su = a.R * a.KS;
         s = u0 / su;
@@ -120,35 +162,43 @@ struct Cursor {
         gi = 0;
         while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
         rl = r - a.rt_off[gi];
-        p = a.packed[gi] + ((long long)rl * a.KB + (long long)s * a.KS + bp) * 512 + lane * 16;
+        size(a, u1);
     }
-    __device__ __forceinline__ void next(const GroupArgs &a, int lane) {
-        ++u;
-        if (++bp < a.KS) {
-            p += 512;
-            return;
+    __device__ __forceinline__ void size(const GroupArgs &a, int u1) {
+        n = min(kChunkTiles, min(a.KS - bp, u1 - u));
+    }
+    __device__ __forceinline__ void next(const GroupArgs &a, int u1) {
+        u += n;
+        bp += n;
+        if (bp == a.KS) {
+            bp = 0;
+            if (++r == a.R) {
+                r = 0; ++s; gi = 0; rl = 0;
+            } else if (r == a.rt_off[gi + 1]) {
+                ++gi; rl = 0;
+            } else {
+                ++rl;
+            }
         }
-        bp = 0;
-        if (++r == a.R) {
-            r = 0; ++s; gi = 0; rl = 0;
-        } else if (r == a.rt_off[gi + 1]) {
-            ++gi; rl = 0;
-        } else {
-            ++rl;
-        }
-        p = a.packed[gi] + ((long long)rl * a.KB + (long long)s * a.KS) * 512 + lane * 16;
+        size(a, u1);
+    }
+    __device__ __forceinline__ const char *src(const GroupArgs &a) const {
+        return a.packed[gi] + ((long long)rl * a.KB + (long long)s * a.KS + bp) * 512;
+    }
+    __device__ __forceinline__ bool seg_end(const GroupArgs &a, int u1) const {
+        return bp + n == a.KS || u + n == u1;
     }
 };
 
+// Y[n][m] from the scaled sum y_acc = sum_k w*x (mode A) or the exact
+// integer sum_k w*q (mode B).
 __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int n, float acc) {
-    // acc holds 2 * sum_k w*x (weights decode to +-2.0); halving is exact.
     const int M = a.M[gi];
-    const float half = acc * 0.5f;
     float y;
     if (a.mode == TL_MODE_BF16) {
-        y = __fmul_rn(half, a.scale[gi][m]);
+        y = __fmul_rn(acc, a.scale[gi][m]);
     } else {
-        const int iacc = __float2int_rn(half);
+        const int iacc = __float2int_rn(acc);
         if (a.out == TL_OUT_I32_RAW) {
             reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * M + m] = iacc;
             return;
@@ -201,22 +251,31 @@ __device__ __noinline__ void reduce_row_tile(const GroupArgs &a, int r, unsigned
     if (lane == 0) a.cnt[r] = 0ull;
 }
 
-// Publish this warp's pending pieces: one fence for all of them, then one
-// counter update each; the warp that completes a row tile's count reduces it.
-// Runs when the warp's weight loads have all landed (or, rarely, when its
-// pending list is full), so the fence never drains the load pipeline.
+// Publish this warp's pending pieces.  The lanes' partial-sum stores are
+// ordered before lane 0's counter update by __syncwarp, and the update is a
+// release (and acquire) at GPU scope, so the warp that completes a row tile's
+// count sees every piece; it then reduces the row tile.  No full fence.
+__device__ __forceinline__ unsigned long long atomic_add_acq_rel(unsigned long long *p,
+                                                                 unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+                 : "=l"(old)
+                 : "l"(p), "l"(v)
+                 : "memory");
+    return old;
+}
+
 __device__ __noinline__ void commit_pieces(const GroupArgs &a, const int *pend_r,
                                            const unsigned long long *pend_add, int count,
                                            int lane) {
-    __threadfence();
     __syncwarp();
     for (int i = 0; i < count; ++i) {
         const int r = pend_r[i];
         unsigned long long now = 0ull;
-        if (lane == 0) now = atomicAdd(a.cnt + r, pend_add[i]) + pend_add[i];
+        if (lane == 0) now = atomic_add_acq_rel(a.cnt + r, pend_add[i]) + pend_add[i];
         now = __shfl_sync(0xffffffffu, now, 0);
         if ((unsigned)(now & 0xffffffffull) == (unsigned)a.KB) {
-            __threadfence();
+            __syncwarp();
             reduce_row_tile(a, r, (unsigned)(now >> 32), lane);
         }
     }
@@ -224,8 +283,7 @@ __device__ __noinline__ void commit_pieces(const GroupArgs &a, const int *pend_r
 
 // Emit one piece (row tile r, slice s, piece p, nk blocks): the final result
 // when it covers the whole k-range, else its partial sums go to the workspace
-// and the piece joins the warp's pending list.
-// Returns the new length of the pending list.
+// and the piece joins the warp's pending list.  Returns the new list length.
 __device__ __noinline__ int emit_piece(const GroupArgs &a, int r, int s, int p, int nk, int gi,
                                        int rl, int lane, float c0, float c1, float c2, float c3,
                                        int *pend_r, unsigned long long *pend_add,
@@ -257,51 +315,80 @@ __device__ __noinline__ int emit_piece(const GroupArgs &a, int r, int s, int p, 
     return pend_count;
 }
 
+// One 128-column block of one 16-row tile: 8 MMAs over the lane's 16-byte
+// slice of the tile (w) and the 4 B-fragment quarters (b).
+__device__ __forceinline__ void tile_mma(float (&c)[4][4], const uint4 &w, const uint4 (&b)[4]) {
+    const uint32_t M2 = 0xC000C000u;
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+        const uint32_t word = qd == 0 ? w.x : qd == 1 ? w.y : qd == 2 ? w.z : w.w;
+        mma_bf16_16816(c[qd], word & M2, (word << 2) & M2, (word << 4) & M2, (word << 6) & M2,
+                       b[qd].x, b[qd].y);
+        mma_bf16_16816(c[qd], (word << 8) & M2, (word << 10) & M2, (word << 12) & M2,
+                       (word << 14) & M2, b[qd].z, b[qd].w);
+    }
+}
+
+// kModeA: bf16 activations (else int8 from the quantiser).  NT: token
+// columns staged (a power of two >= N; columns n >= N repeat token N-1 and
+// their results are discarded).
+template <bool kModeA, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
 tl_mma_kernel(const __grid_constant__ GroupArgs a) {
-    extern __shared__ uint4 xs[];
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;                                    // [kWarps][kSlots][2 KB]
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + kRingBytes); // staged activations
+    __shared__ __align__(8) unsigned long long bars[kWarps][kSlots];
+    __shared__ int pend_r[kWarps][kMaxPending];
+    __shared__ unsigned long long pend_add[kWarps][kMaxPending];
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-
-    const long long v = (long long)blockIdx.x * kWarps + warp;
-    const int u0 = (int)bnd(a, v), u1 = (int)bnd(a, v + 1);
-    const int cu0 = (int)bnd(a, (long long)blockIdx.x * kWarps);
-    const int cu1 = (int)bnd(a, (long long)(blockIdx.x + 1) * kWarps);
+    const int v = blockIdx.x * kWarps + warp;
+    const int u0 = bnd(a, v), u1 = bnd(a, v + 1);
+    const int cu0 = bnd(a, blockIdx.x * kWarps), cu1 = bnd(a, (blockIdx.x + 1) * kWarps);
     const int su = a.R * a.KS;
     const int s_lo = cu0 / su;
     const int n_sl = cu1 > cu0 ? (cu1 - 1) / su - s_lo + 1 : 0;
+    const int N = a.N;
 
-    // Weights do not depend on the previous kernel: start streaming them
+    if (threadIdx.x < kWarps * kSlots)
+        mbar_init(smem_u32(&bars[0][0]) + 8u * threadIdx.x, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+
+    // Weights do not depend on the previous kernel: start the bulk copies
     // before waiting for it.
-    uint4 ring[kDepth];
-    Cursor pf;
-    pf.seek(a, u0, lane);
-#pragma unroll
-    for (int i = 0; i < kDepth; ++i) {
-        if (pf.u < u1) ring[i] = ldg_stream(pf.p);
-        pf.next(a, lane);
-    }
+    const uint32_t ring_w = smem_u32(ring) + warp * (kSlots * kChunkTiles * 512);
+    const uint32_t bar_w = smem_u32(&bars[warp][0]);
+    Chunk pf;
+    pf.seek(a, u0, u1);
+    if (lane == 0)
+        for (int i = 0; i < kSlots && pf.u < u1; ++i) {
+            bulk_load(ring_w + i * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * i);
+            pf.next(a, u1);
+        }
     griddep_wait();
     griddep_launch();
 
-    // Stage X for this CTA's slices in B-fragment order:
-    // word ((((sl*KS + bp)*4 + qd)*N + n)*4 + t)*4 + w holds x[n][k], x[n][k+1]
-    // with k = ((s_lo+sl)*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
+    // ---- stage X for this CTA's slices in B-fragment order:
+    // word ((((sl*KS + bp)*4 + qd)*NT + n)*4 + t)*4 + w holds x[n'][k], x[n'][k+1],
+    // n' = min(n, N-1), k = ((s_lo+sl)*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
     {
-        const int N = a.N;
-        const int words = n_sl * a.KS * 64 * N;
+        const int words = n_sl * a.KS * 64 * NT;
         uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
         for (int idx = threadIdx.x; idx < words; idx += kThreads) {
             const int w = idx & 3, tt = (idx >> 2) & 3;
-            int rest = idx >> 4;
-            const int n = rest % N; rest /= N;
-            const int qd = rest & 3; rest >>= 2;
+            const int n = min((idx >> 4) % NT, N - 1);
+            int rest = (idx >> 4) / NT;
+            const int qd = rest & 3;
+            rest >>= 2;
             const int bp = rest % a.KS;
             const int sl = rest / a.KS;
             const int k = ((s_lo + sl) * a.KS + bp) * 128 + 16 * (2 * qd + (w >> 1)) + 2 * tt +
                           8 * (w & 1);
             uint32_t lo = 0, hi = 0;
-            if (a.mode == TL_MODE_BF16) {
+            if (kModeA) {
                 const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
                 if (k < a.K) lo = x[k];
                 if (k + 1 < a.K) hi = x[k + 1];
@@ -315,68 +402,102 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     }
     __syncthreads();
 
-    const uint32_t M2 = 0xC000C000u;
-    const bool xlane = g < a.N;
-    const int xq = a.N * 4;                     // uint4 per 32-column quarter
-    const int xstride = 4 * xq;                 // uint4 per 128-column block
-    // four independent accumulator chains (one per 32-column quarter)
+    // ---- stream the warp's units
+    constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
+    constexpr int XB = 4 * XQ;                  // uint4 per 128-column block
     float c[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-    __shared__ int pend_r[kWarps][kMaxPending];
-    __shared__ unsigned long long pend_add[kWarps][kMaxPending];
     int pend_count = 0;
-    Cursor cc;
-    cc.seek(a, u0, lane);
-    int piece_p = cc.bp == 0 ? 0 : 1;
     int piece_nk = 0;
-    const uint4 *xb = xs + ((cc.s - s_lo) * a.KS + cc.bp) * xstride + g * 4 + t;
+    Chunk cc;
+    cc.seek(a, u0, u1);
+    int piece_p = cc.bp == 0 ? 0 : 1;
+    int slot = 0;
+    uint32_t phases = 0;                        // parity bit per slot
+    bool ok = true;
 
-    for (int base = u0; base < u1; base += kDepth) {
+    while (cc.u < u1) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar_w + 8u * slot, (phases >> slot) & 1u,
+                                                            a.status));
+        if (!got) { ok = false; break; }
+        phases ^= 1u << slot;
+        const uint4 *tiles = reinterpret_cast<const uint4 *>(
+            ring + warp * (kSlots * kChunkTiles * 512) + slot * (kChunkTiles * 512)) + lane;
+        const uint4 *xb = xs + ((cc.s - s_lo) * a.KS + cc.bp) * XB + (g % NT) * 4 + t;
+        if (cc.n == kChunkTiles) {
+            // full chunk: load tile i+1 while tile i is multiplied
+            uint4 w = tiles[0];
+            uint4 b[4];
 #pragma unroll
-        for (int i = 0; i < kDepth; ++i) {
-            if (base + i < u1) {
-                const uint4 w = ring[i];
-                if (pf.u < u1) ring[i] = ldg_stream(pf.p);
-                pf.next(a, lane);
+            for (int qd = 0; qd < 4; ++qd) b[qd] = xb[qd * XQ];
+#pragma unroll
+            for (int i = 0; i < kChunkTiles; ++i) {
+                uint4 wn = w, bn[4] = {b[0], b[1], b[2], b[3]};
+                if (i + 1 < kChunkTiles) {
+                    wn = tiles[(i + 1) * 32];
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) bn[qd] = xb[(i + 1) * XB + qd * XQ];
+                }
+                tile_mma(c, w, b);
+                w = wn;
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) b[qd] = bn[qd];
+            }
+        } else {
+            for (int i = 0; i < cc.n; ++i) {
+                const uint4 w = tiles[i * 32];
                 uint4 b[4];
 #pragma unroll
-                for (int qd = 0; qd < 4; ++qd) {
-                    b[qd] = make_uint4(0u, 0u, 0u, 0u);
-                    if (xlane) b[qd] = xb[qd * xq];
-                }
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) {
-                    const uint32_t word = qd == 0 ? w.x : qd == 1 ? w.y : qd == 2 ? w.z : w.w;
-                    mma_bf16_16816(c[qd], word & M2, (word << 2) & M2, (word << 4) & M2,
-                                   (word << 6) & M2, b[qd].x, b[qd].y);
-                    mma_bf16_16816(c[qd], (word << 8) & M2, (word << 10) & M2,
-                                   (word << 12) & M2, (word << 14) & M2, b[qd].z, b[qd].w);
-                }
-                ++piece_nk;
-                const bool seg_end = (cc.bp == a.KS - 1) || (base + i + 1 == u1);
-                if (seg_end) {
-                    pend_count = emit_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane,
-                               (c[0][0] + c[1][0]) + (c[2][0] + c[3][0]),
-                               (c[0][1] + c[1][1]) + (c[2][1] + c[3][1]),
-                               (c[0][2] + c[1][2]) + (c[2][2] + c[3][2]),
-                               (c[0][3] + c[1][3]) + (c[2][3] + c[3][3]), pend_r[warp],
-                               pend_add[warp], pend_count);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-                    piece_p = 0;
-                    piece_nk = 0;
-                }
-                cc.next(a, lane);
-                if (cc.bp == 0)
-                    xb = xs + ((cc.s - s_lo) * a.KS) * xstride + g * 4 + t;
-                else
-                    xb += xstride;
+                for (int qd = 0; qd < 4; ++qd) b[qd] = xb[i * XB + qd * XQ];
+                tile_mma(c, w, b);
             }
         }
+        piece_nk += cc.n;
+        if (cc.seg_end(a, u1)) {
+            // weights decode to +-2: halve (exact)
+            pend_count = emit_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane,
+                                    ((c[0][0] + c[1][0]) + (c[2][0] + c[3][0])) * 0.5f,
+                                    ((c[0][1] + c[1][1]) + (c[2][1] + c[3][1])) * 0.5f,
+                                    ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2])) * 0.5f,
+                                    ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3])) * 0.5f,
+                                    pend_r[warp], pend_add[warp], pend_count);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+            piece_p = 0;
+            piece_nk = 0;
+        }
+        // refill this slot with the chunk kSlots ahead
+        __syncwarp();
+        if (lane == 0 && pf.u < u1) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            bulk_load(ring_w + slot * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * slot);
+            pf.next(a, u1);
+        }
+        cc.next(a, u1);
+        slot = slot + 1 == kSlots ? 0 : slot + 1;
+    }
+    if (!ok) {
+        // a copy never landed: drain what is still in flight (bounded), then leave
+        for (int i = 0; i < kSlots; ++i) mbar_wait(bar_w + 8u * i, (phases >> i) & 1u, a.status);
+        return;
     }
     if (pend_count) commit_pieces(a, pend_r[warp], pend_add[warp], pend_count, lane);
 }
+
+using KernelFn = void (*)(GroupArgs);
+
+KernelFn kernel_for(int mode, int nt) {
+    const bool A = mode == TL_MODE_BF16;
+    switch (nt) {
+        case 1: return A ? tl_mma_kernel<true, 1> : tl_mma_kernel<false, 1>;
+        case 2: return A ? tl_mma_kernel<true, 2> : tl_mma_kernel<false, 2>;
+        case 4: return A ? tl_mma_kernel<true, 4> : tl_mma_kernel<false, 4>;
+        default: return A ? tl_mma_kernel<true, 8> : tl_mma_kernel<false, 8>;
+    }
+}
+
+inline int padded_tokens(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
 // ------------------------------------------------------------------ quant
 __global__ void __launch_bounds__(256)
@@ -460,8 +581,11 @@ tl_status device_info(DeviceInfo **out) {
         if (major != 10 || minor != 3) {
             d.init = -1;
         } else {
-            if (cudaFuncSetAttribute(tl_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemLimit) != cudaSuccess)
+            for (int mode = 0; mode < 2; ++mode)
+                for (int nt = 1; nt <= 8; nt *= 2)
+                    if (cudaFuncSetAttribute(kernel_for(mode, nt),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kRingBytes + kSmemLimit)) != cudaSuccess)
                 return TL_ERR_CUDA;
             const tl_status pst = tl_internal::prefill_init_device();
             if (pst != TL_OK) return pst;
@@ -500,7 +624,8 @@ void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     // slice segment within two warps (min warp range >= KS - 1) and keeps
     // the staged activations of one CTA within the shared-memory budget at
     // N = 8.  Chosen without looking at N.
-    const long long cta_units = ceil_div(p->U, p->P);
+    // a CTA covers kWarps consecutive warp ranges of ceil(U/V) units each
+    long long cta_units = kWarps * ceil_div(p->U, p->V);
     p->KS = 1;
     for (int d = 1; d <= p->KB && d <= kMaxSlice; ++d) {
         if (p->KB % d != 0 || d > avg + 1) continue;
@@ -521,8 +646,9 @@ void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     }
     // the per-CTA range may have grown above; size the staging for the final plan
     const long long su = (long long)p->R * p->KS;
-    const long long n_sl = std::min<long long>(p->S, ceil_div(ceil_div(p->U, p->P), su) + 1);
-    const int n = std::min(std::max(N, 1), kNMax);
+    cta_units = kWarps * ceil_div(p->U, p->V);
+    const long long n_sl = std::min<long long>(p->S, ceil_div(cta_units, su) + 1);
+    const int n = padded_tokens(std::min(std::max(N, 1), kNMax));
     p->smem = (size_t)n_sl * p->KS * 128 * n * 2;
     const size_t cnt_bytes = ((size_t)p->R * 8 + 255) / 256 * 256;
     p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * p->S * 2 * 16 * n * 4;
@@ -579,9 +705,10 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     }
     Plan p;
     make_plan(Ms, G, K, n, dev.sms, &p);
-    if (p.smem > kSmemLimit || p.U >= (1ll << 31)) return TL_ERR_SHAPE;
+    if (p.smem > kSmemLimit || p.U >= (1ll << 30)) return TL_ERR_SHAPE;
     if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
     a.R = p.R; a.KB = p.KB; a.KS = p.KS; a.S = p.S; a.K = K; a.U = p.U; a.V = p.V;
+    a.L = (int)ceil_div(p.U, p.V);
     const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
     a.X = static_cast<const char *>(X) + (size_t)n0 * K * xsz;
     a.s = s ? s + n0 : nullptr;
@@ -590,20 +717,22 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     const size_t cnt_bytes = ((size_t)p.R * 8 + 255) / 256 * 256;
     char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
     a.cnt = reinterpret_cast<unsigned long long *>(wsb);
+    a.status = static_cast<int *>(ws);
     a.part = reinterpret_cast<float *>(wsb + cnt_bytes);
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)p.P);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.smem;
+    cfg.dynamicSmemBytes = kRingBytes + p.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, tl_mma_kernel, a) != cudaSuccess) return TL_ERR_CUDA;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kernel_for(mode, padded_tokens(n)), a);
+    if (le != cudaSuccess) return TL_ERR_CUDA;
     return TL_OK;
 }
 
