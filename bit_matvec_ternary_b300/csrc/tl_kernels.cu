@@ -14,23 +14,29 @@
 //     of one mma n8 tile.
 //
 // Kernel tl_mma_kernel (N <= 8, modes A and B):
-//   Weights.  Each warp owns a contiguous range of (slice, 16-row tile,
-//   128-column block) units and streams them with cp.async.bulk into its own
-//   ring of shared-memory slots (one bulk copy moves up to 4 tiles, 2 KB,
-//   and completes on the slot's mbarrier).  A TL2P v1 tile is in
-//   mma.m16n8k16 A-fragment order: a lane's 16 bytes are 4 words, each
-//   covering two 16-column steps, and register f of a step is
+//   Work.  The launch's (16-row tile, 128-column block) units are ordered row
+//   tile by row tile; CTA c owns the contiguous range [c*Lc, (c+1)*Lc), so
+//   every CTA streams the same number of bytes and a row tile spans at most
+//   two CTAs.  Inside a CTA the k-range is processed in passes of KS blocks
+//   (the activations of one pass fit the staging buffer at 8 tokens); the 8
+//   warps split each pass's units into contiguous ranges.
+//   Weights.  Each warp streams its units with cp.async.bulk into its own
+//   ring of shared-memory slots (up to 4 tiles, 2 KB, per copy, completing
+//   on the slot's mbarrier), running ahead across passes.  A TL2P v1 tile is
+//   in mma.m16n8k16 A-fragment order: register f of a 16-column step is
 //   (word << 2q) & 0xC000C000, a bf16x2 pair of +-2.0 / +-0.0 -- one shift
-//   (IMAD, FMA pipe) and one AND (LOP3, ALU pipe) per two weights.  The
-//   tensor cores do the multiply-adds (bf16 x bf16 -> fp32, products exact).
-//   Activations.  Staged once per CTA in shared memory in B-fragment order
-//   (mode B converts int8 to bf16, exact).  Token columns n >= N read token
-//   N-1 (their results are discarded), so no lane is predicated off.
-//   Split-K.  Warp v owns units [v*L, min((v+1)*L, U)), L = ceil(U / warps).
-//   A row tile whose k-range spans several warps is finished by the warp
-//   that completes its arrival count (workspace counter); it adds the pieces
-//   in a fixed order, so results are deterministic and every token's result
-//   is independent of N.
+//   (IMAD, FMA pipe) and one AND (LOP3, ALU pipe) per two weights; the
+//   tensor cores do the multiply-adds (products exact, fp32 sums).
+//   Activations.  Staged per pass in shared memory in B-fragment order (mode
+//   B converts int8 to bf16, exact); columns n >= N repeat token N-1 and
+//   their results are discarded, so no lane is predicated off.
+//   Reduction.  A warp that covers all of a row tile's units in a pass adds
+//   its sum straight into the CTA's row accumulator (shared memory); rows
+//   split between warps go through per-warp boundary slots that are added in
+//   warp order after the pass.  A row tile cut by a CTA boundary is finished
+//   by whichever of its two CTAs arrives second (workspace counter), adding
+//   the two halves in a fixed order.  The plan never depends on N, so every
+//   token's result is bitwise independent of the batch.
 
 #include "tl.h"
 #include "tl_internal.cuh"
@@ -44,17 +50,15 @@
 
 namespace {
 
-constexpr int kWarps = 16;            // warps per CTA of the N <= 8 kernel (one CTA per SM)
+constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunkTiles = 4;        // tiles (512 B each) per bulk copy
 constexpr int kSlots = 3;             // bulk copies in flight per warp
-constexpr int kRingBytes = kWarps * kSlots * kChunkTiles * 512;   // 96 KB
+constexpr int kRingBytes = kWarps * kSlots * kChunkTiles * 512;   // 48 KB
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
-constexpr size_t kSmemLimit = 120 * 1024;   // activation staging budget per CTA
-constexpr int kMaxSlice = 32;         // 128-column blocks per split-K slice, at most
-constexpr int kMaxPending = 8;        // partial pieces a warp holds before publishing
-constexpr int kMaxSlices = 32;        // split-K slices per launch (one flag bit each)
+constexpr int kStageBlocks = 16;      // 128-column blocks per pass (32 KB at 8 tokens)
+constexpr int kMaxCtaRows = 32;       // row tiles one CTA may touch
 constexpr long long kWaitLimit = 1ll << 31;   // SM cycles before a wait gives up
 
 struct GroupArgs {
@@ -67,27 +71,21 @@ struct GroupArgs {
     int G;
     int R;          // row tiles in the launch
     int KB;         // 128-column blocks
-    int KS;         // blocks per slice
-    int S;          // slices
+    int KS;         // blocks per pass
+    int S;          // passes
     int K;
-    long long U;    // units = R * KB
-    long long V;    // warps in the grid
-    int L;          // units per warp (the last warps may get fewer or none)
+    int U;          // units = R * KB
+    int Lc;         // units per CTA (the last CTAs may get fewer)
     const void *X;  // bf16 [N][K] (mode A) or int8 [N][K] (mode B)
     const float *s;
     const int32_t *z;
     int N;
     int mode;
     int out;
-    float *part;    // split-K partials [R*S*2][N][16]
-    unsigned long long *cnt;  // [R] arrivals: low 32 bits = blocks summed so far,
-                              // bit 32+s = slice s arrived in two pieces; zero between launches
+    float *part;    // halves of CTA-split row tiles [R][2][N][16]
+    unsigned long long *cnt;  // [R] blocks arrived; zero between launches
     int *status;    // workspace status word
 };
-
-__device__ __forceinline__ int bnd(const GroupArgs &a, int v) {
-    return (int)min((long long)v * a.L, a.U);
-}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -112,10 +110,12 @@ __device__ __forceinline__ void griddep_launch() {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes (or the hint expires) instead of spinning.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -146,52 +146,123 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-// A run of consecutive tiles of one (slice, row tile) segment: at most
-// kChunkTiles, never across a segment or the warp's range end, so its bytes
-// are contiguous in the packed matrix.
-struct Chunk {
-    int u, s, r, bp, gi, rl, n;
+// ------------------------------------------------------------ work geometry
+// The CTA's unit range and the row tiles it touches.
+struct CtaGeo {
+    int cu0, cu1;           // units [cu0, cu1), unit = row_tile * KB + block
+    int r_first, r_last;    // row tiles touched (r_last < r_first: none)
+    int lo_first, hi_last;  // first block of r_first, one past the last block of r_last
+};
 
-    __device__ void seek(const GroupArgs &a, int u0, int u1) {
-        u = u0;
-        const int su = a.R * a.KS;
-        s = u0 / su;
-        const int rem = u0 - s * su;
-        r = rem / a.KS;
-        bp = rem - r * a.KS;
+__device__ __forceinline__ CtaGeo cta_geo(const GroupArgs &a, int c) {
+    CtaGeo g;
+    g.cu0 = min(c * a.Lc, a.U);
+    g.cu1 = min(g.cu0 + a.Lc, a.U);
+    if (g.cu1 > g.cu0) {
+        g.r_first = g.cu0 / a.KB;
+        g.r_last = (g.cu1 - 1) / a.KB;
+        g.lo_first = g.cu0 - g.r_first * a.KB;
+        g.hi_last = g.cu1 - g.r_last * a.KB;
+    } else {
+        g.r_first = 0; g.r_last = -1; g.lo_first = 0; g.hi_last = 0;
+    }
+    return g;
+}
+
+// Blocks [lo, hi) of row tile r that the CTA covers in pass s.
+__device__ __forceinline__ void row_span(const GroupArgs &a, const CtaGeo &g, int r, int s,
+                                         int &lo, int &hi) {
+    lo = max(r == g.r_first ? g.lo_first : 0, s * a.KS);
+    hi = min(r == g.r_last ? g.hi_last : a.KB, (s + 1) * a.KS);
+}
+
+__device__ __forceinline__ int row_count(const GroupArgs &a, const CtaGeo &g, int r, int s) {
+    int lo, hi;
+    row_span(a, g, r, s, lo, hi);
+    return max(0, hi - lo);
+}
+
+__device__ __forceinline__ int pass_units(const GroupArgs &a, const CtaGeo &g, int s) {
+    if (g.r_last < g.r_first) return 0;
+    const int c0 = row_count(a, g, g.r_first, s);
+    if (g.r_last == g.r_first) return c0;
+    return c0 + (g.r_last - g.r_first - 1) * a.KS + row_count(a, g, g.r_last, s);
+}
+
+// Row tile and block of the i-th unit of pass s in the CTA.
+__device__ __forceinline__ void pass_locate(const GroupArgs &a, const CtaGeo &g, int s, int i,
+                                            int &r, int &b) {
+    int lo, hi;
+    row_span(a, g, g.r_first, s, lo, hi);
+    const int c0 = max(0, hi - lo);
+    if (i < c0) { r = g.r_first; b = lo + i; return; }
+    const int j = i - c0;
+    const int mid = g.r_last > g.r_first ? (g.r_last - g.r_first - 1) * a.KS : 0;
+    if (j < mid) { r = g.r_first + 1 + j / a.KS; b = s * a.KS + j % a.KS; return; }
+    row_span(a, g, g.r_last, s, lo, hi);
+    r = g.r_last;
+    b = lo + (j - mid);
+}
+
+// A warp's walk over its units, pass after pass, in chunks: runs of at most
+// kChunkTiles consecutive blocks of one row tile (contiguous in memory).
+struct Walk {
+    int s, i, iend;          // pass, unit index in the pass, end of the warp's range
+    int r, b, row_hi;        // current row tile, block, end block of the row in this pass
+    int gi, rl;              // matrix of the group and its local row tile
+    int n;                   // tiles in the current chunk (0: done)
+
+    __device__ void map_row(const GroupArgs &a) {
         gi = 0;
         while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
         rl = r - a.rt_off[gi];
-        size(a, u1);
     }
-    __device__ __forceinline__ void size(const GroupArgs &a, int u1) {
-        n = min(kChunkTiles, min(a.KS - bp, u1 - u));
-    }
-    __device__ __forceinline__ void next(const GroupArgs &a, int u1) {
-        u += n;
-        bp += n;
-        if (bp == a.KS) {
-            bp = 0;
-            if (++r == a.R) {
-                r = 0; ++s; gi = 0; rl = 0;
-            } else if (r == a.rt_off[gi + 1]) {
-                ++gi; rl = 0;
-            } else {
-                ++rl;
+    __device__ void enter(const GroupArgs &a, const CtaGeo &g, int w) {
+        // from pass s on: the first pass in which warp w has units
+        for (; s < a.S; ++s) {
+            const int np = pass_units(a, g, s);
+            const int lw = (np + kWarps - 1) / kWarps;
+            i = min(w * lw, np);
+            iend = min(i + lw, np);
+            if (i < iend) {
+                pass_locate(a, g, s, i, r, b);
+                int lo;
+                row_span(a, g, r, s, lo, row_hi);
+                map_row(a);
+                n = min(kChunkTiles, min(iend - i, row_hi - b));
+                return;
             }
         }
-        size(a, u1);
+        n = 0;
+    }
+    __device__ void start(const GroupArgs &a, const CtaGeo &g, int w) {
+        s = 0;
+        enter(a, g, w);
+    }
+    __device__ void next(const GroupArgs &a, const CtaGeo &g, int w) {
+        i += n;
+        b += n;
+        if (i >= iend) {
+            ++s;
+            enter(a, g, w);
+            return;
+        }
+        if (b >= row_hi) {
+            ++r;
+            int lo;
+            row_span(a, g, r, s, lo, row_hi);
+            b = lo;
+            map_row(a);
+        }
+        n = min(kChunkTiles, min(iend - i, row_hi - b));
     }
     __device__ __forceinline__ const char *src(const GroupArgs &a) const {
-        return a.packed[gi] + ((long long)rl * a.KB + (long long)s * a.KS + bp) * 512;
-    }
-    __device__ __forceinline__ bool seg_end(const GroupArgs &a, int u1) const {
-        return bp + n == a.KS || u + n == u1;
+        return a.packed[gi] + ((long long)rl * a.KB + b) * 512;
     }
 };
 
-// Y[n][m] from the scaled sum y_acc = sum_k w*x (mode A) or the exact
-// integer sum_k w*q (mode B).
+// ------------------------------------------------------------ epilogue
+// Y[n][m] from acc_y = sum_k w*x (mode A) or the exact integer sum_k w*q (mode B).
 __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int n, float acc) {
     const int M = a.M[gi];
     float y;
@@ -212,107 +283,22 @@ __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int
         reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * M + m] = __float2bfloat16_rn(y);
 }
 
-__device__ __forceinline__ void epilogue(const GroupArgs &a, int gi, int rl, int g, int t,
-                                         const float (&c)[4]) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int m = rl * 16 + g + 8 * h;
-            const int n = 2 * t + e;
-            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, c[2 * h + e]);
-        }
-}
-
-// Sum every piece of row tile r in fixed (slice, piece) order and store Y.
-// Called by the warp whose arrival completed the row tile's count; `split`
-// has bit s set when slice s came in two pieces.
-__device__ __noinline__ void reduce_row_tile(const GroupArgs &a, int r, unsigned split,
-                                             int lane) {
+// The 16 x N results of row tile r held as acc[n * 16 + row] (sums of +-2
+// weights: halved here, exactly).  One warp; lane (g, t) stores rows g, g+8
+// of tokens 2t, 2t+1.
+__device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const float *acc,
+                                               int lane) {
     const int g = lane >> 2, t = lane & 3;
     int gi = 0;
     while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
     const int rl = r - a.rt_off[gi];
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int ss = 0; ss < a.S; ++ss) {
-        const int pieces = ((split >> ss) & 1u) ? 2 : 1;
-        for (int pp = 0; pp < pieces; ++pp) {
-            const float *src = a.part + (((long long)r * a.S + ss) * 2 + pp) * a.N * 16;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int n = 2 * t + e;
-                    if (n < a.N) acc[2 * h + e] += __ldcg(src + n * 16 + g + 8 * h);
-                }
-        }
-    }
-    epilogue(a, gi, rl, g, t, acc);
-    if (lane == 0) a.cnt[r] = 0ull;
-}
-
-// Publish this warp's pending pieces.  The lanes' partial-sum stores are
-// ordered before lane 0's counter update by __syncwarp, and the update is a
-// release (and acquire) at GPU scope, so the warp that completes a row tile's
-// count sees every piece; it then reduces the row tile.  No full fence.
-__device__ __forceinline__ unsigned long long atomic_add_acq_rel(unsigned long long *p,
-                                                                 unsigned long long v) {
-    unsigned long long old;
-    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
-                 : "=l"(old)
-                 : "l"(p), "l"(v)
-                 : "memory");
-    return old;
-}
-
-__device__ __noinline__ void commit_pieces(const GroupArgs &a, const int *pend_r,
-                                           const unsigned long long *pend_add, int count,
-                                           int lane) {
-    __syncwarp();
-    for (int i = 0; i < count; ++i) {
-        const int r = pend_r[i];
-        unsigned long long now = 0ull;
-        if (lane == 0) now = atomic_add_acq_rel(a.cnt + r, pend_add[i]) + pend_add[i];
-        now = __shfl_sync(0xffffffffu, now, 0);
-        if ((unsigned)(now & 0xffffffffull) == (unsigned)a.KB) {
-            __syncwarp();
-            reduce_row_tile(a, r, (unsigned)(now >> 32), lane);
-        }
-    }
-}
-
-// Emit one piece (row tile r, slice s, piece p, nk blocks): the final result
-// when it covers the whole k-range, else its partial sums go to the workspace
-// and the piece joins the warp's pending list.  Returns the new list length.
-__device__ __noinline__ int emit_piece(const GroupArgs &a, int r, int s, int p, int nk, int gi,
-                                       int rl, int lane, float c0, float c1, float c2, float c3,
-                                       int *pend_r, unsigned long long *pend_add,
-                                       int pend_count) {
-    const int g = lane >> 2, t = lane & 3;
-    const float c[4] = {c0, c1, c2, c3};
-    if (a.S == 1 && nk == a.KB) {   // the whole k-range in one piece: final
-        epilogue(a, gi, rl, g, t, c);
-        return pend_count;
-    }
-    const long long slot = ((long long)r * a.S + s) * 2 + p;
-    float *dst = a.part + slot * a.N * 16;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int n = 2 * t + e;
-            if (n < a.N) __stcg(dst + n * 16 + g + 8 * h, c[2 * h + e]);
+            const int m = rl * 16 + g + 8 * h, n = 2 * t + e;
+            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, acc[n * 16 + g + 8 * h] * 0.5f);
         }
-    if (lane == 0) {
-        pend_r[pend_count] = r;
-        pend_add[pend_count] = (unsigned long long)nk | ((unsigned long long)p << (32 + s));
-    }
-    __syncwarp();
-    if (++pend_count == kMaxPending) {
-        commit_pieces(a, pend_r, pend_add, pend_count, lane);
-        pend_count = 0;
-    }
-    return pend_count;
 }
 
 // One 128-column block of one 16-row tile: 8 MMAs over the lane's 16-byte
@@ -329,160 +315,219 @@ __device__ __forceinline__ void tile_mma(float (&c)[4][4], const uint4 &w, const
     }
 }
 
+// ------------------------------------------------------------ kernel
 // kModeA: bf16 activations (else int8 from the quantiser).  NT: token
-// columns staged (a power of two >= N; columns n >= N repeat token N-1 and
-// their results are discarded).
+// columns staged (a power of two >= N).
 template <bool kModeA, int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads)
 tl_mma_kernel(const __grid_constant__ GroupArgs a) {
+    constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
+    constexpr int XB = 4 * XQ;                  // uint4 per 128-column block
+    constexpr int RV = 16 * NT;                 // floats per row-tile result
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ring = smem;                                    // [kWarps][kSlots][2 KB]
-    uint4 *xs = reinterpret_cast<uint4 *>(smem + kRingBytes); // staged activations
+    uint8_t *ring = smem;                                              // [kWarps][kSlots][2 KB]
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + kRingBytes);          // one pass of X
+    float *acc = reinterpret_cast<float *>(smem + kRingBytes + a.KS * XB * 16);  // [rows][RV]
+    __shared__ float bslot[kWarps][2][RV];      // boundary pieces of the current pass
+    __shared__ int bslot_row[kWarps][2];
     __shared__ __align__(8) unsigned long long bars[kWarps][kSlots];
-    __shared__ int pend_r[kWarps][kMaxPending];
-    __shared__ unsigned long long pend_add[kWarps][kMaxPending];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int v = blockIdx.x * kWarps + warp;
-    const int u0 = bnd(a, v), u1 = bnd(a, v + 1);
-    const int cu0 = bnd(a, blockIdx.x * kWarps), cu1 = bnd(a, (blockIdx.x + 1) * kWarps);
-    const int su = a.R * a.KS;
-    const int s_lo = cu0 / su;
-    const int n_sl = cu1 > cu0 ? (cu1 - 1) / su - s_lo + 1 : 0;
+    const CtaGeo geo = cta_geo(a, blockIdx.x);
+    const int nrows = geo.r_last - geo.r_first + 1;
     const int N = a.N;
 
     if (threadIdx.x < kWarps * kSlots)
         mbar_init(smem_u32(&bars[0][0]) + 8u * threadIdx.x, 1);
+    if (threadIdx.x < kWarps * 2) (&bslot_row[0][0])[threadIdx.x] = -1;
+    for (int i = threadIdx.x; i < nrows * RV; i += kThreads) acc[i] = 0.f;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
 
     // Weights do not depend on the previous kernel: start the bulk copies
-    // before waiting for it.
+    // before waiting for it.  The producer (lane 0) runs kSlots chunks ahead
+    // of the consumer, across pass boundaries.
     const uint32_t ring_w = smem_u32(ring) + warp * (kSlots * kChunkTiles * 512);
     const uint32_t bar_w = smem_u32(&bars[warp][0]);
-    Chunk pf;
-    pf.seek(a, u0, u1);
+    Walk pf;
+    pf.start(a, geo, warp);
     if (lane == 0)
-        for (int i = 0; i < kSlots && pf.u < u1; ++i) {
-            bulk_load(ring_w + i * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * i);
-            pf.next(a, u1);
+        for (int k = 0; k < kSlots && pf.n > 0; ++k) {
+            bulk_load(ring_w + k * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * k);
+            pf.next(a, geo, warp);
         }
     griddep_wait();
     griddep_launch();
 
-    // ---- stage X for this CTA's slices in B-fragment order:
-    // word ((((sl*KS + bp)*4 + qd)*NT + n)*4 + t)*4 + w holds x[n'][k], x[n'][k+1],
-    // n' = min(n, N-1), k = ((s_lo+sl)*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
-    {
-        const int words = n_sl * a.KS * 64 * NT;
-        uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
-        for (int idx = threadIdx.x; idx < words; idx += kThreads) {
-            const int w = idx & 3, tt = (idx >> 2) & 3;
-            const int n = min((idx >> 4) % NT, N - 1);
-            int rest = (idx >> 4) / NT;
-            const int qd = rest & 3;
-            rest >>= 2;
-            const int bp = rest % a.KS;
-            const int sl = rest / a.KS;
-            const int k = ((s_lo + sl) * a.KS + bp) * 128 + 16 * (2 * qd + (w >> 1)) + 2 * tt +
-                          8 * (w & 1);
-            uint32_t lo = 0, hi = 0;
-            if (kModeA) {
-                const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
-                if (k < a.K) lo = x[k];
-                if (k + 1 < a.K) hi = x[k + 1];
-            } else {
-                const int8_t *x = reinterpret_cast<const int8_t *>(a.X) + (long long)n * a.K;
-                if (k < a.K) lo = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k]));
-                if (k + 1 < a.K) hi = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k + 1]));
-            }
-            xw[idx] = lo | (hi << 16);
-        }
-    }
-    __syncthreads();
-
-    // ---- stream the warp's units
-    constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
-    constexpr int XB = 4 * XQ;                  // uint4 per 128-column block
-    float c[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-    int pend_count = 0;
-    int piece_nk = 0;
-    Chunk cc;
-    cc.seek(a, u0, u1);
-    int piece_p = cc.bp == 0 ? 0 : 1;
+    Walk cw;
+    cw.start(a, geo, warp);
     int slot = 0;
     uint32_t phases = 0;                        // parity bit per slot
     bool ok = true;
+    float c[4][4];
 
-    while (cc.u < u1) {
-        const bool got = __all_sync(0xffffffffu, mbar_wait(bar_w + 8u * slot, (phases >> slot) & 1u,
-                                                            a.status));
-        if (!got) { ok = false; break; }
-        phases ^= 1u << slot;
-        const uint4 *tiles = reinterpret_cast<const uint4 *>(
-            ring + warp * (kSlots * kChunkTiles * 512) + slot * (kChunkTiles * 512)) + lane;
-        const uint4 *xb = xs + ((cc.s - s_lo) * a.KS + cc.bp) * XB + (g % NT) * 4 + t;
-        if (cc.n == kChunkTiles) {
-            // full chunk: load tile i+1 while tile i is multiplied
-            uint4 w = tiles[0];
-            uint4 b[4];
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) b[qd] = xb[qd * XQ];
-#pragma unroll
-            for (int i = 0; i < kChunkTiles; ++i) {
-                uint4 wn = w, bn[4] = {b[0], b[1], b[2], b[3]};
-                if (i + 1 < kChunkTiles) {
-                    wn = tiles[(i + 1) * 32];
-#pragma unroll
-                    for (int qd = 0; qd < 4; ++qd) bn[qd] = xb[(i + 1) * XB + qd * XQ];
+    for (int s = 0; s < a.S; ++s) {
+        // ---- stage X for pass s in B-fragment order:
+        // word ((((bp*4 + qd)*NT + n)*4 + t)*4 + w) holds x[n'][k], x[n'][k+1],
+        // n' = min(n, N-1), k = (s*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
+        {
+            const int words = a.KS * 64 * NT;
+            uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
+            for (int idx = threadIdx.x; idx < words; idx += kThreads) {
+                const int w = idx & 3, tt = (idx >> 2) & 3;
+                const int n = min((idx >> 4) % NT, N - 1);
+                const int rest = (idx >> 4) / NT;
+                const int qd = rest & 3, bp = rest >> 2;
+                const int k = (s * a.KS + bp) * 128 + 16 * (2 * qd + (w >> 1)) + 2 * tt + 8 * (w & 1);
+                uint32_t lo = 0, hi = 0;
+                if (kModeA) {
+                    const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
+                    if (k < a.K) lo = x[k];
+                    if (k + 1 < a.K) hi = x[k + 1];
+                } else {
+                    const int8_t *x = reinterpret_cast<const int8_t *>(a.X) + (long long)n * a.K;
+                    if (k < a.K) lo = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k]));
+                    if (k + 1 < a.K) hi = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k + 1]));
                 }
-                tile_mma(c, w, b);
-                w = wn;
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) b[qd] = bn[qd];
-            }
-        } else {
-            for (int i = 0; i < cc.n; ++i) {
-                const uint4 w = tiles[i * 32];
-                uint4 b[4];
-#pragma unroll
-                for (int qd = 0; qd < 4; ++qd) b[qd] = xb[i * XB + qd * XQ];
-                tile_mma(c, w, b);
+                xw[idx] = lo | (hi << 16);
             }
         }
-        piece_nk += cc.n;
-        if (cc.seg_end(a, u1)) {
-            // weights decode to +-2: halve (exact)
-            pend_count = emit_piece(a, cc.r, cc.s, piece_p, piece_nk, cc.gi, cc.rl, lane,
-                                    ((c[0][0] + c[1][0]) + (c[2][0] + c[3][0])) * 0.5f,
-                                    ((c[0][1] + c[1][1]) + (c[2][1] + c[3][1])) * 0.5f,
-                                    ((c[0][2] + c[1][2]) + (c[2][2] + c[3][2])) * 0.5f,
-                                    ((c[0][3] + c[1][3]) + (c[2][3] + c[3][3])) * 0.5f,
-                                    pend_r[warp], pend_add[warp], pend_count);
+        __syncthreads();
+
+        // ---- this warp's units of pass s
+        int run_lo = cw.b, nslot = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-            piece_p = 0;
-            piece_nk = 0;
+        for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+        while (ok && cw.n > 0 && cw.s == s) {
+            const bool got = __all_sync(0xffffffffu,
+                                        mbar_wait(bar_w + 8u * slot, (phases >> slot) & 1u, a.status));
+            if (!got) { ok = false; break; }
+            phases ^= 1u << slot;
+            const uint4 *tiles = reinterpret_cast<const uint4 *>(
+                ring + warp * (kSlots * kChunkTiles * 512) + slot * (kChunkTiles * 512)) + lane;
+            const uint4 *xb = xs + (cw.b - s * a.KS) * XB + (g % NT) * 4 + t;
+            if (cw.n == kChunkTiles) {
+                // full chunk: load tile i+1 while tile i is multiplied
+                uint4 w = tiles[0];
+                uint4 bq[4];
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd) bq[qd] = xb[qd * XQ];
+#pragma unroll
+                for (int i = 0; i < kChunkTiles; ++i) {
+                    uint4 wn = w, bn[4] = {bq[0], bq[1], bq[2], bq[3]};
+                    if (i + 1 < kChunkTiles) {
+                        wn = tiles[(i + 1) * 32];
+#pragma unroll
+                        for (int qd = 0; qd < 4; ++qd) bn[qd] = xb[(i + 1) * XB + qd * XQ];
+                    }
+                    tile_mma(c, w, bq);
+                    w = wn;
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) bq[qd] = bn[qd];
+                }
+            } else {
+                for (int i = 0; i < cw.n; ++i) {
+                    const uint4 w = tiles[i * 32];
+                    uint4 bq[4];
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) bq[qd] = xb[i * XB + qd * XQ];
+                    tile_mma(c, w, bq);
+                }
+            }
+            // end of a run of one row tile: this chunk ends the row or the warp's range
+            const bool run_end = (cw.b + cw.n == cw.row_hi) || (cw.i + cw.n == cw.iend);
+            if (run_end) {
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = (c[0][q] + c[1][q]) + (c[2][q] + c[3][q]);
+                int lo, hi;
+                row_span(a, geo, cw.r, s, lo, hi);
+                const int rho = cw.r - geo.r_first;
+                // lane (g, t) holds rows g, g+8 of tokens 2t, 2t+1
+                if (run_lo == lo && cw.b + cw.n == hi) {
+                    // the whole row tile of this pass: no other warp touches it
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if (2 * t + e < NT) acc[rho * RV + (2 * t + e) * 16 + g + 8 * h] += v[2 * h + e];
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if (2 * t + e < NT) bslot[warp][nslot][(2 * t + e) * 16 + g + 8 * h] = v[2 * h + e];
+                    if (lane == 0) bslot_row[warp][nslot] = rho;
+                    ++nslot;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+                run_lo = cw.b + cw.n < cw.row_hi ? cw.b + cw.n : -1;   // next run starts a row
+            }
+            // refill this slot with the chunk kSlots ahead
+            __syncwarp();
+            if (lane == 0 && pf.n > 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                bulk_load(ring_w + slot * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * slot);
+                pf.next(a, geo, warp);
+            }
+            cw.next(a, geo, warp);
+            if (run_lo < 0) run_lo = cw.b;
+            slot = slot + 1 == kSlots ? 0 : slot + 1;
         }
-        // refill this slot with the chunk kSlots ahead
-        __syncwarp();
-        if (lane == 0 && pf.u < u1) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            bulk_load(ring_w + slot * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * slot);
-            pf.next(a, u1);
+        __syncthreads();
+        // ---- boundary pieces of pass s, added in warp order (one thread per element)
+        if (threadIdx.x < RV) {
+            for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int rho = bslot_row[w][k];
+                    if (rho >= 0) acc[rho * RV + threadIdx.x] += bslot[w][k][threadIdx.x];
+                }
         }
-        cc.next(a, u1);
-        slot = slot + 1 == kSlots ? 0 : slot + 1;
+        __syncthreads();
+        if (threadIdx.x < kWarps * 2) (&bslot_row[0][0])[threadIdx.x] = -1;
+        // (the next pass's staging __syncthreads orders this reset before reuse)
     }
     if (!ok) {
         // a copy never landed: drain what is still in flight (bounded), then leave
-        for (int i = 0; i < kSlots; ++i) mbar_wait(bar_w + 8u * i, (phases >> i) & 1u, a.status);
+        for (int k = 0; k < kSlots; ++k) mbar_wait(bar_w + 8u * k, (phases >> k) & 1u, a.status);
         return;
     }
-    if (pend_count) commit_pieces(a, pend_r[warp], pend_add[warp], pend_count, lane);
+
+    // ---- results: rows covered entirely by this CTA go straight to Y; a row
+    // tile cut by a CTA boundary is finished by the second of its two CTAs.
+    for (int rho = warp; rho < nrows; rho += kWarps) {
+        const int r = geo.r_first + rho;
+        const int lo = r == geo.r_first ? geo.lo_first : 0;
+        const int hi = r == geo.r_last ? geo.hi_last : a.KB;
+        const float *v = acc + rho * RV;
+        if (lo == 0 && hi == a.KB) {
+            store_row_tile(a, r, v, lane);
+            continue;
+        }
+        const int half = lo == 0 ? 0 : 1;       // 0: holds block 0 of the row
+        float *dst = a.part + ((long long)r * 2 + half) * N * 16;
+        for (int e = lane; e < N * 16; e += 32) __stcg(dst + e, v[e]);
+        __syncwarp();
+        unsigned long long now = 0ull;
+        if (lane == 0) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            now = atomicAdd(a.cnt + r, (unsigned long long)(hi - lo)) + (unsigned long long)(hi - lo);
+        }
+        now = __shfl_sync(0xffffffffu, now, 0);
+        if (now == (unsigned long long)a.KB) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            const float *h0 = a.part + (long long)r * 2 * N * 16;
+            // combine the halves (block-0 half first) through this CTA's acc row
+            for (int e = lane; e < N * 16; e += 32)
+                acc[rho * RV + e] = __ldcg(h0 + e) + __ldcg(h0 + N * 16 + e);
+            __syncwarp();
+            store_row_tile(a, r, acc + rho * RV, lane);
+            if (lane == 0) a.cnt[r] = 0ull;
+        }
+    }
 }
 
 using KernelFn = void (*)(GroupArgs);
@@ -561,11 +606,14 @@ tl_quant_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Q,
 }
 
 // ------------------------------------------------------------------ host side
+
 struct DeviceInfo {
     int init;     // 0 = unknown, 1 = ok, -1 = unsupported
     int sms;
 };
 DeviceInfo g_dev[kMaxDevices];
+
+constexpr int kMaxDynSmem = kRingBytes + kStageBlocks * 128 * kNMax * 2 + kMaxCtaRows * 16 * kNMax * 4;
 
 tl_status device_info(DeviceInfo **out) {
     int dev = 0;
@@ -585,8 +633,8 @@ tl_status device_info(DeviceInfo **out) {
                 for (int nt = 1; nt <= 8; nt *= 2)
                     if (cudaFuncSetAttribute(kernel_for(mode, nt),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(kRingBytes + kSmemLimit)) != cudaSuccess)
-                return TL_ERR_CUDA;
+                                             kMaxDynSmem) != cudaSuccess)
+                        return TL_ERR_CUDA;
             const tl_status pst = tl_internal::prefill_init_device();
             if (pst != TL_OK) return pst;
             d.sms = sms;
@@ -599,9 +647,9 @@ tl_status device_info(DeviceInfo **out) {
 }
 
 struct Plan {
-    int R, KB, KS, S, P;
-    long long U, V;
-    size_t smem;       // for the given N
+    int R, KB, KS, S, P, Lc, rows;
+    long long U;
+    size_t smem;       // dynamic shared memory for the given N
     size_t ws_bytes;   // workspace for the given N
 };
 
@@ -609,53 +657,36 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // The plan depends on the shapes and the SM count only, never on N, so every
 // token is summed in the same order whatever the batch.
-void make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
+tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     p->R = 0;
     for (int g = 0; g < G; ++g) p->R += (int)ceil_div(Ms[g], 16);
     p->KB = (int)ceil_div(K, 128);
     p->U = (long long)p->R * p->KB;
-    long long ctas = sms;                       // one CTA of kWarps warps per SM
-    ctas = std::min<long long>(ctas, ceil_div(p->U, (long long)kWarps * 2));
-    if (ctas < 1) ctas = 1;
-    p->P = (int)ctas;
-    p->V = ctas * kWarps;
-    const long long avg = p->U / p->V;
-    // Largest slice (in 128-column blocks) that divides KB, keeps every
-    // slice segment within two warps (min warp range >= KS - 1) and keeps
-    // the staged activations of one CTA within the shared-memory budget at
-    // N = 8.  Chosen without looking at N.
-    // a CTA covers kWarps consecutive warp ranges of ceil(U/V) units each
-    long long cta_units = kWarps * ceil_div(p->U, p->V);
+    if (p->U >= (1ll << 30)) return TL_ERR_SHAPE;
+    // passes: the largest divisor of KB not above kStageBlocks
     p->KS = 1;
-    for (int d = 1; d <= p->KB && d <= kMaxSlice; ++d) {
-        if (p->KB % d != 0 || d > avg + 1) continue;
-        const long long su = (long long)p->R * d;
-        const long long n_sl = std::min<long long>(p->KB / d, ceil_div(cta_units, su) + 1);
-        if ((size_t)n_sl * d * 128 * kNMax * 2 <= kSmemLimit) p->KS = d;
-    }
+    for (int d = 1; d <= std::min(p->KB, kStageBlocks); ++d)
+        if (p->KB % d == 0) p->KS = d;
     p->S = p->KB / p->KS;
-    if (p->S > kMaxSlices) {                // fewer warps, longer slices
-        p->KS = (int)ceil_div(p->KB, kMaxSlices);
-        while (p->KB % p->KS) ++p->KS;
-        p->S = p->KB / p->KS;
-        const long long need_avg = p->KS - 1;       // min warp range >= KS - 1
-        long long V = need_avg > 0 ? p->U / need_avg : p->V;
-        V = std::max<long long>(kWarps, std::min<long long>(V, p->V)) / kWarps * kWarps;
-        p->V = V;
-        p->P = (int)(V / kWarps);
-    }
-    // the per-CTA range may have grown above; size the staging for the final plan
-    const long long su = (long long)p->R * p->KS;
-    cta_units = kWarps * ceil_div(p->U, p->V);
-    const long long n_sl = std::min<long long>(p->S, ceil_div(cta_units, su) + 1);
-    const int n = padded_tokens(std::min(std::max(N, 1), kNMax));
-    p->smem = (size_t)n_sl * p->KS * 128 * n * 2;
+    // CTAs: at most one per SM, and ranges of at least KB - 1 units so a row
+    // tile never spans more than two CTAs
+    long long P = sms;
+    if (p->KB > 1) P = std::min<long long>(P, std::max<long long>(1, p->U / (p->KB - 1)));
+    else P = std::min<long long>(P, p->U);
+    p->P = (int)std::max<long long>(1, P);
+    p->Lc = (int)ceil_div(p->U, p->P);
+    p->rows = (int)(ceil_div(p->Lc + p->KB - 1, p->KB) + 1);
+    p->rows = std::min(p->rows, p->R);
+    if (p->rows > kMaxCtaRows) return TL_ERR_SHAPE;
+    const int nt = padded_tokens(std::min(std::max(N, 1), kNMax));
+    const int n = std::min(std::max(N, 1), kNMax);
+    p->smem = (size_t)kRingBytes + (size_t)p->KS * 128 * nt * 2 + (size_t)p->rows * 16 * nt * 4;
     const size_t cnt_bytes = ((size_t)p->R * 8 + 255) / 256 * 256;
-    p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * p->S * 2 * 16 * n * 4;
+    p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * 2 * 16 * n * 4;
+    return TL_OK;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 tl_status check_weights(const tl_weight *Ws, int G, int mode) {
     if (!Ws) return TL_ERR_NULL;
     if (G < 1 || G > TL_MAX_GROUP) return TL_ERR_SHAPE;
@@ -680,7 +711,7 @@ size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
         return std::max(tl_internal::prefill_workspace_bytes(N, K, TL_MODE_BF16),
                         tl_internal::prefill_workspace_bytes(N, K, TL_MODE_I8));
     Plan p;
-    make_plan(Ms, G, K, N, sms, &p);
+    if (make_plan(Ms, G, K, N, sms, &p) != TL_OK) return 0;
     return p.ws_bytes;
 }
 
@@ -704,11 +735,10 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
         a.rt_off[g + 1] = a.rt_off[g] + (int)ceil_div(Ws[g].M, 16);
     }
     Plan p;
-    make_plan(Ms, G, K, n, dev.sms, &p);
-    if (p.smem > kSmemLimit || p.U >= (1ll << 30)) return TL_ERR_SHAPE;
+    const tl_status pst = make_plan(Ms, G, K, n, dev.sms, &p);
+    if (pst != TL_OK) return pst;
     if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
-    a.R = p.R; a.KB = p.KB; a.KS = p.KS; a.S = p.S; a.K = K; a.U = p.U; a.V = p.V;
-    a.L = (int)ceil_div(p.U, p.V);
+    a.R = p.R; a.KB = p.KB; a.KS = p.KS; a.S = p.S; a.K = K; a.U = (int)p.U; a.Lc = p.Lc;
     const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
     a.X = static_cast<const char *>(X) + (size_t)n0 * K * xsz;
     a.s = s ? s + n0 : nullptr;
@@ -717,14 +747,14 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     const size_t cnt_bytes = ((size_t)p.R * 8 + 255) / 256 * 256;
     char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
     a.cnt = reinterpret_cast<unsigned long long *>(wsb);
-    a.status = static_cast<int *>(ws);
     a.part = reinterpret_cast<float *>(wsb + cnt_bytes);
+    a.status = static_cast<int *>(ws);
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)p.P);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kRingBytes + p.smem;
+    cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -747,7 +777,8 @@ tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t 
     int Ms[TL_MAX_GROUP];
     for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
     Plan p;
-    make_plan(Ms, G, Ws[0].K, kNMax, dev->sms, &p);   // chunks never exceed 8 tokens
+    const tl_status pst = make_plan(Ms, G, Ws[0].K, kNMax, dev->sms, &p);  // chunks <= 8 tokens
+    if (pst != TL_OK) return pst;
     *need = p.ws_bytes;
     *zeroed = kStatusBytes + ((size_t)p.R * 8 + 255) / 256 * 256;
     return TL_OK;

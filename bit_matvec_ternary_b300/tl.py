@@ -36,7 +36,7 @@ TL_MAX_GROUP = 4
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
            "tl_quantize_act", "tl_linear", "tl_linear_group", "tl_linear_noalloc",
            "tl_status_string", "tl_version")
-TL_NOALLOC_SCRATCH_BYTES = 8 << 20
+TL_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class tl_weight(C.Structure):

@@ -163,9 +163,10 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
                           int out_dtype, void *workspace, size_t workspace_bytes,
                           unsigned flags, void *stream);
 
-/* Size of the library's fixed scratch array for tl_linear_noalloc (8 MiB):
- * enough for every Qwen3-8B-shaped matrix at up to 8 tokens per chunk. */
-#define TL_NOALLOC_SCRATCH_BYTES (8u << 20)
+/* Size of the library's fixed scratch array for tl_linear_noalloc (4 MiB):
+ * enough for every Qwen3-8B-shaped matrix at up to 8 tokens per chunk, and
+ * for any matrix of up to 65,024 rows. */
+#define TL_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* DEVICE.  tl_linear for callers that cannot allocate device memory.
  * The pages describe no such call; it exists for users of this library who
