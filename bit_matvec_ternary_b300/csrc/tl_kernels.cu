@@ -18,7 +18,7 @@
 //   tile by row tile; CTA c owns the contiguous range [c*Lc, (c+1)*Lc), so
 //   every CTA streams the same number of bytes and a row tile spans at most
 //   two CTAs.  Inside a CTA the k-range is processed in passes of KS blocks
-//   (the activations of one pass fit the staging buffer at 8 tokens); the 8
+//   (the activations of one pass fit the staging buffer at 8 tokens); the 16
 //   warps split each pass's units into contiguous ranges.
 //   Weights.  Each warp streams its units with cp.async.bulk into its own
 //   ring of shared-memory slots (up to 4 tiles, 2 KB, per copy, completing
@@ -50,11 +50,11 @@
 
 namespace {
 
-constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
+constexpr int kWarps = 16;            // warps per CTA of the N <= 8 kernel (one CTA per SM)
 constexpr int kThreads = kWarps * 32;
 constexpr int kChunkTiles = 4;        // tiles (512 B each) per bulk copy
-constexpr int kSlots = 3;             // bulk copies in flight per warp
-constexpr int kRingBytes = kWarps * kSlots * kChunkTiles * 512;   // 48 KB
+constexpr int kSlots = 2;             // bulk copies in flight per warp
+constexpr int kRingBytes = kWarps * kSlots * kChunkTiles * 512;   // 64 KB
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
 constexpr int kStageBlocks = 16;      // 128-column blocks per pass (32 KB at 8 tokens)
@@ -305,14 +305,16 @@ __device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const 
 // slice of the tile (w) and the 4 B-fragment quarters (b).
 __device__ __forceinline__ void tile_mma(float (&c)[4][4], const uint4 &w, const uint4 (&b)[4]) {
     const uint32_t M2 = 0xC000C000u;
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    // four independent accumulator chains; consecutive MMAs never share one
 #pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-        const uint32_t word = qd == 0 ? w.x : qd == 1 ? w.y : qd == 2 ? w.z : w.w;
-        mma_bf16_16816(c[qd], word & M2, (word << 2) & M2, (word << 4) & M2, (word << 6) & M2,
-                       b[qd].x, b[qd].y);
-        mma_bf16_16816(c[qd], (word << 8) & M2, (word << 10) & M2, (word << 12) & M2,
-                       (word << 14) & M2, b[qd].z, b[qd].w);
-    }
+    for (int qd = 0; qd < 4; ++qd)
+        mma_bf16_16816(c[qd], wd[qd] & M2, (wd[qd] << 2) & M2, (wd[qd] << 4) & M2,
+                       (wd[qd] << 6) & M2, b[qd].x, b[qd].y);
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd)
+        mma_bf16_16816(c[qd], (wd[qd] << 8) & M2, (wd[qd] << 10) & M2, (wd[qd] << 12) & M2,
+                       (wd[qd] << 14) & M2, b[qd].z, b[qd].w);
 }
 
 // ------------------------------------------------------------ kernel
