@@ -69,7 +69,7 @@ def tl2p_words(M: int, K: int) -> int:
 
 
 def pack(W: np.ndarray) -> np.ndarray:
-    """int8 W[M, K] in {-1, 0, 1} -> TL2P v1 words (uint32)."""
+    """int8 W[M, K] in {-1, 0, 1} -> TL2P v2 words (uint32)."""
     W = _c(W, np.int8)
     M, K = W.shape
     P = np.zeros(max(tl2p_words(M, K), 1), dtype=np.uint32)
@@ -80,7 +80,7 @@ def pack(W: np.ndarray) -> np.ndarray:
 
 
 def unpack(P: np.ndarray, M: int, K: int) -> tuple[np.ndarray, int]:
-    """TL2P v1 words -> (int8 W[M, K], count of invalid codes / bad padding)."""
+    """TL2P v2 words -> (int8 W[M, K], count of invalid codes / bad padding)."""
     P = _c(P, np.uint32)
     W = np.zeros((M, K), dtype=np.int8)
     bad = lib().oracle_unpack(_ptr(P), M, K, _ptr(W))

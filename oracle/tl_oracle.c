@@ -15,7 +15,7 @@
  *     "Architecture": per-row metadata holds "row dimensions, scales, and row
  *     sums");
  *   - weights stay packed and are decoded inside the matrix kernel (model
- *     page, "Overview"); the packing is the library's own TL2P v1 layout,
+ *     page, "Overview"); the packing is the library's own TL2P v2 layout,
  *     because the pages' format is unpublished (wiki "Neutrino-1", "What is
  *     actually new").  The layout is restated in tl2p_position() below.
  *
@@ -39,7 +39,7 @@
 #include <pthread.h>
 
 /* ------------------------------------------------------------------ */
-/* TL2P v1 layout                                                       */
+/* TL2P v2 layout                                                       */
 /* ------------------------------------------------------------------ */
 /*
  * Logical W[M][K], padded with zero weights to Mp = ceil(M/16)*16 rows and
@@ -52,29 +52,24 @@
  *     g = i % 8,  h = i / 8           (row g or row g+8)
  *     s = c / 16, cc = c % 16         (16-column step inside the tile)
  *     u = cc / 8, t = (cc % 8) / 2, e = cc % 2
- *     f = 2*u + h                     (0..3)
- *     lane L = 4*g + t, word j = s / 2, slot q = 4*(s % 2) + f  (0..7)
- * Its 2-bit code sits at bits (15-2q, 14-2q) if e == 0 and at bits
- * (31-2q, 30-2q) if e == 1, the higher bit being the sign and the lower the
- * non-zero flag:  00 -> 0,  01 -> +1,  11 -> -1,  10 -> never written
- * (decodes to 0 and is counted as invalid).
+ *     lane L = 4*g + t, word j = 2*u + h  (0..3)
+ * Its 2-bit field starts at bit 2*s + 16*e and holds 1 - w as an unsigned
+ * number:  00 -> +1,  01 -> 0,  10 -> -1,  11 -> never written (decodes to
+ * 0 and is counted as invalid).  Padding positions hold 01.
  */
 static void tl2p_position(int64_t m, int64_t k, int64_t Kp,
-                          int64_t *word_index, int *sign_bit, int *nz_bit)
+                          int64_t *word_index, int *lo_bit)
 {
     int64_t r = m / 16, i = m % 16;
     int64_t b = k / 128, c = k % 128;
     int g = (int)(i % 8), h = (int)(i / 8);
     int s = (int)(c / 16), cc = (int)(c % 16);
     int u = cc / 8, t = (cc % 8) / 2, e = cc % 2;
-    int f = 2 * u + h;
     int lane = 4 * g + t;
-    int j = s / 2;
-    int q = 4 * (s % 2) + f;
+    int j = 2 * u + h;
     int64_t tile = r * (Kp / 128) + b;
     *word_index = (tile * 32 + lane) * 4 + j;
-    if (e == 0) { *sign_bit = 15 - 2 * q; *nz_bit = 14 - 2 * q; }
-    else        { *sign_bit = 31 - 2 * q; *nz_bit = 30 - 2 * q; }
+    *lo_bit = 2 * s + 16 * e;
 }
 
 static int64_t pad16(int64_t M) { return (M + 15) / 16 * 16; }
@@ -87,7 +82,8 @@ int64_t oracle_tl2p_words(int64_t M, int64_t K)
 }
 
 /* Pack W (int8, row-major M x K) into P.  Returns the number of entries of W
- * outside {-1, 0, 1}; P is fully written (padding = 0) only when that is 0. */
+ * outside {-1, 0, 1}; P is fully written (padding = zero weights) only when
+ * that is 0. */
 int64_t oracle_pack(const int8_t *W, int64_t M, int64_t K, uint32_t *P)
 {
     int64_t bad = 0;
@@ -98,33 +94,31 @@ int64_t oracle_pack(const int8_t *W, int64_t M, int64_t K, uint32_t *P)
         }
     if (bad) return bad;
     int64_t words = oracle_tl2p_words(M, K);
-    memset(P, 0, (size_t)words * sizeof(uint32_t));
+    for (int64_t i = 0; i < words; ++i) P[i] = 0x55555555u;   /* every field 01 */
     int64_t Kp = pad128(K);
     for (int64_t m = 0; m < M; ++m)
         for (int64_t k = 0; k < K; ++k) {
-            int8_t v = W[m * K + k];
-            if (v == 0) continue;
-            int64_t wi; int sb, nb;
-            tl2p_position(m, k, Kp, &wi, &sb, &nb);
-            P[wi] |= (uint32_t)1u << nb;
-            if (v < 0) P[wi] |= (uint32_t)1u << sb;
+            int v = W[m * K + k];
+            int64_t wi; int lb;
+            tl2p_position(m, k, Kp, &wi, &lb);
+            P[wi] &= ~((uint32_t)3u << lb);
+            P[wi] |= (uint32_t)(1 - v) << lb;
         }
     return 0;
 }
 
-/* Decode one weight.  *invalid is incremented for the code 10. */
+/* Decode one weight.  *invalid is incremented for the field 11. */
 static int oracle_weight(const uint32_t *P, int64_t m, int64_t k, int64_t Kp,
                          int64_t *invalid)
 {
-    int64_t wi; int sb, nb;
-    tl2p_position(m, k, Kp, &wi, &sb, &nb);
-    uint32_t w = P[wi];
-    int sign = (int)((w >> sb) & 1u), nz = (int)((w >> nb) & 1u);
-    if (!nz) {
-        if (sign && invalid) ++*invalid;
+    int64_t wi; int lb;
+    tl2p_position(m, k, Kp, &wi, &lb);
+    int f = (int)((P[wi] >> lb) & 3u);
+    if (f == 3) {
+        if (invalid) ++*invalid;
         return 0;
     }
-    return sign ? -1 : 1;
+    return 1 - f;
 }
 
 /* Unpack the logical M x K block.  Returns the count of invalid codes seen in

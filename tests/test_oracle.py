@@ -24,6 +24,9 @@ def _rand_case(M, K, seed, p0=0.626):
 
 # ---------------------------------------------------------------- format
 
+ZERO_WORD = np.uint32(0x55555555)     # a TL2P v2 word of sixteen zero weights
+
+
 def test_layout_hand_derived_positions(oracle_mod):
     """Single non-zero weights land on the hand-derived word and bits."""
     for M, K, m, k, w, wi, val in read_golden("tl2p_layout.txt"):
@@ -32,7 +35,7 @@ def test_layout_hand_derived_positions(oracle_mod):
         W[m, k] = w
         P = oracle_mod.pack(W)
         assert P.size == ((M + 15) // 16 * 16) * ((K + 127) // 128 * 128) // 16
-        nz = np.flatnonzero(P)
+        nz = np.flatnonzero(P != ZERO_WORD)
         assert list(nz) == [wi], (M, K, m, k, nz)
         assert int(P[wi]) == int(val, 16), (M, K, m, k, hex(int(P[wi])))
         back, bad = oracle_mod.unpack(P, M, K)
@@ -48,8 +51,8 @@ def test_layout_is_a_bijection(oracle_mod):
             W = np.zeros((M, K), dtype=np.int8)
             W[m, k] = -1
             P = oracle_mod.pack(W)
-            (wi,) = np.flatnonzero(P)
-            bits = int(P[wi])
+            (wi,) = np.flatnonzero(P != ZERO_WORD)
+            bits = int(P[wi]) ^ int(ZERO_WORD)       # field 01 -> 10
             assert bin(bits).count("1") == 2
             lo = (bits & -bits).bit_length() - 1
             assert lo % 2 == 0 and bits == (3 << lo)
@@ -79,7 +82,7 @@ def test_pack_rejects_values_outside_ternary(oracle_mod):
 def test_invalid_code_decodes_to_zero_and_is_counted(oracle_mod):
     W = np.zeros((16, 128), dtype=np.int8)
     P = oracle_mod.pack(W)
-    P[0] |= np.uint32(0x8000)          # sign bit without the non-zero bit
+    P[0] |= np.uint32(0x3)             # field 11
     back, bad = oracle_mod.unpack(P, 16, 128)
     assert bad == 1 and not back.any()
 
@@ -90,7 +93,7 @@ def test_padding_must_stay_zero(oracle_mod):
     _, bad = oracle_mod.unpack(P, 5, 37)
     assert bad == 0
     P2 = P.copy()
-    P2[-1] |= np.uint32(0x4000)        # row 15 / far column: padding
+    P2[-1] ^= np.uint32(0x40000000)    # row 15 / far column: padding 01 -> 00 (+1)
     _, bad = oracle_mod.unpack(P2, 5, 37)
     assert bad == 1
 
@@ -102,12 +105,12 @@ def test_rowsum_three_ways(oracle_mod, M, K):
     rs = oracle_mod.rowsum(P, M, K)
     assert np.array_equal(rs, W.astype(np.int64).sum(axis=1))
     # position-free popcount identity over the whole matrix: each field is
-    # (sign, nz) with nz on even bits; +1 = nz & ~sign, -1 = nz & sign.
+    # 1 - w with its low bit on an even position; +1 = 00, 0 = 01, -1 = 10.
     words = P.astype(np.uint64)
-    nz = words & 0x55555555
-    sg = (words >> 1) & 0x55555555
-    plus = sum(bin(int(v)).count("1") for v in (nz & ~sg & 0x55555555))
-    minus = sum(bin(int(v)).count("1") for v in (nz & sg))
+    lo = words & 0x55555555
+    hi = (words >> 1) & 0x55555555
+    plus = sum(bin(int(v)).count("1") for v in (~lo & ~hi & 0x55555555))
+    minus = sum(bin(int(v)).count("1") for v in (hi & ~lo & 0x55555555))
     assert plus - minus == int(rs.sum())
     assert plus == int((W == 1).sum()) and minus == int((W == -1).sum())
 

@@ -17,11 +17,11 @@ from tests import test_oracle as T
 
 MUTATIONS = {
     "lane_index": ("int lane = 4 * g + t;", "int lane = 4 * t + g;"),
-    "fragment_index": ("int f = 2 * u + h;", "int f = 2 * h + u;"),
-    "hi_lo_columns": ("if (e == 0) { *sign_bit", "if (e == 1) { *sign_bit"),
-    "word_of_step": ("int j = s / 2;", "int j = s % 4;"),
-    "slot_of_step": ("int q = 4 * (s % 2) + f;", "int q = 4 * (s / 4) + f;"),
-    "sign_map": ("return sign ? -1 : 1;", "return sign ? 1 : -1;"),
+    "word_index": ("int j = 2 * u + h;", "int j = 2 * h + u;"),
+    "hi_lo_columns": ("*lo_bit = 2 * s + 16 * e;", "*lo_bit = 2 * s + 16 * (1 - e);"),
+    "step_order": ("*lo_bit = 2 * s + 16 * e;", "*lo_bit = 2 * (7 - s) + 16 * e;"),
+    "sign_map": ("return 1 - f;", "return f - 1;"),
+    "padding_fill": ("P[i] = 0x55555555u;", "P[i] = 0u;"),
     "dropped_term": ("acc += (double)w[k] * (double)bf16_to_float(X[n * K + k]);",
                      "if (k) acc += (double)w[k] * (double)bf16_to_float(X[n * K + k]);"),
     "transposed_x": ("(double)bf16_to_float(X[n * K + k])", "(double)bf16_to_float(X[k * N + n])"),
