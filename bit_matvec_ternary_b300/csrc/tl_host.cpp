@@ -1,9 +1,9 @@
-// tl_host.cpp -- host side of the C ABI: the TL2P v1 packer, the validator,
+// tl_host.cpp -- host side of the C ABI: the TL2P v2 packer, the validator,
 // status strings.  No CUDA here.
 //
 // Packing is the offline step next to the per-row metadata the model page
 // describes ("Neutrino-1 8B", "Architecture": per-row "scales, and row
-// sums"); the bit layout is the library's own TL2P v1 (see include/tl.h).
+// sums"); the bit layout is the library's own TL2P v2 (see include/tl.h).
 // The packer walks the packed image word by word and gathers each word's
 // sixteen codes, so every word is written exactly once.
 
@@ -19,8 +19,9 @@ namespace {
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-// 2-bit code of one weight: bit 1 = sign, bit 0 = non-zero.
-inline uint32_t code_of(int8_t w) { return w == 0 ? 0u : (w > 0 ? 1u : 3u); }
+// 2-bit field of one weight: 1 - w (00 = +1, 01 = 0, 10 = -1).
+inline uint32_t code_of(int8_t w) { return (uint32_t)(1 - w); }
+constexpr uint32_t kZeroCode = 1u;   // padding
 
 struct Shape {
     int64_t M, K, Mp, Kp, RT, KB;
@@ -34,25 +35,23 @@ Shape shape_of(int64_t M, int64_t K) {
     return s;
 }
 
-// Builds the 128 words of tile (r, b).
+// Builds the 128 words of tile (r, b).  Word j of lane (g, t) holds row
+// g + 8*(j & 1), columns 16s + 8*(j >> 1) + 2t (+1) at bits 2s (16 + 2s).
 void pack_tile(const int8_t *W, const Shape &sh, int64_t r, int64_t b, uint32_t *out) {
     for (int lane = 0; lane < 32; ++lane) {
         const int g = lane >> 2, t = lane & 3;
         for (int j = 0; j < 4; ++j) {
+            const int64_t row = r * 16 + g + 8 * (j & 1);
             uint32_t word = 0;
-            for (int q = 0; q < 8; ++q) {
-                const int step = 2 * j + q / 4;      // 16-column step inside the tile
-                const int f = q & 3;                 // mma A-fragment register
-                const int hi_cols = f >> 1, hi_row = f & 1;
-                const int64_t row = r * 16 + g + 8 * hi_row;
-                const int64_t col = b * 128 + 16 * step + 8 * hi_cols + 2 * t;
-                uint32_t lo = 0, hi = 0;
+            for (int s = 0; s < 8; ++s) {
+                const int64_t col = b * 128 + 16 * s + 8 * (j >> 1) + 2 * t;
+                uint32_t lo = kZeroCode, hi = kZeroCode;
                 if (row < sh.M) {
                     if (col < sh.K) lo = code_of(W[row * sh.K + col]);
                     if (col + 1 < sh.K) hi = code_of(W[row * sh.K + col + 1]);
                 }
-                word |= lo << (14 - 2 * q);
-                word |= hi << (30 - 2 * q);
+                word |= lo << (2 * s);
+                word |= hi << (16 + 2 * s);
             }
             out[lane * 4 + j] = word;
         }
@@ -129,14 +128,13 @@ tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K, int64
                 const int g = lane >> 2, t = lane & 3;
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t word = tile[lane * 4 + j];
-                    for (int q = 0; q < 8; ++q) {
-                        const int step = 2 * j + q / 4, f = q & 3;
-                        const int64_t row = r * 16 + g + 8 * (f & 1);
-                        const int64_t col = b * 128 + 16 * step + 8 * (f >> 1) + 2 * t;
+                    const int64_t row = r * 16 + g + 8 * (j & 1);
+                    for (int s = 0; s < 8; ++s) {
+                        const int64_t col = b * 128 + 16 * s + 8 * (j >> 1) + 2 * t;
                         for (int e = 0; e < 2; ++e) {
-                            const uint32_t c = (word >> ((e ? 30 : 14) - 2 * q)) & 3u;
-                            if (c == 2u) ++bad;                       // sign without non-zero
-                            else if (c != 0u && (row >= M || col + e >= K)) ++bad;  // padding
+                            const uint32_t c = (word >> (2 * s + 16 * e)) & 3u;
+                            if (c == 3u) ++bad;                                   // invalid field
+                            else if (c != kZeroCode && (row >= M || col + e >= K)) ++bad;  // padding
                         }
                     }
                 }

@@ -14,29 +14,39 @@
 //     of one mma n8 tile.
 //
 // Kernel tl_mma_kernel (N <= 8, modes A and B):
-//   Work.  The launch's (16-row tile, 128-column block) units are ordered row
+//   Work.  K is cut into slices of at most kMaxSlice 128-column blocks.  The
+//   launch's (16-row tile, block) units are ordered slice by slice, then row
 //   tile by row tile; CTA c owns the contiguous range [c*Lc, (c+1)*Lc), so
-//   every CTA streams the same number of bytes and a row tile spans at most
-//   two CTAs.  Inside a CTA the k-range is processed in passes of KS blocks
-//   (the activations of one pass fit the staging buffer at 8 tokens); the 16
-//   warps split each pass's units into contiguous ranges.
+//   every CTA streams the same number of bytes, stages only the activations
+//   of the one or two slices it touches, and a (row tile, slice) piece spans
+//   at most two CTAs.  The 16 warps split the CTA's units of a slice into
+//   contiguous ranges.
 //   Weights.  Each warp streams its units with cp.async.bulk into its own
-//   ring of shared-memory slots (up to 4 tiles, 2 KB, per copy, completing
-//   on the slot's mbarrier), running ahead across passes.  A TL2P v1 tile is
-//   in mma.m16n8k16 A-fragment order: register f of a 16-column step is
-//   (word << 2q) & 0xC000C000, a bf16x2 pair of +-2.0 / +-0.0 -- one shift
-//   (IMAD, FMA pipe) and one AND (LOP3, ALU pipe) per two weights; the
-//   tensor cores do the multiply-adds (products exact, fp32 sums).
-//   Activations.  Staged per pass in shared memory in B-fragment order (mode
-//   B converts int8 to bf16, exact); columns n >= N repeat token N-1 and
-//   their results are discarded, so no lane is predicated off.
-//   Reduction.  A warp that covers all of a row tile's units in a pass adds
+//   ring of shared-memory slots (up to 8 tiles per copy, completing on the
+//   slot's mbarrier), running ahead across slices.  A TL2P v2 tile is in
+//   mma.m16n8k16 A-fragment order and each 2-bit field holds 1 - w, so
+//   register j of k-step m is (word >> 8*(m/4)) & (0x00030003 << 2*(m%4)):
+//   a bf16x2 pair whose halves are (1 - w) * 2^(2q - 133), q = m%4 -- bf16
+//   subnormals (or, for field 10 at q == 3, the smallest normal), exactly
+//   linear in the field.  One AND per two weights, plus one shift per word.
+//   Activations.  Staged per slice in shared memory in B-fragment order,
+//   multiplied by 2^67 (an exponent add, exact), so a class-q product is
+//   (1 - w) * x * 2^(2q - 66), exact in fp32; the tensor cores form the sums,
+//   one accumulator chain per class, and each chain is rescaled exactly when
+//   a run of tiles is folded.  The staging also sums x per 128-column block,
+//   and a row's result is (sum of x over its blocks) - sum (1 - w) x.
+//   Activations outside [2^-60, 2^61) in magnitude (mode A only) switch that
+//   token's slice to a scale chosen from its largest exponent.  Columns
+//   n >= N are zero and their results are discarded, so no lane is
+//   predicated off.
+//   Reduction.  A warp that covers all of a row tile's units in a slice adds
 //   its sum straight into the CTA's row accumulator (shared memory); rows
 //   split between warps go through per-warp boundary slots that are added in
-//   warp order after the pass.  A row tile cut by a CTA boundary is finished
-//   by whichever of its two CTAs arrives second (workspace counter), adding
-//   the two halves in a fixed order.  The plan never depends on N, so every
-//   token's result is bitwise independent of the batch.
+//   warp order after the slice.  A row tile whose pieces sit in several CTAs
+//   is finished by whichever CTA completes it (workspace counter), adding the
+//   pieces in a fixed order.  The plan never depends on N, and the power-of-
+//   two scaling does not change any rounding, so every token's result is
+//   bitwise independent of the batch.
 
 #include "tl.h"
 #include "tl_internal.cuh"
@@ -50,42 +60,25 @@
 
 namespace {
 
-constexpr int kWarps = 16;            // warps per CTA of the N <= 8 kernel (one CTA per SM)
+constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
+constexpr int kCtasPerSm = 2;         // resident CTAs per SM (registers and shared memory allow 2)
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunkTiles = 4;        // tiles (512 B each) per bulk copy
 constexpr int kSlots = 2;             // bulk copies in flight per warp
-constexpr int kRingBytes = kWarps * kSlots * kChunkTiles * 512;   // 64 KB
+// Tiles (512 B each) per bulk copy, smaller as the staged activations grow
+// (two CTAs must fit in one SM's shared memory).
+__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 2 ? 8 : nt == 4 ? 4 : 2; }
+__host__ __device__ constexpr int ring_bytes(int nt) { return kWarps * kSlots * chunk_tiles(nt) * 512; }
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
-constexpr int kStageBlocks = 16;      // 128-column blocks per pass (32 KB at 8 tokens)
-constexpr int kMaxCtaRows = 32;       // row tiles one CTA may touch
+constexpr int kMaxSlice = 32;         // 128-column blocks per K slice (64 KB of X at 8 tokens)
+constexpr int kMaxCtaRows = 16;       // row tiles one CTA may touch in one slice
+constexpr int kStageBatch = 4;        // activation loads in flight per thread while staging
 constexpr long long kWaitLimit = 1ll << 31;   // SM cycles before a wait gives up
-
-struct GroupArgs {
-    const char *packed[TL_MAX_GROUP];
-    const float *scale[TL_MAX_GROUP];
-    const int32_t *rowsum[TL_MAX_GROUP];
-    void *Y[TL_MAX_GROUP];
-    int M[TL_MAX_GROUP];
-    int rt_off[TL_MAX_GROUP + 1];   // row-tile prefix over the group
-    int G;
-    int R;          // row tiles in the launch
-    int KB;         // 128-column blocks
-    int KS;         // blocks per pass
-    int S;          // passes
-    int K;
-    int U;          // units = R * KB
-    int Lc;         // units per CTA (the last CTAs may get fewer)
-    const void *X;  // bf16 [N][K] (mode A) or int8 [N][K] (mode B)
-    const float *s;
-    const int32_t *z;
-    int N;
-    int mode;
-    int out;
-    float *part;    // halves of CTA-split row tiles [R][2][N][16]
-    unsigned long long *cnt;  // [R] blocks arrived; zero between launches
-    int *status;    // workspace status word
-};
+// Activations are staged times 2^kT: a k-step class q product is then
+// (1 - w) * x * 2^(2q - 66), a normal fp32 number for |x| in [2^-60, 2^61).
+constexpr int kT = 67;
+constexpr int kWinLo = 127 - 60;      // bf16 exponent fields of the fixed-scale window
+constexpr int kWinHi = 127 + 60;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -147,135 +140,145 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 
 // ------------------------------------------------------------ work geometry
-// The CTA's unit range and the row tiles it touches.
-struct CtaGeo {
-    int cu0, cu1;           // units [cu0, cu1), unit = row_tile * KB + block
+// Units are ordered slice by slice, then row tile, then block:
+// u = sigma*R*KW + r*kw(sigma) + b, with kw(sigma) the slice's width (KW for
+// every slice but the last, which is KWL wide).
+
+// n / d for 0 <= n < 2^31 as (umulhi(n, m) + n) >> s (m, s from the host).
+struct FastDiv {
+    uint32_t m, s;
+};
+__device__ __forceinline__ int fdiv(int n, FastDiv d) {
+    return (int)(((unsigned long long)__umulhi((uint32_t)n, d.m) + (uint32_t)n) >> d.s);
+}
+
+struct Slice {
+    int sigma, kb0, kw;     // slice, its first block, its width in blocks
+    int a0, a1;             // the CTA's units of the slice, slice-local
     int r_first, r_last;    // row tiles touched (r_last < r_first: none)
     int lo_first, hi_last;  // first block of r_first, one past the last block of r_last
 };
 
-__device__ __forceinline__ CtaGeo cta_geo(const GroupArgs &a, int c) {
-    CtaGeo g;
-    g.cu0 = min(c * a.Lc, a.U);
-    g.cu1 = min(g.cu0 + a.Lc, a.U);
-    if (g.cu1 > g.cu0) {
-        g.r_first = g.cu0 / a.KB;
-        g.r_last = (g.cu1 - 1) / a.KB;
-        g.lo_first = g.cu0 - g.r_first * a.KB;
-        g.hi_last = g.cu1 - g.r_last * a.KB;
-    } else {
-        g.r_first = 0; g.r_last = -1; g.lo_first = 0; g.hi_last = 0;
-    }
-    return g;
-}
-
-// Blocks [lo, hi) of row tile r that the CTA covers in pass s.
-__device__ __forceinline__ void row_span(const GroupArgs &a, const CtaGeo &g, int r, int s,
-                                         int &lo, int &hi) {
-    lo = max(r == g.r_first ? g.lo_first : 0, s * a.KS);
-    hi = min(r == g.r_last ? g.hi_last : a.KB, (s + 1) * a.KS);
-}
-
-__device__ __forceinline__ int row_count(const GroupArgs &a, const CtaGeo &g, int r, int s) {
-    int lo, hi;
-    row_span(a, g, r, s, lo, hi);
-    return max(0, hi - lo);
-}
-
-__device__ __forceinline__ int pass_units(const GroupArgs &a, const CtaGeo &g, int s) {
-    if (g.r_last < g.r_first) return 0;
-    const int c0 = row_count(a, g, g.r_first, s);
-    if (g.r_last == g.r_first) return c0;
-    return c0 + (g.r_last - g.r_first - 1) * a.KS + row_count(a, g, g.r_last, s);
-}
-
-// Row tile and block of the i-th unit of pass s in the CTA.
-__device__ __forceinline__ void pass_locate(const GroupArgs &a, const CtaGeo &g, int s, int i,
-                                            int &r, int &b) {
-    int lo, hi;
-    row_span(a, g, g.r_first, s, lo, hi);
-    const int c0 = max(0, hi - lo);
-    if (i < c0) { r = g.r_first; b = lo + i; return; }
-    const int j = i - c0;
-    const int mid = g.r_last > g.r_first ? (g.r_last - g.r_first - 1) * a.KS : 0;
-    if (j < mid) { r = g.r_first + 1 + j / a.KS; b = s * a.KS + j % a.KS; return; }
-    row_span(a, g, g.r_last, s, lo, hi);
-    r = g.r_last;
-    b = lo + (j - mid);
-}
-
-// A warp's walk over its units, pass after pass, in chunks: runs of at most
-// kChunkTiles consecutive blocks of one row tile (contiguous in memory).
-struct Walk {
-    int s, i, iend;          // pass, unit index in the pass, end of the warp's range
-    int r, b, row_hi;        // current row tile, block, end block of the row in this pass
-    int gi, rl;              // matrix of the group and its local row tile
-    int n;                   // tiles in the current chunk (0: done)
-
-    __device__ void map_row(const GroupArgs &a) {
-        gi = 0;
-        while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
-        rl = r - a.rt_off[gi];
-    }
-    __device__ void enter(const GroupArgs &a, const CtaGeo &g, int w) {
-        // from pass s on: the first pass in which warp w has units
-        for (; s < a.S; ++s) {
-            const int np = pass_units(a, g, s);
-            const int lw = (np + kWarps - 1) / kWarps;
-            i = min(w * lw, np);
-            iend = min(i + lw, np);
-            if (i < iend) {
-                pass_locate(a, g, s, i, r, b);
-                int lo;
-                row_span(a, g, r, s, lo, row_hi);
-                map_row(a);
-                n = min(kChunkTiles, min(iend - i, row_hi - b));
-                return;
-            }
-        }
-        n = 0;
-    }
-    __device__ void start(const GroupArgs &a, const CtaGeo &g, int w) {
-        s = 0;
-        enter(a, g, w);
-    }
-    __device__ void next(const GroupArgs &a, const CtaGeo &g, int w) {
-        i += n;
-        b += n;
-        if (i >= iend) {
-            ++s;
-            enter(a, g, w);
-            return;
-        }
-        if (b >= row_hi) {
-            ++r;
-            int lo;
-            row_span(a, g, r, s, lo, row_hi);
-            b = lo;
-            map_row(a);
-        }
-        n = min(kChunkTiles, min(iend - i, row_hi - b));
-    }
-    __device__ __forceinline__ const char *src(const GroupArgs &a) const {
-        return a.packed[gi] + ((long long)rl * a.KB + b) * 512;
-    }
+// A warp's position: slice-local unit u of its range [u, uend) in slice
+// sigma, at row tile r, block b (slice-local) of a slice kw blocks wide.
+struct Cursor {
+    int sigma, u, uend, r, b, kw, kb0;
 };
 
+// Everything below reads these launch constants.
+struct GroupArgs {
+    const char *packed[TL_MAX_GROUP];
+    const float *scale[TL_MAX_GROUP];
+    const int32_t *rowsum[TL_MAX_GROUP];
+    void *Y[TL_MAX_GROUP];
+    int M[TL_MAX_GROUP];
+    int rt_off[TL_MAX_GROUP + 1];   // row-tile prefix over the group
+    int G;
+    int R;          // row tiles in the launch
+    int KB;         // 128-column blocks
+    int KW;         // blocks per K slice
+    int KWL;        // blocks of the last slice
+    int NS;         // slices
+    int K;
+    int U;          // units = R * KB
+    int Lc;         // units per CTA (the last CTAs may get fewer)
+    int rows;       // accumulator rows per CTA
+    FastDiv dKW, dKWL;
+    const void *X;  // bf16 [N][K] (mode A) or int8 [N][K] (mode B)
+    const float *s;
+    const int32_t *z;
+    int N;
+    int mode;
+    int out;
+    int xvec;       // X rows allow 16-byte loads (16-byte aligned, K a multiple of 8 / 16)
+    float *part;    // pieces of row tiles finished across CTAs [R][NS][2][N][16]
+    unsigned long long *cnt;  // [R] blocks arrived; zero between launches
+    int *status;    // workspace status word
+};
+
+__device__ __forceinline__ int slice_width(const GroupArgs &a, int sigma) {
+    return sigma == a.NS - 1 ? a.KWL : a.KW;
+}
+
+__device__ __forceinline__ void slice_of(const GroupArgs &a, int cu0, int cu1, int sigma,
+                                         Slice &p) {
+    p.sigma = sigma;
+    p.kb0 = sigma * a.KW;
+    p.kw = slice_width(a, sigma);
+    const FastDiv dv = sigma == a.NS - 1 ? a.dKWL : a.dKW;
+    const int base = sigma * a.R * a.KW;
+    p.a0 = max(cu0, base) - base;
+    p.a1 = min(cu1, base + a.R * p.kw) - base;
+    if (p.a1 > p.a0) {
+        p.r_first = fdiv(p.a0, dv);
+        p.r_last = fdiv(p.a1 - 1, dv);
+        p.lo_first = p.a0 - p.r_first * p.kw;
+        p.hi_last = p.a1 - p.r_last * p.kw;
+    } else {
+        p.r_first = 0; p.r_last = -1; p.lo_first = 0; p.hi_last = 0;
+    }
+}
+
+// Blocks [lo, hi) of row tile r that the CTA covers in slice p.
+__device__ __forceinline__ void row_span(const Slice &p, int r, int &lo, int &hi) {
+    lo = r == p.r_first ? p.lo_first : 0;
+    hi = r == p.r_last ? p.hi_last : p.kw;
+}
+
+// Whether the (row tile r, slice sigma) piece is cut by a CTA boundary.
+__device__ __forceinline__ bool piece_split(const GroupArgs &a, int r, int sigma) {
+    const int kw = slice_width(a, sigma);
+    const int u0 = sigma * a.R * a.KW + r * kw;
+    return u0 / a.Lc != (u0 + kw - 1) / a.Lc;
+}
+
+// Move c to warp w's first unit in slice c.sigma or a later one before
+// sig_end; false when the warp has no units left.
+__device__ __forceinline__ bool cursor_enter(const GroupArgs &a, int cu0, int cu1, int sig_end,
+                                             int w, Cursor &c) {
+    for (; c.sigma < sig_end; ++c.sigma) {
+        c.kb0 = c.sigma * a.KW;
+        c.kw = slice_width(a, c.sigma);
+        const int base = c.sigma * a.R * a.KW;
+        const int a0 = max(cu0, base) - base, a1 = min(cu1, base + a.R * c.kw) - base;
+        const int np = a1 - a0;
+        if (np <= 0) continue;
+        const int lw = (np + kWarps - 1) / kWarps;
+        c.u = a0 + min(w * lw, np);
+        c.uend = a0 + min(w * lw + lw, np);
+        if (c.u < c.uend) {
+            c.r = fdiv(c.u, c.sigma == a.NS - 1 ? a.dKWL : a.dKW);
+            c.b = c.u - c.r * c.kw;
+            return true;
+        }
+    }
+    return false;
+}
+
+// Matrix of the group that holds row tile r, and r's first tile.
+__device__ __forceinline__ const char *row_base(const GroupArgs &a, int r, int &gi) {
+    gi = 0;
+    while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
+    return a.packed[gi] + (long long)(r - a.rt_off[gi]) * a.KB * 512;
+}
+
 // ------------------------------------------------------------ epilogue
-// Y[n][m] from acc_y = sum_k w*x (mode A) or the exact integer sum_k w*q (mode B).
-__device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int n, float acc) {
+// Y[n][m] from acc = sum_k w*x (mode A) or the exact integer sum_k w*q (mode
+// B); sc = scale[m], rs = rowsum[m].
+__device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int n, float acc,
+                                          float sc, int rs) {
     const int M = a.M[gi];
     float y;
     if (a.mode == TL_MODE_BF16) {
-        y = __fmul_rn(acc, a.scale[gi][m]);
+        y = __fmul_rn(acc, sc);
     } else {
         const int iacc = __float2int_rn(acc);
         if (a.out == TL_OUT_I32_RAW) {
             reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * M + m] = iacc;
             return;
         }
-        const int corrected = iacc - a.z[n] * a.rowsum[gi][m];
-        y = __fmul_rn(__fmul_rn((float)corrected, a.s[n]), a.scale[gi][m]);
+        const int corrected = iacc - a.z[n] * rs;
+        y = __fmul_rn(__fmul_rn((float)corrected, a.s[n]), sc);
     }
     if (a.out == TL_OUT_F32)
         reinterpret_cast<float *>(a.Y[gi])[(long long)n * M + m] = y;
@@ -283,11 +286,11 @@ __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int
         reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * M + m] = __float2bfloat16_rn(y);
 }
 
-// The 16 x N results of row tile r held as acc[n * 16 + row] (sums of +-2
-// weights: halved here, exactly).  One warp; lane (g, t) stores rows g, g+8
-// of tokens 2t, 2t+1.
-__device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const float *acc,
-                                               int lane) {
+// The 16 x N results of row tile r held as v[n * 16 + row], with the row
+// tile's scales and row sums in sc[16], rs[16].  One warp; lane (g, t)
+// stores rows g, g+8 of tokens 2t, 2t+1.
+__device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const float *v,
+                                               const float *sc, const int *rs, int lane) {
     const int g = lane >> 2, t = lane & 3;
     int gi = 0;
     while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
@@ -296,129 +299,382 @@ __device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const 
     for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int m = rl * 16 + g + 8 * h, n = 2 * t + e;
-            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, acc[n * 16 + g + 8 * h] * 0.5f);
+            const int i = g + 8 * h, m = rl * 16 + i, n = 2 * t + e;
+            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, v[n * 16 + i], sc[i], rs[i]);
         }
 }
 
-// One 128-column block of one 16-row tile: 8 MMAs over the lane's 16-byte
-// slice of the tile (w) and the 4 B-fragment quarters (b).
+// One 128-column block of one 16-row tile: 8 MMAs (k-steps m = 0..7) over
+// the lane's 16-byte slice of the tile (w) and the 4 B-fragment quarters (b).
+// Register j of k-step m is word j shifted right by 8*(m/4) and masked to the
+// fields at bits 2*(m%4) and 16 + 2*(m%4).
 __device__ __forceinline__ void tile_mma(float (&c)[4][4], const uint4 &w, const uint4 (&b)[4]) {
-    const uint32_t M2 = 0xC000C000u;
-    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t hx = w.x >> 8, hy = w.y >> 8, hz = w.z >> 8, hw = w.w >> 8;
     // four independent accumulator chains; consecutive MMAs never share one
 #pragma unroll
-    for (int qd = 0; qd < 4; ++qd)
-        mma_bf16_16816(c[qd], wd[qd] & M2, (wd[qd] << 2) & M2, (wd[qd] << 4) & M2,
-                       (wd[qd] << 6) & M2, b[qd].x, b[qd].y);
-#pragma unroll
-    for (int qd = 0; qd < 4; ++qd)
-        mma_bf16_16816(c[qd], (wd[qd] << 8) & M2, (wd[qd] << 10) & M2, (wd[qd] << 12) & M2,
-                       (wd[qd] << 14) & M2, b[qd].z, b[qd].w);
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t F = 0x00030003u << (2 * (m & 3));
+        const uint32_t a0 = (m < 4 ? w.x : hx) & F, a1 = (m < 4 ? w.y : hy) & F;
+        const uint32_t a2 = (m < 4 ? w.z : hz) & F, a3 = (m < 4 ? w.w : hw) & F;
+        const uint4 &q = b[m >> 1];
+        mma_bf16_16816(c[m & 3], a0, a1, a2, a3, (m & 1) ? q.z : q.x, (m & 1) ? q.w : q.y);
+    }
 }
 
+// VPL consecutive activations of token n from column k0 (VPL = 8 bf16 in mode
+// A, 16 int8 in mode B; k0 a multiple of VPL): one 16-byte load when X allows
+// it, else element loads; columns >= K read as 0.
+template <bool kModeA>
+__device__ __forceinline__ uint4 load_group(const GroupArgs &a, int n, int k0) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (kModeA) {
+        const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K + k0;
+        if (a.xvec) {
+            if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4 *>(x));
+        } else {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (k0 + e < a.K) w[e >> 1] |= (uint32_t)x[e] << (16 * (e & 1));
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        const uint8_t *x = reinterpret_cast<const uint8_t *>(a.X) + (long long)n * a.K + k0;
+        if (a.xvec) {
+            if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4 *>(x));
+        } else {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (k0 + e < a.K) w[e >> 2] |= (uint32_t)x[e] << (8 * (e & 3));
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    return v;
+}
+
+// bf16 bits -> float (exact).
+__device__ __forceinline__ float bf16f(uint32_t h) { return __uint_as_float(h << 16); }
+// x * 2^d for any bf16 x through fp32 (two exact power-of-two products).
+__device__ __forceinline__ uint32_t scale_any(uint32_t h, int d) {
+    const int d1 = d / 2, d2 = d - d1;
+    const float f = __fmul_rn(__fmul_rn(bf16f(h), __int_as_float((d1 + 127) << 23)),
+                              __int_as_float((d2 + 127) << 23));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// The activation groups of one slice: VPL activations per group, LB groups
+// per 128-column block, N * kw * LB groups in all, taken kStageBatch *
+// kThreads at a time starting at `base`.
+template <bool kModeA>
+__device__ __forceinline__ void stage_load(const GroupArgs &a, const Slice &P, int base,
+                                           uint4 (&v)[kStageBatch]) {
+    constexpr int VPL = kModeA ? 8 : 16;
+    constexpr int LB = 128 / VPL;
+    const int total = a.N * P.kw * LB;
+    const FastDiv dv = P.sigma == a.NS - 1 ? a.dKWL : a.dKW;
+#pragma unroll
+    for (int i = 0; i < kStageBatch; ++i) {
+        const int idx = base + i * kThreads + (int)threadIdx.x;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < total) {
+            const int q = idx / LB, o = idx % LB;     // q = n * kw + jb
+            const int n = fdiv(q, dv), jb = q - n * P.kw;
+            v[i] = load_group<kModeA>(a, n, (P.kb0 + jb) * 128 + o * VPL);
+        }
+    }
+}
+
+// Kernel launch helpers shared with the host side.
 // ------------------------------------------------------------ kernel
 // kModeA: bf16 activations (else int8 from the quantiser).  NT: token
 // columns staged (a power of two >= N).
 template <bool kModeA, int NT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 tl_mma_kernel(const __grid_constant__ GroupArgs a) {
+    constexpr int CH = chunk_tiles(NT);         // tiles per bulk copy
+    constexpr int SLOT = CH * 512;
     constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
     constexpr int XB = 4 * XQ;                  // uint4 per 128-column block
     constexpr int RV = 16 * NT;                 // floats per row-tile result
+    constexpr int VPL = kModeA ? 8 : 16;        // activations per staging group
+    constexpr int LB = 128 / VPL;               // staging groups per block
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ring = smem;                                              // [kWarps][kSlots][2 KB]
-    uint4 *xs = reinterpret_cast<uint4 *>(smem + kRingBytes);          // one pass of X
-    float *acc = reinterpret_cast<float *>(smem + kRingBytes + a.KS * XB * 16);  // [rows][RV]
-    __shared__ float bslot[kWarps][2][RV];      // boundary pieces of the current pass
+    uint8_t *ring = smem;                                                // [kWarps][kSlots][SLOT]
+    uint4 *xs = reinterpret_cast<uint4 *>(smem + ring_bytes(NT));      // one slice of X
+    float *acc = reinterpret_cast<float *>(smem + ring_bytes(NT) + a.KW * XB * 16);  // [rows][RV]
+    float *scl = acc + a.rows * RV;                                      // [rows][16] scales
+    int *rsm = reinterpret_cast<int *>(scl + a.rows * 16);               // [rows][16] row sums
+    __shared__ float bslot[kWarps][2][RV];      // boundary pieces of the current slice
     __shared__ int bslot_row[kWarps][2];
+    __shared__ float osum[kMaxSlice][NT];       // sum of x per block of the slice
+    __shared__ float opre[kMaxSlice + 1][NT];   // prefix sums of osum
+    __shared__ int texp[NT];                    // T per token: X is staged times 2^T
+    __shared__ int redo;                        // tokens outside the fixed window (bit mask)
+    __shared__ int emax[NT];
     __shared__ __align__(8) unsigned long long bars[kWarps][kSlots];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const CtaGeo geo = cta_geo(a, blockIdx.x);
-    const int nrows = geo.r_last - geo.r_first + 1;
     const int N = a.N;
+    const int cu0 = (int)min((long long)blockIdx.x * a.Lc, (long long)a.U);
+    const int cu1 = min(cu0 + a.Lc, a.U);
+    const int sunits = a.R * a.KW;
+    const int sig0 = cu0 / sunits;
+    const int sig1 = cu1 > cu0 ? (cu1 - 1) / sunits + 1 : sig0;
+    uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
 
-    if (threadIdx.x < kWarps * kSlots)
-        mbar_init(smem_u32(&bars[0][0]) + 8u * threadIdx.x, 1);
-    if (threadIdx.x < kWarps * 2) (&bslot_row[0][0])[threadIdx.x] = -1;
-    for (int i = threadIdx.x; i < nrows * RV; i += kThreads) acc[i] = 0.f;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncthreads();
-
-    // Weights do not depend on the previous kernel: start the bulk copies
-    // before waiting for it.  The producer (lane 0) runs kSlots chunks ahead
-    // of the consumer, across pass boundaries.
-    const uint32_t ring_w = smem_u32(ring) + warp * (kSlots * kChunkTiles * 512);
-    const uint32_t bar_w = smem_u32(&bars[warp][0]);
-    Walk pf;
-    pf.start(a, geo, warp);
-    if (lane == 0)
-        for (int k = 0; k < kSlots && pf.n > 0; ++k) {
-            bulk_load(ring_w + k * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * k);
-            pf.next(a, geo, warp);
-        }
-    griddep_wait();
+    // The dependent launch may be scheduled at once; it only streams weights
+    // until this grid has finished.
     griddep_launch();
 
-    Walk cw;
-    cw.start(a, geo, warp);
+    // Weights do not depend on the previous kernel: each warp's lane 0 sets up
+    // its ring and starts its first copies before waiting for it.  The
+    // producer then runs kSlots chunks ahead of the warp's consumer, across
+    // slices.
+    const uint32_t ring_w = smem_u32(ring) + warp * (kSlots * SLOT);
+    const uint32_t bar_w = smem_u32(&bars[warp][0]);
+    Cursor pc;
+    pc.sigma = sig0;
+    bool pc_on = cursor_enter(a, cu0, cu1, sig1, warp, pc);
+    int pgi = 0;
+    const char *prow = pc_on ? row_base(a, pc.r, pgi) : nullptr;
+    auto produce = [&](int slot_) {
+        const int n = min(CH, min(pc.uend - pc.u, pc.kw - pc.b));
+        bulk_load(ring_w + slot_ * SLOT, prow + (long long)(pc.kb0 + pc.b) * 512, n * 512,
+                  bar_w + 8u * slot_);
+        pc.u += n;
+        pc.b += n;
+        if (pc.b == pc.kw) {
+            pc.b = 0;
+            ++pc.r;
+            if (pgi + 1 < a.G && pc.r == a.rt_off[pgi + 1]) prow = a.packed[++pgi];
+            else prow += (long long)a.KB * 512;
+        }
+        if (pc.u == pc.uend) {
+            ++pc.sigma;
+            pc_on = cursor_enter(a, cu0, cu1, sig1, warp, pc);
+            if (pc_on) prow = row_base(a, pc.r, pgi);
+        }
+    };
+    if (lane == 0) {
+        for (int k = 0; k < kSlots; ++k) mbar_init(bar_w + 8u * k, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int k = 0; k < kSlots && pc_on; ++k) produce(k);
+    }
+    // this CTA's scales (and row sums) of its first slice, one per thread
+    Slice P;
+    slice_of(a, cu0, cu1, sig0, P);
+    float sc_pre = 0.f;
+    int rs_pre = 0;
+    {
+        const int rho = threadIdx.x >> 4, i = threadIdx.x & 15;
+        if (rho <= P.r_last - P.r_first) {
+            int gi;
+            row_base(a, P.r_first + rho, gi);
+            const int m = (P.r_first + rho - a.rt_off[gi]) * 16 + i;
+            if (m < a.M[gi]) {
+                sc_pre = __ldg(a.scale[gi] + m);
+                if (!kModeA) rs_pre = __ldg(a.rowsum[gi] + m);
+            }
+        }
+    }
+    if (threadIdx.x < kWarps * 2) (&bslot_row[0][0])[threadIdx.x] = -1;
+    if (threadIdx.x == 0) redo = 0;
+    if (threadIdx.x < NT) emax[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < a.rows * RV; i += kThreads) acc[i] = 0.f;
+    if (N < NT)   // the columns past the batch stay zero in every slice
+        for (int i = threadIdx.x; i < a.KW * 64 * NT; i += kThreads)
+            if (((i >> 4) % NT) >= N) xw[i] = 0u;
+    __syncthreads();
+
+    // Now the activations, written by the previous kernel.
+    griddep_wait();
+    uint4 xv[kStageBatch];
+    stage_load<kModeA>(a, P, 0, xv);
+
+    Cursor cc;
+    cc.sigma = sig0;
+    bool cc_on = cursor_enter(a, cu0, cu1, sig1, warp, cc);
     int slot = 0;
     uint32_t phases = 0;                        // parity bit per slot
     bool ok = true;
     float c[4][4];
 
-    for (int s = 0; s < a.S; ++s) {
-        // ---- stage X for pass s in B-fragment order:
-        // word ((((bp*4 + qd)*NT + n)*4 + t)*4 + w) holds x[n'][k], x[n'][k+1],
-        // n' = min(n, N-1), k = (s*KS + bp)*128 + 16*(2qd + w/2) + 2t + 8*(w%2).
+    for (int sigma = sig0; sigma < sig1; ++sigma) {
+        if (sigma != sig0) slice_of(a, cu0, cu1, sigma, P);
+        const int nrows = P.r_last - P.r_first + 1;
+        // ---- stage X for the slice in B-fragment order, times 2^kT, and sum
+        // it per block.  Word ((j*4 + qd)*NT + n)*16 + 4*tt + w holds
+        // x[n][k], x[n][k+1] for m = 2qd + w/2, k = (kb0 + j)*128 + 16*m +
+        // 2*tt + 8*(w%2); columns n >= N stay zero.  A thread takes VPL
+        // consecutive activations at a time (one 16-byte load when X allows
+        // it); the LB threads of a block sum it in a fixed order, the same
+        // for either kind of load.
         {
-            const int words = a.KS * 64 * NT;
-            uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
-            for (int idx = threadIdx.x; idx < words; idx += kThreads) {
-                const int w = idx & 3, tt = (idx >> 2) & 3;
-                const int n = min((idx >> 4) % NT, N - 1);
-                const int rest = (idx >> 4) / NT;
-                const int qd = rest & 3, bp = rest >> 2;
-                const int k = (s * a.KS + bp) * 128 + 16 * (2 * qd + (w >> 1)) + 2 * tt + 8 * (w & 1);
-                uint32_t lo = 0, hi = 0;
-                if (kModeA) {
-                    const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
-                    if (k < a.K) lo = x[k];
-                    if (k + 1 < a.K) hi = x[k + 1];
-                } else {
-                    const int8_t *x = reinterpret_cast<const int8_t *>(a.X) + (long long)n * a.K;
-                    if (k < a.K) lo = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k]));
-                    if (k + 1 < a.K) hi = __bfloat16_as_ushort(__float2bfloat16_rn((float)x[k + 1]));
+            const int total = N * P.kw * LB;
+            const FastDiv dv = sigma == a.NS - 1 ? a.dKWL : a.dKW;
+            for (int base = 0; base < total; base += kThreads * kStageBatch) {
+                if (sigma != sig0 || base != 0) stage_load<kModeA>(a, P, base, xv);
+#pragma unroll
+                for (int i = 0; i < kStageBatch; ++i) {
+                    if (base + i * kThreads >= total) break;   // uniform over the block
+                    const int idx = base + i * kThreads + (int)threadIdx.x;
+                    const bool valid = idx < total;
+                    const int q = idx / LB, o = idx % LB;
+                    const int n = valid ? fdiv(q, dv) : 0, jb = q - n * P.kw;
+                    float sum = 0.f;
+                    uint32_t bad = 0u;
+                    if (valid) {
+                        const uint32_t wd[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+                        if (kModeA) {
+                            const int m = o >> 1;
+                            uint32_t *dst = xw + ((jb * 4 + (m >> 1)) * NT + n) * 16 + 2 * (m & 1) + (o & 1);
+#pragma unroll
+                            for (int tt = 0; tt < 4; ++tt) {
+                                const uint32_t v = wd[tt];
+                                sum = __fadd_rn(__fadd_rn(sum, __uint_as_float(v << 16)),
+                                                __uint_as_float(v & 0xFFFF0000u));
+                                // per half: nonzero, and exponent outside [kWinLo, kWinHi]
+                                const uint32_t nz = __vcmpne2(v & 0x7FFF7FFFu, 0u);
+                                const uint32_t off = __vsub2(v & 0x7F807F80u, (uint32_t)kWinLo * 0x00800080u);
+                                bad |= __vcmpgtu2(off, (uint32_t)(kWinHi - kWinLo) * 0x00800080u) & nz;
+                                dst[tt * 4] = v + ((uint32_t)kT * 0x00800080u & nz);
+                            }
+                        } else {
+                            const int m = o;
+                            uint32_t *dst = xw + ((jb * 4 + (m >> 1)) * NT + n) * 16 + 2 * (m & 1);
+                            const float two_t = __int_as_float((kT + 127) << 23);
+                            int isum = 0;
+#pragma unroll
+                            for (int h8 = 0; h8 < 2; ++h8)
+#pragma unroll
+                                for (int tt = 0; tt < 4; ++tt) {
+                                    const uint32_t word = wd[2 * h8 + (tt >> 1)] >> (16 * (tt & 1));
+                                    const int qlo = (int)(int8_t)(word & 0xFFu);
+                                    const int qhi = (int)(int8_t)((word >> 8) & 0xFFu);
+                                    isum += qlo + qhi;
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                        __fmul_rn((float)qlo, two_t), __fmul_rn((float)qhi, two_t));
+                                    dst[tt * 4 + h8] = *reinterpret_cast<const uint32_t *>(&b2);
+                                }
+                            sum = (float)isum;
+                        }
+                    }
+#pragma unroll
+                    for (int off = LB / 2; off > 0; off >>= 1)
+                        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
+                    if (valid && (lane % LB) == 0) osum[jb][n] = sum;
+                    if (kModeA && valid && bad) atomicOr(&redo, 1 << n);
                 }
-                xw[idx] = lo | (hi << 16);
+            }
+            // this slice's scales and row sums (one per thread)
+            if (sigma == sig0) {
+                if ((int)(threadIdx.x >> 4) < a.rows) {
+                    scl[threadIdx.x] = sc_pre;
+                    if (!kModeA) rsm[threadIdx.x] = rs_pre;
+                }
+            } else {
+                const int rho = threadIdx.x >> 4, i = threadIdx.x & 15;
+                float sc = 0.f;
+                int rs = 0;
+                if (rho < nrows) {
+                    int gi;
+                    row_base(a, P.r_first + rho, gi);
+                    const int m = (P.r_first + rho - a.rt_off[gi]) * 16 + i;
+                    if (m < a.M[gi]) {
+                        sc = __ldg(a.scale[gi] + m);
+                        if (!kModeA) rs = __ldg(a.rowsum[gi] + m);
+                    }
+                }
+                if (rho < a.rows) {
+                    scl[threadIdx.x] = sc;
+                    if (!kModeA) rsm[threadIdx.x] = rs;
+                }
             }
         }
+        if (threadIdx.x < NT) texp[threadIdx.x] = kT;
         __syncthreads();
 
-        // ---- this warp's units of pass s
-        int run_lo = cw.b, nslot = 0;
+        if (kModeA && redo != 0) {
+            // Rare: some token has activations outside the fixed window.  Its
+            // scale follows its largest exponent field E in the slice: 2^(254 - E)
+            // keeps every staged value finite; values more than 2^120 below the
+            // largest may lose their contribution.
+            const int mask = redo;
+            const int klo = P.kb0 * 128, khi = min((P.kb0 + P.kw) * 128, a.K);
+            for (int n = 0; n < N; ++n) {
+                if (!(mask >> n & 1)) continue;
+                const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
+                uint32_t e = 0;
+                for (int k = klo + threadIdx.x; k < khi; k += kThreads) e = max(e, ((uint32_t)x[k] >> 7) & 0xFFu);
+                e = __reduce_max_sync(0xffffffffu, e);
+                if (lane == 0) atomicMax(&emax[n], (int)e);
+            }
+            __syncthreads();
+            if (threadIdx.x < NT && (mask >> threadIdx.x & 1)) texp[threadIdx.x] = 254 - emax[threadIdx.x];
+            for (int idx = threadIdx.x; idx < P.kw * 64 * NT; idx += kThreads) {
+                const int n = (idx >> 4) % NT;
+                if (!(mask >> n & 1)) continue;
+                const int w = idx & 3, tt = (idx >> 2) & 3, rest = (idx >> 4) / NT;
+                const int qd = rest & 3, j = rest >> 2;
+                const int m = 2 * qd + (w >> 1);
+                const int k = (P.kb0 + j) * 128 + 16 * m + 2 * tt + 8 * (w & 1);
+                const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
+                const uint32_t lo = k < a.K ? x[k] : 0u, hi = k + 1 < a.K ? x[k + 1] : 0u;
+                const int d = 254 - emax[n];
+                xw[idx] = scale_any(lo, d) | (scale_any(hi, d) << 16);
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) redo = 0;
+            if (threadIdx.x < NT) emax[threadIdx.x] = 0;
+        }
+
+        // prefix sums of the block sums, one warp per token column
+        if (warp < NT) {
+            const int n = warp;
+            float v0 = lane < P.kw ? osum[lane][n] : 0.f;
+            float v1 = lane + 32 < P.kw ? osum[lane + 32][n] : 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y0 = __shfl_up_sync(0xffffffffu, v0, off);
+                const float y1 = __shfl_up_sync(0xffffffffu, v1, off);
+                if (lane >= off) { v0 = __fadd_rn(v0, y0); v1 = __fadd_rn(v1, y1); }
+            }
+            v1 = __fadd_rn(v1, __shfl_sync(0xffffffffu, v0, 31));
+            if (lane == 0) opre[0][n] = 0.f;
+            if (lane < P.kw) opre[lane + 1][n] = v0;
+            if (lane + 32 < P.kw) opre[lane + 33][n] = v1;
+        }
+        // this lane's tokens 2t, 2t+1: chain q holds the products of k-step
+        // class q, (1 - w) x 2^(2q - 133 + T); undo 2^(2q - 133 + T) with two
+        // exact factors each
+        int tx[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) tx[e] = texp[min(2 * t + e, NT - 1)];
+
+        // ---- this warp's units of the slice
+        int run_lo = cc.b, nslot = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-        while (ok && cw.n > 0 && cw.s == s) {
+        while (ok && cc_on && cc.sigma == sigma) {
+            const int n = min(CH, min(cc.uend - cc.u, cc.kw - cc.b));
             const bool got = __all_sync(0xffffffffu,
                                         mbar_wait(bar_w + 8u * slot, (phases >> slot) & 1u, a.status));
             if (!got) { ok = false; break; }
             phases ^= 1u << slot;
-            const uint4 *tiles = reinterpret_cast<const uint4 *>(
-                ring + warp * (kSlots * kChunkTiles * 512) + slot * (kChunkTiles * 512)) + lane;
-            const uint4 *xb = xs + (cw.b - s * a.KS) * XB + (g % NT) * 4 + t;
-            if (cw.n == kChunkTiles) {
+            const uint4 *tiles = reinterpret_cast<const uint4 *>(ring + warp * (kSlots * SLOT) + slot * SLOT) + lane;
+            const uint4 *xb = xs + cc.b * XB + (g % NT) * 4 + t;
+            if (n == CH) {
                 // full chunk: load tile i+1 while tile i is multiplied
                 uint4 w = tiles[0];
                 uint4 bq[4];
 #pragma unroll
                 for (int qd = 0; qd < 4; ++qd) bq[qd] = xb[qd * XQ];
 #pragma unroll
-                for (int i = 0; i < kChunkTiles; ++i) {
+                for (int i = 0; i < CH; ++i) {
                     uint4 wn = w, bn[4] = {bq[0], bq[1], bq[2], bq[3]};
-                    if (i + 1 < kChunkTiles) {
+                    if (i + 1 < CH) {
                         wn = tiles[(i + 1) * 32];
 #pragma unroll
                         for (int qd = 0; qd < 4; ++qd) bn[qd] = xb[(i + 1) * XB + qd * XQ];
@@ -429,7 +685,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                     for (int qd = 0; qd < 4; ++qd) bq[qd] = bn[qd];
                 }
             } else {
-                for (int i = 0; i < cw.n; ++i) {
+                for (int i = 0; i < n; ++i) {
                     const uint4 w = tiles[i * 32];
                     uint4 bq[4];
 #pragma unroll
@@ -438,17 +694,25 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 }
             }
             // end of a run of one row tile: this chunk ends the row or the warp's range
-            const bool run_end = (cw.b + cw.n == cw.row_hi) || (cw.i + cw.n == cw.iend);
-            if (run_end) {
+            if (cc.b + n == cc.kw || cc.u + n == cc.uend) {
+                // lane (g, t) holds rows g, g+8 of tokens 2t, 2t+1: v[2h + e]
                 float v[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = (c[0][q] + c[1][q]) + (c[2][q] + c[3][q]);
+                for (int q = 0; q < 4; ++q) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int cl = 0; cl < 4; ++cl) {
+                        const int d = 133 - tx[q & 1] - 2 * cl, d1 = d / 2;
+                        s = __fadd_rn(s, __fmul_rn(__fmul_rn(c[cl][q], __int_as_float((d1 + 127) << 23)),
+                                                   __int_as_float((d - d1 + 127) << 23)));
+                    }
+                    v[q] = s;
+                }
                 int lo, hi;
-                row_span(a, geo, cw.r, s, lo, hi);
-                const int rho = cw.r - geo.r_first;
-                // lane (g, t) holds rows g, g+8 of tokens 2t, 2t+1
-                if (run_lo == lo && cw.b + cw.n == hi) {
-                    // the whole row tile of this pass: no other warp touches it
+                row_span(P, cc.r, lo, hi);
+                const int rho = cc.r - P.r_first;
+                if (run_lo == lo && cc.b + n == hi) {
+                    // the whole row tile of this slice: no other warp touches it
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -465,21 +729,26 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
-                run_lo = cw.b + cw.n < cw.row_hi ? cw.b + cw.n : -1;   // next run starts a row
+                run_lo = cc.b + n < cc.kw ? cc.b + n : -1;   // next run starts a row
             }
             // refill this slot with the chunk kSlots ahead
             __syncwarp();
-            if (lane == 0 && pf.n > 0) {
+            if (lane == 0 && pc_on) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                bulk_load(ring_w + slot * (kChunkTiles * 512), pf.src(a), pf.n * 512, bar_w + 8u * slot);
-                pf.next(a, geo, warp);
+                produce(slot);
             }
-            cw.next(a, geo, warp);
-            if (run_lo < 0) run_lo = cw.b;
-            slot = slot + 1 == kSlots ? 0 : slot + 1;
+            cc.u += n;
+            cc.b += n;
+            if (cc.b == cc.kw) { cc.b = 0; ++cc.r; }
+            if (cc.u == cc.uend) {
+                ++cc.sigma;
+                cc_on = cursor_enter(a, cu0, cu1, sig1, warp, cc);
+            }
+            if (run_lo < 0) run_lo = cc.b;
+            slot ^= 1;
         }
         __syncthreads();
-        // ---- boundary pieces of pass s, added in warp order (one thread per element)
+        // ---- boundary pieces of the slice, added in warp order (one thread per element)
         if (threadIdx.x < RV) {
             for (int w = 0; w < kWarps; ++w)
 #pragma unroll
@@ -490,45 +759,62 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         }
         __syncthreads();
         if (threadIdx.x < kWarps * 2) (&bslot_row[0][0])[threadIdx.x] = -1;
-        // (the next pass's staging __syncthreads orders this reset before reuse)
+
+        // ---- the slice's rows: sum_k w*x over the CTA's blocks of row tile r
+        // is (sum of x over those blocks) - 2^P * S.  A row tile wholly inside
+        // this CTA and slice goes straight to Y; otherwise the piece goes to
+        // the workspace and whoever completes the row tile adds all pieces.
+        if (ok) {
+            for (int rho = warp; rho < nrows; rho += kWarps) {
+                const int r = P.r_first + rho;
+                int lo, hi;
+                row_span(P, r, lo, hi);
+                float *v = acc + rho * RV;
+                for (int e = lane; e < N * 16; e += 32) {
+                    const int n = e >> 4;
+                    v[e] = __fsub_rn(__fsub_rn(opre[hi][n], opre[lo][n]), v[e]);
+                }
+                __syncwarp();
+                if (a.NS == 1 && lo == 0 && hi == P.kw) {
+                    store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
+                } else {
+                    const int half = lo == 0 ? 0 : 1;   // 0: holds the slice's first block
+                    float *dst = a.part + (((long long)r * a.NS + sigma) * 2 + half) * N * 16;
+                    for (int e = lane; e < N * 16; e += 32) __stcg(dst + e, v[e]);
+                    __syncwarp();
+                    unsigned long long now = 0ull;
+                    if (lane == 0) {
+                        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                        now = atomicAdd(a.cnt + r, (unsigned long long)(hi - lo)) + (unsigned long long)(hi - lo);
+                    }
+                    now = __shfl_sync(0xffffffffu, now, 0);
+                    if (now == (unsigned long long)a.KB) {
+                        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                        // all pieces, slice by slice, the half with the slice's first block first
+                        for (int e = lane; e < N * 16; e += 32) {
+                            float y = 0.f;
+                            for (int s2 = 0; s2 < a.NS; ++s2) {
+                                const float *pc2 = a.part + ((long long)r * a.NS + s2) * 2 * N * 16;
+                                y = __fadd_rn(y, __ldcg(pc2 + e));
+                                if (piece_split(a, r, s2)) y = __fadd_rn(y, __ldcg(pc2 + N * 16 + e));
+                            }
+                            v[e] = y;
+                        }
+                        __syncwarp();
+                        store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
+                        if (lane == 0) a.cnt[r] = 0ull;
+                    }
+                }
+                __syncwarp();
+                for (int e = lane; e < RV; e += 32) v[e] = 0.f;   // ready for the next slice
+            }
+        }
+        // (the next slice's staging barrier orders these reads of opre, acc
+        // and scl before they are rewritten)
     }
     if (!ok) {
         // a copy never landed: drain what is still in flight (bounded), then leave
         for (int k = 0; k < kSlots; ++k) mbar_wait(bar_w + 8u * k, (phases >> k) & 1u, a.status);
-        return;
-    }
-
-    // ---- results: rows covered entirely by this CTA go straight to Y; a row
-    // tile cut by a CTA boundary is finished by the second of its two CTAs.
-    for (int rho = warp; rho < nrows; rho += kWarps) {
-        const int r = geo.r_first + rho;
-        const int lo = r == geo.r_first ? geo.lo_first : 0;
-        const int hi = r == geo.r_last ? geo.hi_last : a.KB;
-        const float *v = acc + rho * RV;
-        if (lo == 0 && hi == a.KB) {
-            store_row_tile(a, r, v, lane);
-            continue;
-        }
-        const int half = lo == 0 ? 0 : 1;       // 0: holds block 0 of the row
-        float *dst = a.part + ((long long)r * 2 + half) * N * 16;
-        for (int e = lane; e < N * 16; e += 32) __stcg(dst + e, v[e]);
-        __syncwarp();
-        unsigned long long now = 0ull;
-        if (lane == 0) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            now = atomicAdd(a.cnt + r, (unsigned long long)(hi - lo)) + (unsigned long long)(hi - lo);
-        }
-        now = __shfl_sync(0xffffffffu, now, 0);
-        if (now == (unsigned long long)a.KB) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            const float *h0 = a.part + (long long)r * 2 * N * 16;
-            // combine the halves (block-0 half first) through this CTA's acc row
-            for (int e = lane; e < N * 16; e += 32)
-                acc[rho * RV + e] = __ldcg(h0 + e) + __ldcg(h0 + N * 16 + e);
-            __syncwarp();
-            store_row_tile(a, r, acc + rho * RV, lane);
-            if (lane == 0) a.cnt[r] = 0ull;
-        }
     }
 }
 
@@ -615,7 +901,12 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 
-constexpr int kMaxDynSmem = kRingBytes + kStageBlocks * 128 * kNMax * 2 + kMaxCtaRows * 16 * kNMax * 4;
+// Dynamic shared memory: weight ring, one slice of X, row accumulators, and
+// the rows' scales and row sums.
+constexpr size_t dyn_smem(int nt, int kw, int rows) {
+    return (size_t)ring_bytes(nt) + (size_t)kw * 128 * nt * 2 + (size_t)rows * 16 * nt * 4 +
+           (size_t)rows * 16 * 8;
+}
 
 tl_status device_info(DeviceInfo **out) {
     int dev = 0;
@@ -635,7 +926,7 @@ tl_status device_info(DeviceInfo **out) {
                 for (int nt = 1; nt <= 8; nt *= 2)
                     if (cudaFuncSetAttribute(kernel_for(mode, nt),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kMaxDynSmem) != cudaSuccess)
+                                             (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess)
                         return TL_ERR_CUDA;
             const tl_status pst = tl_internal::prefill_init_device();
             if (pst != TL_OK) return pst;
@@ -649,13 +940,26 @@ tl_status device_info(DeviceInfo **out) {
 }
 
 struct Plan {
-    int R, KB, KS, S, P, Lc, rows;
+    int R, KB, KW, KWL, NS, P, Lc, rows;
     long long U;
     size_t smem;       // dynamic shared memory for the given N
     size_t ws_bytes;   // workspace for the given N
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// m = ceil(2^(32+l) / d) - 2^32 with l = ceil(log2 d): then for every
+// 32-bit n, floor(n / d) = (umulhi(n, m) + n) >> l (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994).
+FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const unsigned long long big = 1ull << (32 + l);
+    FastDiv f;
+    f.m = (uint32_t)((big + d - 1) / d - (1ull << 32));
+    f.s = l;
+    return f;
+}
 
 // The plan depends on the shapes and the SM count only, never on N, so every
 // token is summed in the same order whatever the batch.
@@ -665,26 +969,38 @@ tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     p->KB = (int)ceil_div(K, 128);
     p->U = (long long)p->R * p->KB;
     if (p->U >= (1ll << 30)) return TL_ERR_SHAPE;
-    // passes: the largest divisor of KB not above kStageBlocks
-    p->KS = 1;
-    for (int d = 1; d <= std::min(p->KB, kStageBlocks); ++d)
-        if (p->KB % d == 0) p->KS = d;
-    p->S = p->KB / p->KS;
-    // CTAs: at most one per SM, and ranges of at least KB - 1 units so a row
-    // tile never spans more than two CTAs
-    long long P = sms;
-    if (p->KB > 1) P = std::min<long long>(P, std::max<long long>(1, p->U / (p->KB - 1)));
+    // Slices: as wide as kMaxSlice allows, but narrow enough that every CTA
+    // slot gets a range of at least KW - 1 units (a piece then spans <= 2 CTAs).
+    const long long slots = (long long)sms * kCtasPerSm;   // CTAs resident at once
+    long long kwt = std::min<long long>(kMaxSlice, p->U / slots + 1);
+    kwt = std::max<long long>(1, std::min<long long>(kwt, p->KB));
+    const int ns0 = (int)ceil_div(p->KB, kwt);
+    p->KW = (int)ceil_div(p->KB, ns0);
+    p->NS = (int)ceil_div(p->KB, p->KW);
+    const int kwmin = p->KB - (p->NS - 1) * p->KW;   // the last slice's width
+    p->KWL = kwmin;
+    long long P = slots;
+    if (p->KW > 1) P = std::min<long long>(P, std::max<long long>(1, p->U / (p->KW - 1)));
     else P = std::min<long long>(P, p->U);
-    p->P = (int)std::max<long long>(1, P);
-    p->Lc = (int)ceil_div(p->U, p->P);
-    p->rows = (int)(ceil_div(p->Lc + p->KB - 1, p->KB) + 1);
-    p->rows = std::min(p->rows, p->R);
+    P = std::max<long long>(1, P);
+    auto rows_for = [&](long long Lc) { return ceil_div(Lc + kwmin - 1, kwmin) + 1; };
+    long long Lc = ceil_div(p->U, P);
+    if (rows_for(Lc) > kMaxCtaRows) {
+        // very tall, short-K groups: more CTAs than slots, each within kMaxCtaRows rows
+        P = ceil_div(p->U, (long long)(kMaxCtaRows - 2) * kwmin);
+        Lc = ceil_div(p->U, P);
+        if (p->KW > 1 && Lc < p->KW - 1) return TL_ERR_SHAPE;
+    }
+    if (P > (1ll << 31) - 1) return TL_ERR_SHAPE;
+    p->P = (int)P;
+    p->Lc = (int)Lc;
+    p->rows = (int)std::min<long long>(rows_for(Lc), p->R);
     if (p->rows > kMaxCtaRows) return TL_ERR_SHAPE;
     const int nt = padded_tokens(std::min(std::max(N, 1), kNMax));
     const int n = std::min(std::max(N, 1), kNMax);
-    p->smem = (size_t)kRingBytes + (size_t)p->KS * 128 * nt * 2 + (size_t)p->rows * 16 * nt * 4;
+    p->smem = dyn_smem(nt, p->KW, p->rows);
     const size_t cnt_bytes = ((size_t)p->R * 8 + 255) / 256 * 256;
-    p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * 2 * 16 * n * 4;
+    p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * p->NS * 2 * 16 * n * 4;
     return TL_OK;
 }
 
@@ -696,7 +1012,7 @@ tl_status check_weights(const tl_weight *Ws, int G, int mode) {
         const tl_weight &w = Ws[g];
         if (!w.packed || !w.scale) return TL_ERR_NULL;
         if (mode == TL_MODE_I8 && !w.rowsum) return TL_ERR_NULL;
-        if (w.layout != TL_LAYOUT_TL2P_V1) return TL_ERR_UNSUPPORTED;
+        if (w.layout != TL_LAYOUT_TL2P_V2) return TL_ERR_UNSUPPORTED;
         if (w.M < 1 || w.K < 1 || w.M > TL_MAX_M || w.K > TL_MAX_K) return TL_ERR_SHAPE;
         if (w.K != Ws[0].K) return TL_ERR_SHAPE;
         if (!aligned(w.packed, 16) || !aligned(w.scale, 4)) return TL_ERR_ALIGN;
@@ -740,12 +1056,16 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     const tl_status pst = make_plan(Ms, G, K, n, dev.sms, &p);
     if (pst != TL_OK) return pst;
     if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
-    a.R = p.R; a.KB = p.KB; a.KS = p.KS; a.S = p.S; a.K = K; a.U = (int)p.U; a.Lc = p.Lc;
+    a.R = p.R; a.KB = p.KB; a.KW = p.KW; a.KWL = p.KWL; a.NS = p.NS; a.K = K; a.U = (int)p.U;
+    a.Lc = p.Lc; a.rows = p.rows;
+    a.dKW = make_fastdiv((uint32_t)p.KW);
+    a.dKWL = make_fastdiv((uint32_t)p.KWL);
     const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
     a.X = static_cast<const char *>(X) + (size_t)n0 * K * xsz;
     a.s = s ? s + n0 : nullptr;
     a.z = z ? z + n0 : nullptr;
     a.N = n; a.mode = mode; a.out = out;
+    a.xvec = aligned(a.X, 16) && (K % (mode == TL_MODE_BF16 ? 8 : 16)) == 0;
     const size_t cnt_bytes = ((size_t)p.R * 8 + 255) / 256 * 256;
     char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
     a.cnt = reinterpret_cast<unsigned long long *>(wsb);

@@ -54,7 +54,7 @@ tl_status tl_linear_noalloc(const tl_weight *W, const void *X, const float *s, c
                             void *stream) {
     if (!W || !X || !Y) return TL_ERR_NULL;
     if (!W->packed || !W->scale) return TL_ERR_NULL;
-    if (W->layout != TL_LAYOUT_TL2P_V1) return TL_ERR_UNSUPPORTED;
+    if (W->layout != TL_LAYOUT_TL2P_V2) return TL_ERR_UNSUPPORTED;
     if (W->M < 1 || W->K < 1 || W->M > TL_MAX_M || W->K > TL_MAX_K || N < 1) return TL_ERR_SHAPE;
     if (mode != TL_MODE_BF16 && mode != TL_MODE_I8) return TL_ERR_MODE;
     if (out_dtype != TL_OUT_F32 && out_dtype != TL_OUT_BF16 && out_dtype != TL_OUT_I32_RAW)

@@ -163,21 +163,22 @@ __device__ __forceinline__ void griddep_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Write the decoded half (64 columns) of one 16-row TL2P tile into the A stage.
-// The lane holds rows g, g+8 of row tile `rt`; word pair (w0, w1) covers
-// the four 16-column steps of this half.
-__device__ __forceinline__ void store_half(uint8_t *a_stage, int rt, int g, int t, uint32_t w0,
-                                           uint32_t w1) {
-    const uint32_t M2 = 0xC000C000u;
+// Write the decoded half hh (columns 64hh .. 64hh+63, k-steps 4hh .. 4hh+3)
+// of one 16-row TL2P v2 tile into the A stage as bf16 +-2.0 / 0.  Word j of
+// the lane holds row g + 8(j&1), columns 16s + 8(j>>1) + 2t (+1) in the
+// fields at bits 2s (16 + 2s); a field holds 1 - w, so moving it to bits
+// 15..14 and flipping bit 14 gives 00 -> 0x4000 (+2), 01 -> 0, 10 -> 0xC000.
+__device__ __forceinline__ void store_half(uint8_t *a_stage, int rt, int g, int t, const uint4 &w,
+                                           int hh) {
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        const uint32_t word = (s < 2) ? w0 : w1;
-        const int q0 = 4 * (s & 1);
+    for (int s4 = 0; s4 < 4; ++s4) {
+        const int s = 4 * hh + s4;
 #pragma unroll
-        for (int f = 0; f < 4; ++f) {
-            const uint32_t v = (word << (2 * (q0 + f))) & M2;
-            const int row = rt * 16 + g + 8 * (f & 1);
-            const int chunk = 2 * s + (f >> 1);
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t v = ((wd[j] << (14 - 2 * s)) & 0xC000C000u) ^ 0x40004000u;
+            const int row = rt * 16 + g + 8 * (j & 1);
+            const int chunk = 2 * s4 + (j >> 1);
             const int off = (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4) + 4 * t;
             *reinterpret_cast<uint32_t *>(a_stage + off) = v;
         }
@@ -279,7 +280,7 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         for (int i = 0; i < RING; ++i)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                ring[i][r] = make_uint4(0u, 0u, 0u, 0u);
+                ring[i][r] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // zero weights
                 if (i < a.KB && rt_base + r < rts)
                     ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + i) * 512 + lane * 16);
             }
@@ -303,8 +304,8 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                         ok = __all_sync(0xffffffffu, ok && mbar_wait(empty(s), ph ^ 1u, a.status));
                         if (ok) {
                             uint8_t *a_stage = smem + s * STAGE_BYTES;
-                            store_half(a_stage, 2 * dw, g, t, h ? cur0.z : cur0.x, h ? cur0.w : cur0.y);
-                            store_half(a_stage, 2 * dw + 1, g, t, h ? cur1.z : cur1.x, h ? cur1.w : cur1.y);
+                            store_half(a_stage, 2 * dw, g, t, cur0, h);
+                            store_half(a_stage, 2 * dw + 1, g, t, cur1, h);
                             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                             __syncwarp();
                             if (lane == 0) mbar_arrive(full_a(s));

@@ -29,7 +29,7 @@ TL_ERR_MODE, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_WORKSPACE =
 TL_MODE_BF16, TL_MODE_I8 = 0, 1
 TL_OUT_F32, TL_OUT_BF16, TL_OUT_I32_RAW = 0, 1, 2
 TL_FLAG_PDL = 1
-TL_LAYOUT_TL2P_V1 = 1
+TL_LAYOUT_TL2P_V2 = 2
 TL_MAX_GROUP = 4
 
 # Every symbol include/tl.h declares.
@@ -163,7 +163,7 @@ class TernaryWeight:
 
     def struct(self) -> tl_weight:
         return tl_weight(self.packed.data_ptr(), self.scale.data_ptr(), self.rowsum.data_ptr(),
-                         self.M, self.K, TL_LAYOUT_TL2P_V1)
+                         self.M, self.K, TL_LAYOUT_TL2P_V2)
 
 
 def _structs(ws):

@@ -35,18 +35,19 @@
  *   - Nothing aborts or throws across the ABI.
  *   - Row-major everywhere: X is [N][K], Y is [N][M].
  *
- * Packed weight format "TL2P v1" (the pages' own format is unpublished; this
+ * Packed weight format "TL2P v2" (the pages' own format is unpublished; this
  * is the library's own):
  *   W[M][K] is padded with zero weights to Mp = ceil(M/16)*16 rows and
  *   Kp = ceil(K/128)*128 columns and cut into 16 x 128 tiles of 512 bytes;
  *   tile (r, b) starts at byte (r * Kp/128 + b) * 512.  In a tile, lane
- *   L = 4g + t (g < 8, t < 4) owns the 16 bytes at 16L.  Weight (i, c) of the
- *   tile (row i < 16, column c < 128) has g = i%8, h = i/8, s = c/16,
- *   cc = c%16, u = cc/8, t = (cc%8)/2, e = cc%2, f = 2u+h; it lives in word
- *   j = s/2 of lane 4g+t, slot q = 4*(s%2)+f, at bits (15-2q, 14-2q) when
- *   e == 0 and (31-2q, 30-2q) when e == 1.  The high bit of the pair is the
- *   sign, the low bit marks non-zero: 00 -> 0, 01 -> +1, 11 -> -1; 10 is
- *   never written.  Size: tl_packed_bytes(M, K) = Mp * Kp / 4 bytes.
+ *   L = 4g + t (g < 8, t < 4) owns the 16 bytes (4 little-endian words) at
+ *   16L.  Weight (i, c) of the tile (row i < 16, column c < 128) has g = i%8,
+ *   h = i/8, s = c/16, cc = c%16, u = cc/8, t = (cc%8)/2, e = cc%2; it lives
+ *   in word j = 2u + h of lane 4g+t, in the 2-bit field starting at bit
+ *   2s + 16e.  The field holds 1 - w as an unsigned number: 00 -> +1,
+ *   01 -> 0, 10 -> -1; 11 is never written.  Padding fields hold 01, so a
+ *   word of sixteen zero weights is 0x55555555.  Size:
+ *   tl_packed_bytes(M, K) = Mp * Kp / 4 bytes.
  */
 #ifndef TL_H
 #define TL_H
@@ -71,7 +72,7 @@ typedef enum {
     TL_ERR_ALIGN = 3,       /* packed not 16-byte aligned, or an element pointer misaligned */
     TL_ERR_BAD_VALUE = 4,   /* tl_pack: a weight outside {-1, 0, 1}; tl_validate: bad codes */
     TL_ERR_MODE = 5,        /* unknown mode / output type, or a combination that does not exist */
-    TL_ERR_UNSUPPORTED = 6, /* layout tag not TL2P v1, or no device of compute capability 10.3 */
+    TL_ERR_UNSUPPORTED = 6, /* layout tag not TL2P v2, or no device of compute capability 10.3 */
     TL_ERR_CUDA = 7,        /* a CUDA runtime call failed */
     TL_ERR_TIMEOUT = 8,     /* a bounded device-side wait gave up */
     TL_ERR_WORKSPACE = 9    /* workspace NULL or smaller than tl_workspace_bytes() */
@@ -87,21 +88,21 @@ enum { TL_OUT_F32 = 0, TL_OUT_BF16 = 1, TL_OUT_I32_RAW = 2 };
                            it when that previous kernel does not write this call's
                            weights, scales or row sums (it may write X). */
 
-#define TL_LAYOUT_TL2P_V1 1u
+#define TL_LAYOUT_TL2P_V2 2u
 #define TL_MAX_GROUP 4
 #define TL_MAX_K (1 << 20)
 #define TL_MAX_M (1 << 24)
 
 /* One packed ternary matrix, all pointers device memory owned by the caller. */
 typedef struct {
-    const uint32_t *packed; /* TL2P v1 words, tl_packed_bytes(M, K) bytes, 16-byte aligned */
+    const uint32_t *packed; /* TL2P v2 words, tl_packed_bytes(M, K) bytes, 16-byte aligned */
     const float *scale;     /* [M] fp32 per-row scale */
     const int32_t *rowsum;  /* [M] int32 sum_k w[m,k]; required in mode B, ignored in mode A */
     int32_t M, K;           /* logical rows (outputs) and columns (inputs) */
-    uint32_t layout;        /* TL_LAYOUT_TL2P_V1 */
+    uint32_t layout;        /* TL_LAYOUT_TL2P_V2 */
 } tl_weight;
 
-/* Bytes of the TL2P v1 image of an M x K matrix (0 if M or K < 1). */
+/* Bytes of the TL2P v2 image of an M x K matrix (0 if M or K < 1). */
 TL_API size_t tl_packed_bytes(int64_t M, int64_t K);
 
 /* HOST.  Pack int8 W[M][K] (row-major, values in {-1, 0, 1}) into `packed`
@@ -114,7 +115,7 @@ TL_API size_t tl_packed_bytes(int64_t M, int64_t K);
 TL_API tl_status tl_pack(const int8_t *W, int64_t M, int64_t K, const float *scale_in,
                   uint32_t *packed, float *scale_out, int32_t *rowsum);
 
-/* HOST.  Check a TL2P v1 image: *bad_codes receives the number of 10 codes
+/* HOST.  Check a TL2P v2 image: *bad_codes receives the number of 11 fields
  * plus non-zero padding weights (NULL allowed).  TL_OK iff that is 0. */
 TL_API tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K,
                              int64_t *bad_codes);

@@ -79,19 +79,17 @@ def test_validator_counts_invalid_codes_and_padding():
     W = np.ones((5, 37), dtype=np.int8)
     packed, _, _ = tl.tl_pack(W)
     assert tl.tl_validate_packed(packed, 5, 37) == 0
-    bad = packed.copy()
-    bad[0] |= np.uint32(0x8000) if not (bad[0] & 0x4000) else np.uint32(0)
     p2 = packed.copy()
-    p2[-1] |= np.uint32(0x00004000)          # a padding position
+    p2[-1] ^= np.uint32(0x40000000)           # a padding field 01 -> 00 (+1)
     assert tl.tl_validate_packed(p2, 5, 37) == 1
-    p3 = np.zeros_like(packed)
-    p3[0] = 0x8000                             # code 10
+    p3 = np.full_like(packed, 0x55555555)
+    p3[0] = 0x55555557                         # field 11
     assert tl.tl_validate_packed(p3, 5, 37) == 1
 
 
 # ---- argument checks: each returns before any CUDA call ----------------------
 
-def _w(M=16, K=128, layout=tl.TL_LAYOUT_TL2P_V1, packed=0x1000, scale=0x2000, rowsum=0x3000):
+def _w(M=16, K=128, layout=tl.TL_LAYOUT_TL2P_V2, packed=0x1000, scale=0x2000, rowsum=0x3000):
     return tl.tl_weight(packed, scale, rowsum, M, K, layout)
 
 

@@ -205,7 +205,11 @@ def test_zero_rows_and_one_hot(oracle_mod):
     m = Mat(oracle_mod, M, K, seed=40, W=W)
     X = synth.activations(8, K, seed=41)
     Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
-    assert np.all(Y[:, 17] == 0) and np.all(Y[:, 299] == 0)
+    ref = oracle_mod.linear_a(m.P, m.scale, M, K, X)
+    assert np.all(ref[:, 17] == 0) and np.all(ref[:, 299] == 0)
+    assert rel_err(Y, ref) <= TOL_A            # zero rows: within the mode A bound
+    *_, Yb = gpu_b(m, X)
+    assert np.all(Yb.cpu().numpy()[:, [17, 299]] == 0)   # mode B: exactly zero
     oh = np.zeros((1, K), dtype=np.float32)
     oh[0, 1234] = 3.0
     Y1 = tl.tl_linear(m.dev, bf16_tensor(synth.to_bf16_bits(oh))).cpu().numpy()
@@ -233,6 +237,45 @@ def test_adversarial_extreme_sums_stay_exact(oracle_mod, sign):
     ref = oracle_mod.linear_a(m.P, m.scale, M, K, X)
     Ya = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
     assert rel_err(Ya, ref) <= TOL_A
+
+
+LONG_OR_TALL = [(16, 65536), (64, 49152), (100000, 128), (40, 20000)]
+
+
+@pytest.mark.parametrize("M,K", LONG_OR_TALL)
+def test_long_k_and_tall_shapes(oracle_mod, M, K):
+    """Many K slices per row tile, or more CTAs than SMs."""
+    m = Mat(oracle_mod, M, K, seed=M % 97 + K)
+    X = synth.activations(3, K, seed=K, outlier_frac=0.01)
+    ref = oracle_mod.linear_a(m.P, m.scale, M, K, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert rel_err(Y, ref) <= TOL_A
+    *_, Yr = oracle_b(oracle_mod, m, X)
+    *_, Yb = gpu_b(m, X)
+    assert np.array_equal(Yb.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+
+
+def _scaled_tokens(K, seed):
+    """Tokens whose magnitudes leave [2^-60, 2^61): huge, tiny, one huge
+    outlier among ordinary values, and bf16 subnormals among ordinary values."""
+    base = synth.bf16_bits_to_f32(synth.activations(5, K, seed=seed))
+    x = np.array(base, dtype=np.float64)
+    x[0] *= 1e25
+    x[1] *= 1e-25
+    x[2, K // 3] = 3e20
+    x[3, ::7] = 1e-39
+    return synth.to_bf16_bits(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("M,K", [(1024, 4096), (300, 12288), (17, 129)])
+@pytest.mark.parametrize("N", [1, 5])
+def test_activations_outside_the_fixed_window(oracle_mod, M, K, N):
+    m = Mat(oracle_mod, M, K, seed=M + K)
+    X = _scaled_tokens(K, seed=M)[:N] if N > 1 else _scaled_tokens(K, seed=M)[1:2]
+    ref = oracle_mod.linear_a(m.P, m.scale, M, K, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert np.all(np.isfinite(Y))
+    assert rel_err(Y, ref) <= TOL_A
 
 
 def test_workspace_is_left_zeroed(oracle_mod):

@@ -70,7 +70,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     # a matrix whose split-K scratch would not fit the fixed array: refused
     # with TL_ERR_WORKSPACE before anything is launched
     M, K = 70000, 4096                # 4375 row tiles: ~4.5 MB of split-K scratch at 8 tokens
-    w = tl.tl_weight(0x1000, 0x2000, 0x3000, M, K, tl.TL_LAYOUT_TL2P_V1)
+    w = tl.tl_weight(0x1000, 0x2000, 0x3000, M, K, tl.TL_LAYOUT_TL2P_V2)
     arr = (tl.tl_weight * 1)(w)
     st = tl.raw_call("tl_linear_noalloc")(arr, 0x4000, None, None, 0x8000, 8, tl.TL_MODE_BF16,
                                           tl.TL_OUT_F32, 0, None)
