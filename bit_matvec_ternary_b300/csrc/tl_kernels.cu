@@ -62,6 +62,8 @@ namespace {
 
 constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
 constexpr int kCtasPerSm = 2;         // resident CTAs per SM (registers and shared memory allow 2)
+// CTAs per SM in a launch's grid.
+constexpr int kGridPerSm = 2;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 2;             // bulk copies in flight per warp
 // Tiles (512 B each) per bulk copy, smaller as the staged activations grow
@@ -461,6 +463,33 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         for (int k = 0; k < kSlots; ++k) mbar_init(bar_w + 8u * k, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int k = 0; k < kSlots && pc_on; ++k) produce(k);
+        // and the rest of this warp's tiles into L2, while the previous
+        // launch may still be running
+        if (pc_on) {
+            Cursor q = pc;
+            int qg = pgi;
+            const char *qr = prow;
+            for (bool on = true; on;) {
+                const int n = min(CH, min(q.uend - q.u, q.kw - q.b));
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 qr + (long long)(q.kb0 + q.b) * 512),
+                             "r"(n * 512)
+                             : "memory");
+                q.u += n;
+                q.b += n;
+                if (q.b == q.kw) {
+                    q.b = 0;
+                    ++q.r;
+                    if (qg + 1 < a.G && q.r == a.rt_off[qg + 1]) qr = a.packed[++qg];
+                    else qr += (long long)a.KB * 512;
+                }
+                if (q.u == q.uend) {
+                    ++q.sigma;
+                    on = cursor_enter(a, cu0, cu1, sig1, warp, q);
+                    if (on) qr = row_base(a, q.r, qg);
+                }
+            }
+        }
     }
     // this CTA's scales (and row sums) of its first slice, one per thread
     Slice P;
@@ -749,13 +778,15 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         }
         __syncthreads();
         // ---- boundary pieces of the slice, added in warp order (one thread per element)
-        if (threadIdx.x < RV) {
+        for (int i = threadIdx.x; i < nrows * RV; i += kThreads) {
+            const int rho = i / RV, e = i % RV;
+            float v = acc[i];
+#pragma unroll
             for (int w = 0; w < kWarps; ++w)
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int rho = bslot_row[w][k];
-                    if (rho >= 0) acc[rho * RV + threadIdx.x] += bslot[w][k][threadIdx.x];
-                }
+                for (int k = 0; k < 2; ++k)
+                    if (bslot_row[w][k] == rho) v += bslot[w][k][e];
+            acc[i] = v;
         }
         __syncthreads();
         if (threadIdx.x < kWarps * 2) (&bslot_row[0][0])[threadIdx.x] = -1;
@@ -971,7 +1002,7 @@ tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     if (p->U >= (1ll << 30)) return TL_ERR_SHAPE;
     // Slices: as wide as kMaxSlice allows, but narrow enough that every CTA
     // slot gets a range of at least KW - 1 units (a piece then spans <= 2 CTAs).
-    const long long slots = (long long)sms * kCtasPerSm;   // CTAs resident at once
+    const long long slots = (long long)sms * kGridPerSm;   // CTAs per launch
     long long kwt = std::min<long long>(kMaxSlice, p->U / slots + 1);
     kwt = std::max<long long>(1, std::min<long long>(kwt, p->KB));
     const int ns0 = (int)ceil_div(p->KB, kwt);
