@@ -105,6 +105,30 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def measured_traffic(alg_per_launch):
+    """DRAM bytes per launch of the decode kernel: the ncu-measured bytes per
+    algorithmic byte (profiles/tl_mma_kernel_traffic.txt) times this run's
+    average algorithmic bytes per launch; None when the record is missing or
+    the kernel source changed since it was captured."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    rec = os.path.join(here, "profiles", "tl_mma_kernel_traffic.txt")
+    src = os.path.join(here, "bit_matvec_ternary_b300", "csrc", "tl_kernels.cu")
+    try:
+        kv = {}
+        for line in open(rec):
+            line = line.strip()
+            if line and not line.startswith("#") and "=" in line:
+                k, v = line.split("=", 1)
+                kv[k] = v
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != kv["kernel_source_sha256"]:
+            return None
+        ratio = (int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])) / int(kv["algorithmic_bytes"])
+        return ratio * alg_per_launch
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------- timing
 def time_graph(stack, steps, warmup, torch):
     g = stack.graph
@@ -350,7 +374,10 @@ def main():
                        "l2": f"inputs larger than L2: {alg / 1e9:.3f} GB streamed per step vs "
                              f"{L2_BYTES / 2**20:.0f} MiB L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": gbs / hbm_peak, "traffic": None,
+                         "frac": gbs / hbm_peak, "traffic": measured_traffic(alg / launches),
+                         "traffic_note": "bytes per launch: ncu DRAM bytes per algorithmic byte "
+                                         "of one gate+up launch, times this step's mean "
+                                         "algorithmic bytes per launch",
                          "kernel": "tl_mma_kernel",
                          "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
                          "algorithmic_bytes_per_step": alg, "launches_per_step": launches,
