@@ -17,7 +17,7 @@ constexpr int kPrefillMinN = 256;
 // Bytes at the start of every workspace reserved for the status word.
 constexpr size_t kStatusBytes = 256;
 
-size_t prefill_workspace_bytes(int N, int K, int mode);
+size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms);
 bool prefill_supported(int N, int K);
 tl_status prefill_init_device();
 tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float *s,

@@ -1057,8 +1057,8 @@ size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
     for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
     const int K = Ws[0].K;
     if (tl_internal::prefill_supported(N, K))
-        return std::max(tl_internal::prefill_workspace_bytes(N, K, TL_MODE_BF16),
-                        tl_internal::prefill_workspace_bytes(N, K, TL_MODE_I8));
+        return std::max(tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_BF16, sms),
+                        tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_I8, sms));
     Plan p;
     if (make_plan(Ms, G, K, N, sms, &p) != TL_OK) return 0;
     return p.ws_bytes;

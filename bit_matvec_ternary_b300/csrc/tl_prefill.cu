@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 
@@ -56,11 +57,15 @@ struct PrefillArgs {
     int mt_off[TL_MAX_GROUP + 1];   // 128-row tiles, prefix over the group
     int G;
     int KB;                          // 128-column TL2P blocks
+    int KBS;                         // blocks per K split (grid z)
+    int S;                           // K splits
     int N;
     int mode, out;
     const float *s;
     const int32_t *z;
     int *status;                     // workspace status word
+    unsigned long long *cnt;         // [tiles] splits arrived (S > 1); zero between launches
+    float *part;                     // [tiles][S][BN][BM] partial sums (S > 1)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -199,14 +204,19 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
     const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 1);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(bars + 3 * STAGES + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt_global = blockIdx.x;
     const int nt = blockIdx.y;
+    const int split = blockIdx.z;
     int gi = 0;
     while (gi + 1 < a.G && a.mt_off[gi + 1] <= mt_global) ++gi;
     const int mt = mt_global - a.mt_off[gi];
-    const int KSTEPS = a.KB * 2;
+    // this CTA's K blocks [kb_lo, kb_hi)
+    const int kb_lo = split * a.KBS, kb_hi = min(a.KB, kb_lo + a.KBS);
+    const int NKB = kb_hi - kb_lo;
+    const int KSTEPS = NKB * 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -238,7 +248,8 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                 const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
                 if (!mbar_wait(empty(s), ph ^ 1u, a.status)) { ok = false; break; }
                 mbar_expect_tx(full_b(s), B_BYTES);
-                tma_load_2d(base + s * STAGE_BYTES + A_BYTES, &xmap, ks * BK, nt * BN, full_b(s));
+                tma_load_2d(base + s * STAGE_BYTES + A_BYTES, &xmap, kb_lo * 128 + ks * BK, nt * BN,
+                            full_b(s));
             }
             // drain: every copy this lane issued must land before the CTA exits
             const int issued = ok ? KSTEPS : 0;
@@ -281,20 +292,20 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 ring[i][r] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // zero weights
-                if (i < a.KB && rt_base + r < rts)
-                    ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + i) * 512 + lane * 16);
+                if (i < NKB && rt_base + r < rts)
+                    ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + kb_lo + i) * 512 + lane * 16);
             }
-        for (int kb0 = 0; kb0 < a.KB; kb0 += RING) {
+        for (int kb0 = 0; kb0 < NKB; kb0 += RING) {
 #pragma unroll
             for (int i = 0; i < RING; ++i) {
-                const int kb = kb0 + i;
-                if (kb < a.KB) {
+                const int kb = kb0 + i;       // block index within this split
+                if (kb < NKB) {
                     const uint4 cur0 = ring[i][0], cur1 = ring[i][1];
                     const int nb = kb + RING;
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
-                        if (nb < a.KB && rt_base + r < rts)
-                            ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + nb) * 512 + lane * 16);
+                        if (nb < NKB && rt_base + r < rts)
+                            ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + kb_lo + nb) * 512 + lane * 16);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int ks = 2 * kb + h;
@@ -318,13 +329,35 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         griddep_wait();
         const bool got = __all_sync(0xffffffffu, ok && mbar_wait(tmem_full, 0u, a.status));
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (got) {
-            const int q = warp & 3;
-            const int row = mt * BM + 32 * q + lane;
-            const bool row_ok = row < a.M[gi];
-            const float sc = row_ok ? a.scale[gi][row] : 0.f;
-            const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
-            const int Mg = a.M[gi];
+        const int q = warp & 3;
+        const int row_local = 32 * q + lane;
+        const int row = mt * BM + row_local;
+        const bool row_ok = row < a.M[gi];
+        const int Mg = a.M[gi];
+        // one finished (row, token) value: the sum of +-2 weights, halved here
+        auto emit = [&](int n, float acc2, float sc, int rsum) {
+            const float half = acc2 * 0.5f;
+            float y;
+            if (a.mode == TL_MODE_BF16) {
+                y = __fmul_rn(half, sc);
+            } else {
+                const int iacc = __float2int_rn(half);
+                if (a.out == TL_OUT_I32_RAW) {
+                    reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * Mg + row] = iacc;
+                    return;
+                }
+                const int corr = iacc - a.z[n] * rsum;
+                y = __fmul_rn(__fmul_rn((float)corr, a.s[n]), sc);
+            }
+            if (a.out == TL_OUT_F32)
+                reinterpret_cast<float *>(a.Y[gi])[(long long)n * Mg + row] = y;
+            else
+                reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * Mg + row] =
+                    __float2bfloat16_rn(y);
+        };
+        const float sc = row_ok ? a.scale[gi][row] : 0.f;
+        const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
+        if (got && a.S == 1) {
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
@@ -334,25 +367,60 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                 for (int j = 0; j < 32; ++j) {
                     const int n = nt * BN + c0 + j;
                     if (n >= a.N) break;
-                    const float half = __uint_as_float(r[j]) * 0.5f;
-                    float y;
-                    if (a.mode == TL_MODE_BF16) {
-                        y = __fmul_rn(half, sc);
-                    } else {
-                        const int iacc = __float2int_rn(half);
-                        if (a.out == TL_OUT_I32_RAW) {
-                            reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * Mg + row] = iacc;
-                            continue;
-                        }
-                        const int corr = iacc - a.z[n] * rsum;
-                        y = __fmul_rn(__fmul_rn((float)corr, a.s[n]), sc);
-                    }
-                    if (a.out == TL_OUT_F32)
-                        reinterpret_cast<float *>(a.Y[gi])[(long long)n * Mg + row] = y;
-                    else
-                        reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * Mg + row] =
-                            __float2bfloat16_rn(y);
+                    emit(n, __uint_as_float(r[j]), sc, rsum);
                 }
+            }
+        } else if (a.S > 1) {
+            // split K: this split's partial tile goes to the workspace; the CTA
+            // that completes the tile adds the splits in order and finishes it.
+            // All four epilogue warps pass both named barriers whatever
+            // happened before, so none can be left waiting.
+            const long long tile = (long long)mt_global * gridDim.y + nt;
+            float *mine = a.part + (tile * a.S + split) * BN * BM;
+            if (got) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(mine + (long long)(c0 + j) * BM + row_local, __uint_as_float(r[j]));
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
+            if (warp == 2 && lane == 0) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                const unsigned long long before = atomicAdd(a.cnt + tile, 1ull);
+                *last_flag = before + 1 == (unsigned long long)a.S ? 1 : 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
+            if (*last_flag) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                const float *p0 = a.part + tile * a.S * BN * BM;
+                if (row_ok) {
+                    // 32 tokens at a time: each split's 32 loads are issued together
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BN && nt * BN + c0 < a.N; c0 += 32) {
+                        float acc2[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc2[j] = 0.f;
+#pragma unroll 1
+                        for (int sp = 0; sp < a.S; ++sp) {
+                            const float *ps = p0 + ((long long)sp * BN + c0) * BM + row_local;
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __ldcg(ps + (long long)j * BM);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) acc2[j] = __fadd_rn(acc2[j], v[j]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int n = nt * BN + c0 + j;
+                            if (n < a.N) emit(n, acc2[j], sc, rsum);
+                        }
+                    }
+                }
+                if (warp == 2 && lane == 0) a.cnt[tile] = 0ull;
             }
         }
     }
@@ -394,12 +462,46 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // ------------------------------------------------------------------ host side
 namespace tl_internal {
 
-size_t prefill_workspace_bytes(int N, int K, int mode) {
-    // status word block + bf16 copy of the int8 activations in mode B (zeroed
-    // again after use, so the workspace stays zero-filled between calls)
-    size_t b = kStatusBytes;
-    if (mode == TL_MODE_I8) b += ((size_t)N * K * 2 + 255) / 256 * 256;
-    return b;
+namespace {
+// K splits for a group: enough CTAs to cover the SMs when the tiles alone
+// do not, each split at least 4 blocks of 128 columns.
+int prefill_splits(int tiles, int KB, int sms) {
+    if (tiles >= sms) return 1;
+    return std::max(1, std::min(sms / tiles, KB / 4));
+}
+
+// Workspace of a prefill call, after the status block:
+//   [the decode path's arrival counters for these matrices: never touched here]
+//   [arrival counter per tile, if K is split: cleared at the start of the call]
+//   [bf16 copy of the int8 activations, mode B]
+//   [fp32 partial tiles, if K is split]
+// so prefill and decode calls may share one workspace in any order.
+struct PrefillLayout {
+    size_t cnt, conv, part, total;
+};
+PrefillLayout prefill_layout(const tl_weight *Ws, int G, int N, int K, int mode, int tiles, int S) {
+    size_t R = 0;
+    for (int g = 0; g < G; ++g) R += (size_t)(Ws[g].M + 15) / 16;
+    PrefillLayout L;
+    L.cnt = kStatusBytes + (R * 8 + 255) / 256 * 256;
+    L.conv = L.cnt + (S > 1 ? ((size_t)tiles * 8 + 255) / 256 * 256 : 0);
+    L.part = L.conv + (mode == TL_MODE_I8 ? ((size_t)N * K * 2 + 255) / 256 * 256 : 0);
+    L.total = L.part + (S > 1 ? (size_t)tiles * S * tlp::BN * tlp::BM * 4 : 0);
+    return L;
+}
+int prefill_tiles(const tl_weight *Ws, int G, int N) {
+    int mt = 0;
+    for (int g = 0; g < G; ++g) mt += (Ws[g].M + tlp::BM - 1) / tlp::BM;
+    return mt * ((N + tlp::BN - 1) / tlp::BN);
+}
+}  // namespace
+
+size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms) {
+    const int tiles = prefill_tiles(Ws, G, N);
+    int S = prefill_splits(tiles, (K + 127) / 128, sms);
+    const int KBS = ((K + 127) / 128 + S - 1) / S;
+    S = ((K + 127) / 128 + KBS - 1) / KBS;
+    return prefill_layout(Ws, G, N, K, mode, tiles, S).total;
 }
 
 bool prefill_supported(int N, int K) { return N >= kPrefillMinN && (K % 8) == 0; }
@@ -415,7 +517,11 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
                          const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,
                          size_t ws_bytes, unsigned flags, cudaStream_t stream) {
     const int K = Ws[0].K;
-    if (!ws || ws_bytes < prefill_workspace_bytes(N, K, mode)) return TL_ERR_WORKSPACE;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TL_ERR_CUDA;
+    if (!ws || ws_bytes < prefill_workspace_bytes(Ws, G, N, K, mode, sms)) return TL_ERR_WORKSPACE;
     tlp::PrefillArgs a;
     std::memset(&a, 0, sizeof a);
     a.G = G;
@@ -429,6 +535,10 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
         a.mt_off[g + 1] = a.mt_off[g] + (Ws[g].M + tlp::BM - 1) / tlp::BM;
     }
     a.KB = (K + 127) / 128;
+    const int tiles = a.mt_off[G] * ((N + tlp::BN - 1) / tlp::BN);
+    a.S = prefill_splits(tiles, a.KB, sms);
+    a.KBS = (a.KB + a.S - 1) / a.S;
+    a.S = (a.KB + a.KBS - 1) / a.KBS;          // no empty split
     a.N = N;
     a.mode = mode;
     a.out = out;
@@ -436,9 +546,15 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     a.z = z;
     a.status = static_cast<int *>(ws);
 
+    const PrefillLayout L = prefill_layout(Ws, G, N, K, mode, tiles, a.S);
+    char *wsc = static_cast<char *>(ws);
     const void *xb = X;
-    __nv_bfloat16 *conv = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(ws) + kStatusBytes);
+    __nv_bfloat16 *conv = reinterpret_cast<__nv_bfloat16 *>(wsc + L.conv);
     const long long n = (long long)N * K;
+    a.cnt = reinterpret_cast<unsigned long long *>(wsc + L.cnt);
+    a.part = reinterpret_cast<float *>(wsc + L.part);
+    if (a.S > 1 && cudaMemsetAsync(a.cnt, 0, (size_t)tiles * 8, stream) != cudaSuccess)
+        return TL_ERR_CUDA;
     if (mode == TL_MODE_I8) {
         tlp::tl_i8_to_bf16_kernel<<<592, 256, 0, stream>>>(static_cast<const int8_t *>(X), conv, n);
         if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
@@ -458,7 +574,7 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)a.mt_off[G], (unsigned)((N + tlp::BN - 1) / tlp::BN));
+    cfg.gridDim = dim3((unsigned)a.mt_off[G], (unsigned)((N + tlp::BN - 1) / tlp::BN), (unsigned)a.S);
     cfg.blockDim = dim3(tlp::THREADS);
     cfg.dynamicSmemBytes = tlp::SMEM_BYTES;
     cfg.stream = stream;
@@ -468,8 +584,6 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     cfg.attrs = attr;
     cfg.numAttrs = (flags & TL_FLAG_PDL) && mode != TL_MODE_I8 ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map) != cudaSuccess) return TL_ERR_CUDA;
-    if (mode == TL_MODE_I8 && cudaMemsetAsync(conv, 0, (size_t)n * 2, stream) != cudaSuccess)
-        return TL_ERR_CUDA;
     return TL_OK;
 }
 

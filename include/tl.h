@@ -121,9 +121,10 @@ TL_API tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K
                              int64_t *bad_codes);
 
 /* Device workspace needed by tl_linear / tl_linear_group for these shapes
- * and this N (all matrices in Ws share K).  The workspace holds split-K
- * partial sums and per-row-tile counters.  It must be zero-filled before its
- * first use; every call leaves it zero-filled again when it completes.  One
+ * and this N (all matrices in Ws share K).  The workspace holds a status word,
+ * per-row-tile arrival counters and split-K partial sums.  It must be
+ * zero-filled before its first use; every call leaves the status word and the
+ * arrival counters zero again when it completes (the rest is scratch).  One
  * workspace may serve any sequence of calls on one stream, but calls that
  * overlap on the GPU must not share it. */
 TL_API size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N);
