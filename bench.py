@@ -109,7 +109,7 @@ def measured_traffic(alg_per_launch):
     """DRAM bytes per launch of the decode kernel: the ncu-measured bytes per
     algorithmic byte (profiles/tl_mma_kernel_traffic.txt) times this run's
     average algorithmic bytes per launch; None when the record is missing or
-    the kernel source changed since it was captured."""
+    the kernel's device code changed since it was captured."""
     import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
     rec = os.path.join(here, "profiles", "tl_mma_kernel_traffic.txt")
@@ -121,7 +121,9 @@ def measured_traffic(alg_per_launch):
             if line and not line.startswith("#") and "=" in line:
                 k, v = line.split("=", 1)
                 kv[k] = v
-        if hashlib.sha256(open(src, "rb").read()).hexdigest() != kv["kernel_source_sha256"]:
+        text = open(src).read()
+        device = text[:text.index("// ------------------------------------------------------------------ host side")]
+        if hashlib.sha256(device.encode()).hexdigest() != kv["device_source_sha256"]:
             return None
         ratio = (int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])) / int(kv["algorithmic_bytes"])
         return ratio * alg_per_launch
