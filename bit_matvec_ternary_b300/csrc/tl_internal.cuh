@@ -17,6 +17,23 @@ constexpr int kPrefillMinN = 256;
 // Bytes at the start of every workspace reserved for the status word.
 constexpr size_t kStatusBytes = 256;
 
+// Workspace layout of every call.  The bytes a call needs zero when it
+// starts, and leaves zero when it ends (status word, arrival counters,
+// exchange slots), sit at the front; its scratch (partial sums, per-call
+// counters cleared at the call's start, converted activations) sits at the
+// back, ending at the workspace's end.  A call asks for twice the larger of
+// the two (plus alignment), so any calls sharing a workspace of the largest
+// size asked for never write into one another's front bytes.
+inline size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+inline size_t workspace_need(size_t front, size_t back) {
+    return 2 * (front > back ? front : back) + 256;
+}
+// Offset of a call's scratch of `back` bytes in a workspace of `ws_bytes`
+// (256-aligned; the workspace itself is 256-aligned).
+inline size_t scratch_offset(size_t ws_bytes, size_t back) {
+    return (ws_bytes - back) / 256 * 256;
+}
+
 size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms);
 bool prefill_supported(int N, int K);
 tl_status prefill_init_device();
@@ -25,9 +42,9 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
                          size_t ws_bytes, unsigned flags, cudaStream_t stream);
 
 // The N <= 8 decode / verify kernel over all N in chunks of 8, with a given
-// scratch buffer; `need` is the scratch it requires for these shapes and
-// `zeroed` the leading bytes (status word and arrival counters) that must
-// be zero when a call starts.
+// scratch buffer used by this call alone; `need` is the scratch it requires
+// for these shapes and `zeroed` the leading bytes (status word, arrival
+// counters and exchange slots) that must be zero when a call starts.
 tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t *zeroed);
 tl_status launch_decode(const tl_weight *Ws, int G, const void *X, const float *s,
                         const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,

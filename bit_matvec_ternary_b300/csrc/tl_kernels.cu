@@ -74,7 +74,13 @@ constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSlice = 32;         // 128-column blocks per K slice (64 KB of X at 8 tokens)
 constexpr int kMaxCtaRows = 16;       // row tiles one CTA may touch in one slice
-constexpr int kStageBatch = 4;        // activation loads in flight per thread while staging
+// 16-byte activation loads in flight per thread while staging a slice: all
+// of a slice at once, up to 8 (4 at eight tokens, where more registers spill).
+__host__ __device__ constexpr int stage_batch(int nt, bool mode_a) {
+    return (nt * kMaxSlice * (mode_a ? 16 : 8) + kThreads - 1) / kThreads < (nt == 8 ? 4 : 8)
+               ? (nt * kMaxSlice * (mode_a ? 16 : 8) + kThreads - 1) / kThreads
+               : (nt == 8 ? 4 : 8);
+}
 constexpr long long kWaitLimit = 1ll << 31;   // SM cycles before a wait gives up
 // Activations are staged times 2^kT: a k-step class q product is then
 // (1 - w) * x * 2^(2q - 66), a normal fp32 number for |x| in [2^-60, 2^61).
@@ -193,8 +199,9 @@ struct GroupArgs {
     int mode;
     int out;
     int xvec;       // X rows allow 16-byte loads (16-byte aligned, K a multiple of 8 / 16)
-    float *part;    // pieces of row tiles finished across CTAs [R][NS][2][N][16]
-    unsigned long long *cnt;  // [R] blocks arrived; zero between launches
+    float *part;    // pieces of row tiles finished across CTAs [R][NS][2][N][16] (NS > 1)
+    unsigned long long *cnt;  // [R] blocks arrived (NS > 1); zero between launches
+    unsigned long long *xslot;  // [R][N][16] exchange slots (NS == 1); zero between launches
     int *status;    // workspace status word
 };
 
@@ -306,6 +313,45 @@ __device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const 
         }
 }
 
+// Row tile r of a one-slice launch whose blocks are split between two CTAs:
+// each CTA swaps its piece of every element into the element's exchange slot
+// (bit 32 set = occupied).  The CTA that finds the other piece there adds the
+// two, stores the element and empties the slot; the other finds the slot
+// empty and is done.  One atomic round trip, and the sum does not depend on
+// which CTA comes second (a + b == b + a in floating point).
+__device__ __forceinline__ void exchange_row_tile(const GroupArgs &a, int r, const float *v,
+                                                  const float *sc, const int *rs, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    int gi = 0;
+    while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
+    const int rl = r - a.rt_off[gi];
+    unsigned long long *slot = a.xslot + (long long)r * a.N * 16;
+    // every swap in flight before any result is used
+    unsigned long long old[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = g + 8 * h, n = 2 * t + e;
+            old[h][e] = n < a.N ? atomicExch(slot + n * 16 + i,
+                                             (1ull << 32) | __float_as_uint(v[n * 16 + i]))
+                                : 0ull;
+        }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = g + 8 * h, m = rl * 16 + i, n = 2 * t + e;
+            if (old[h][e] >> 32) {
+                slot[n * 16 + i] = 0ull;
+                if (m < a.M[gi])
+                    store_out(a, gi, m, n,
+                              __fadd_rn(__uint_as_float((uint32_t)old[h][e]), v[n * 16 + i]),
+                              sc[i], rs[i]);
+            }
+        }
+}
+
 // One 128-column block of one 16-row tile: 8 MMAs (k-steps m = 0..7) over
 // the lane's 16-byte slice of the tile (w) and the 4 B-fragment quarters (b).
 // Register j of k-step m is word j shifted right by 8*(m/4) and masked to the
@@ -365,18 +411,30 @@ __device__ __forceinline__ uint32_t scale_any(uint32_t h, int d) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// dst[4 * tt] = w[tt] for tt = 0..3, written in the order tt = (it + q) % 4.
+__device__ __forceinline__ void store_rotated(uint32_t *dst, const uint32_t (&w)[4], int q) {
+    const bool r1 = q & 1, r2 = q & 2;
+    const uint32_t a0 = r1 ? w[1] : w[0], a1 = r1 ? w[2] : w[1];
+    const uint32_t a2 = r1 ? w[3] : w[2], a3 = r1 ? w[0] : w[3];
+    const uint32_t b0 = r2 ? a2 : a0, b1 = r2 ? a3 : a1, b2 = r2 ? a0 : a2, b3 = r2 ? a1 : a3;
+    dst[4 * (q & 3)] = b0;
+    dst[4 * ((q + 1) & 3)] = b1;
+    dst[4 * ((q + 2) & 3)] = b2;
+    dst[4 * ((q + 3) & 3)] = b3;
+}
+
 // The activation groups of one slice: VPL activations per group, LB groups
-// per 128-column block, N * kw * LB groups in all, taken kStageBatch *
-// kThreads at a time starting at `base`.
-template <bool kModeA>
+// per 128-column block, N * kw * LB groups in all, taken SB * kThreads at a
+// time starting at `base`.
+template <bool kModeA, int SB>
 __device__ __forceinline__ void stage_load(const GroupArgs &a, const Slice &P, int base,
-                                           uint4 (&v)[kStageBatch]) {
+                                           uint4 (&v)[SB]) {
     constexpr int VPL = kModeA ? 8 : 16;
     constexpr int LB = 128 / VPL;
     const int total = a.N * P.kw * LB;
     const FastDiv dv = P.sigma == a.NS - 1 ? a.dKWL : a.dKW;
 #pragma unroll
-    for (int i = 0; i < kStageBatch; ++i) {
+    for (int i = 0; i < SB; ++i) {
         const int idx = base + i * kThreads + (int)threadIdx.x;
         v[i] = make_uint4(0u, 0u, 0u, 0u);
         if (idx < total) {
@@ -401,6 +459,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     constexpr int RV = 16 * NT;                 // floats per row-tile result
     constexpr int VPL = kModeA ? 8 : 16;        // activations per staging group
     constexpr int LB = 128 / VPL;               // staging groups per block
+    constexpr int SB = stage_batch(NT, kModeA); // staging loads in flight per thread
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;                                                // [kWarps][kSlots][SLOT]
     uint4 *xs = reinterpret_cast<uint4 *>(smem + ring_bytes(NT));      // one slice of X
@@ -515,12 +574,27 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     if (N < NT)   // the columns past the batch stay zero in every slice
         for (int i = threadIdx.x; i < a.KW * 64 * NT; i += kThreads)
             if (((i >> 4) % NT) >= N) xw[i] = 0u;
+    // Warm L2 (and the address translation) for this CTA's activations; a
+    // prefetch returns no data, so it may run before the previous kernel has
+    // written them.  One 128-byte line per thread per step, addresses inside
+    // each row's columns [k_lo, k_hi).
+    if (sig1 > sig0) {
+        constexpr int EB = kModeA ? 2 : 1;
+        const long long k_lo = (long long)sig0 * a.KW * 128;
+        const long long k_hi = min((long long)a.K, (long long)sig1 * a.KW * 128);
+        const int lines = (int)((k_hi - k_lo) * EB + 127) / 128;
+        for (int i = threadIdx.x; i < N * lines; i += kThreads) {
+            const int n = i / lines, l = i - n * lines;
+            const char *p = reinterpret_cast<const char *>(a.X) + ((long long)n * a.K + k_lo) * EB + l * 128;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
+    }
     __syncthreads();
 
     // Now the activations, written by the previous kernel.
     griddep_wait();
-    uint4 xv[kStageBatch];
-    stage_load<kModeA>(a, P, 0, xv);
+    uint4 xv[SB];
+    stage_load<kModeA, SB>(a, P, 0, xv);
 
     Cursor cc;
     cc.sigma = sig0;
@@ -543,10 +617,10 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         {
             const int total = N * P.kw * LB;
             const FastDiv dv = sigma == a.NS - 1 ? a.dKWL : a.dKW;
-            for (int base = 0; base < total; base += kThreads * kStageBatch) {
-                if (sigma != sig0 || base != 0) stage_load<kModeA>(a, P, base, xv);
+            for (int base = 0; base < total; base += kThreads * SB) {
+                if (sigma != sig0 || base != 0) stage_load<kModeA, SB>(a, P, base, xv);
 #pragma unroll
-                for (int i = 0; i < kStageBatch; ++i) {
+                for (int i = 0; i < SB; ++i) {
                     if (base + i * kThreads >= total) break;   // uniform over the block
                     const int idx = base + i * kThreads + (int)threadIdx.x;
                     const bool valid = idx < total;
@@ -557,8 +631,9 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                     if (valid) {
                         const uint32_t wd[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
                         if (kModeA) {
-                            const int m = o >> 1;
-                            uint32_t *dst = xw + ((jb * 4 + (m >> 1)) * NT + n) * 16 + 2 * (m & 1) + (o & 1);
+                            const int m = o >> 1, qd = m >> 1;
+                            uint32_t *dst = xw + ((jb * 4 + qd) * NT + n) * 16 + 2 * (m & 1) + (o & 1);
+                            uint32_t st[4];
 #pragma unroll
                             for (int tt = 0; tt < 4; ++tt) {
                                 const uint32_t v = wd[tt];
@@ -568,15 +643,19 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                                 const uint32_t nz = __vcmpne2(v & 0x7FFF7FFFu, 0u);
                                 const uint32_t off = __vsub2(v & 0x7F807F80u, (uint32_t)kWinLo * 0x00800080u);
                                 bad |= __vcmpgtu2(off, (uint32_t)(kWinHi - kWinLo) * 0x00800080u) & nz;
-                                dst[tt * 4] = v + ((uint32_t)kT * 0x00800080u & nz);
+                                st[tt] = v + ((uint32_t)kT * 0x00800080u & nz);
                             }
+                            // store word tt = (it + qd) % 4 at step it: the lanes of one
+                            // block quarter apart then write different banks
+                            store_rotated(dst, st, qd);
                         } else {
-                            const int m = o;
-                            uint32_t *dst = xw + ((jb * 4 + (m >> 1)) * NT + n) * 16 + 2 * (m & 1);
+                            const int m = o, qd = m >> 1;
+                            uint32_t *dst = xw + ((jb * 4 + qd) * NT + n) * 16 + 2 * (m & 1);
                             const float two_t = __int_as_float((kT + 127) << 23);
                             int isum = 0;
 #pragma unroll
-                            for (int h8 = 0; h8 < 2; ++h8)
+                            for (int h8 = 0; h8 < 2; ++h8) {
+                                uint32_t st[4];
 #pragma unroll
                                 for (int tt = 0; tt < 4; ++tt) {
                                     const uint32_t word = wd[2 * h8 + (tt >> 1)] >> (16 * (tt & 1));
@@ -585,8 +664,10 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                                     isum += qlo + qhi;
                                     const __nv_bfloat162 b2 = __floats2bfloat162_rn(
                                         __fmul_rn((float)qlo, two_t), __fmul_rn((float)qhi, two_t));
-                                    dst[tt * 4 + h8] = *reinterpret_cast<const uint32_t *>(&b2);
+                                    st[tt] = *reinterpret_cast<const uint32_t *>(&b2);
                                 }
+                                store_rotated(dst + h8, st, qd);
+                            }
                             sum = (float)isum;
                         }
                     }
@@ -808,6 +889,8 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 __syncwarp();
                 if (a.NS == 1 && lo == 0 && hi == P.kw) {
                     store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
+                } else if (a.NS == 1) {
+                    exchange_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
                 } else {
                     const int half = lo == 0 ? 0 : 1;   // 0: holds the slice's first block
                     float *dst = a.part + (((long long)r * a.NS + sigma) * 2 + half) * N * 16;
@@ -821,16 +904,42 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                     now = __shfl_sync(0xffffffffu, now, 0);
                     if (now == (unsigned long long)a.KB) {
                         asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                        // all pieces, slice by slice, the half with the slice's first block first
-                        for (int e = lane; e < N * 16; e += 32) {
-                            float y = 0.f;
-                            for (int s2 = 0; s2 < a.NS; ++s2) {
-                                const float *pc2 = a.part + ((long long)r * a.NS + s2) * 2 * N * 16;
-                                y = __fadd_rn(y, __ldcg(pc2 + e));
-                                if (piece_split(a, r, s2)) y = __fadd_rn(y, __ldcg(pc2 + N * 16 + e));
+                        // all pieces, slice by slice, the half with the slice's first
+                        // block first; kPS slices' loads in flight at a time
+                        constexpr int kE = (16 * NT + 31) / 32;   // elements per lane
+                        constexpr int kPS = NT >= 8 ? 2 : 4;       // slices per batch of loads
+                        float y[kE];
+#pragma unroll
+                        for (int j = 0; j < kE; ++j) y[j] = 0.f;
+                        for (int s0 = 0; s0 < a.NS; s0 += kPS) {
+                            float pv[kPS][2][kE];
+#pragma unroll
+                            for (int ds = 0; ds < kPS; ++ds) {
+                                const int s2 = s0 + ds;
+                                const bool have = s2 < a.NS;
+                                const bool split = have && piece_split(a, r, s2);
+                                const float *pc2 = a.part + ((long long)r * a.NS + (have ? s2 : 0)) * 2 * N * 16;
+#pragma unroll
+                                for (int j = 0; j < kE; ++j) {
+                                    const int e = lane + 32 * j;
+                                    pv[ds][0][j] = have && e < N * 16 ? __ldcg(pc2 + e) : 0.f;
+                                    pv[ds][1][j] = split && e < N * 16 ? __ldcg(pc2 + N * 16 + e) : 0.f;
+                                }
                             }
-                            v[e] = y;
+#pragma unroll
+                            for (int ds = 0; ds < kPS; ++ds) {
+                                if (s0 + ds >= a.NS) break;
+                                const bool split = piece_split(a, r, s0 + ds);
+#pragma unroll
+                                for (int j = 0; j < kE; ++j) {
+                                    y[j] = __fadd_rn(y[j], pv[ds][0][j]);
+                                    if (split) y[j] = __fadd_rn(y[j], pv[ds][1][j]);
+                                }
+                            }
                         }
+#pragma unroll
+                        for (int j = 0; j < kE; ++j)
+                            if (lane + 32 * j < N * 16) v[lane + 32 * j] = y[j];
                         __syncwarp();
                         store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
                         if (lane == 0) a.cnt[r] = 0ull;
@@ -974,6 +1083,9 @@ struct Plan {
     int R, KB, KW, KWL, NS, P, Lc, rows;
     long long U;
     size_t smem;       // dynamic shared memory for the given N
+    size_t cnt_bytes;  // arrival counters (front of the workspace, after the status word)
+    size_t front;      // status word, counters and exchange slots: zero between calls
+    size_t back;       // partial sums of row tiles across slices (scratch)
     size_t ws_bytes;   // workspace for the given N
 };
 
@@ -1030,8 +1142,12 @@ tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     const int nt = padded_tokens(std::min(std::max(N, 1), kNMax));
     const int n = std::min(std::max(N, 1), kNMax);
     p->smem = dyn_smem(nt, p->KW, p->rows);
-    const size_t cnt_bytes = ((size_t)p->R * 8 + 255) / 256 * 256;
-    p->ws_bytes = tl_internal::kStatusBytes + cnt_bytes + (size_t)p->R * p->NS * 2 * 16 * n * 4;
+    using tl_internal::round256;
+    p->cnt_bytes = round256((size_t)p->R * 8);
+    const size_t slot_bytes = p->NS == 1 ? round256((size_t)p->R * n * 16 * 8) : 0;
+    p->front = tl_internal::kStatusBytes + p->cnt_bytes + slot_bytes;
+    p->back = p->NS > 1 ? (size_t)p->R * p->NS * 2 * 16 * n * 4 : 0;
+    p->ws_bytes = tl_internal::workspace_need(p->front, p->back);
     return TL_OK;
 }
 
@@ -1097,10 +1213,11 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     a.z = z ? z + n0 : nullptr;
     a.N = n; a.mode = mode; a.out = out;
     a.xvec = aligned(a.X, 16) && (K % (mode == TL_MODE_BF16 ? 8 : 16)) == 0;
-    const size_t cnt_bytes = ((size_t)p.R * 8 + 255) / 256 * 256;
     char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
     a.cnt = reinterpret_cast<unsigned long long *>(wsb);
-    a.part = reinterpret_cast<float *>(wsb + cnt_bytes);
+    a.xslot = reinterpret_cast<unsigned long long *>(wsb + p.cnt_bytes);
+    a.part = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                       tl_internal::scratch_offset(ws_bytes, p.back));
     a.status = static_cast<int *>(ws);
 
     cudaLaunchConfig_t cfg;
@@ -1133,7 +1250,7 @@ tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t 
     const tl_status pst = make_plan(Ms, G, Ws[0].K, kNMax, dev->sms, &p);  // chunks <= 8 tokens
     if (pst != TL_OK) return pst;
     *need = p.ws_bytes;
-    *zeroed = kStatusBytes + ((size_t)p.R * 8 + 255) / 256 * 256;
+    *zeroed = p.front;
     return TL_OK;
 }
 

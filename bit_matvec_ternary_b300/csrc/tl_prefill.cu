@@ -470,23 +470,23 @@ int prefill_splits(int tiles, int KB, int sms) {
     return std::max(1, std::min(sms / tiles, KB / 4));
 }
 
-// Workspace of a prefill call, after the status block:
-//   [the decode path's arrival counters for these matrices: never touched here]
+// Workspace of a prefill call: the status word at the front, nothing else
+// kept zero; its scratch at the back, ending at the workspace's end:
 //   [arrival counter per tile, if K is split: cleared at the start of the call]
 //   [bf16 copy of the int8 activations, mode B]
 //   [fp32 partial tiles, if K is split]
-// so prefill and decode calls may share one workspace in any order.
+// (offsets below are from the start of that scratch), so prefill and decode
+// calls may share one workspace in any order.
 struct PrefillLayout {
-    size_t cnt, conv, part, total;
+    size_t cnt, conv, part, back;
 };
-PrefillLayout prefill_layout(const tl_weight *Ws, int G, int N, int K, int mode, int tiles, int S) {
-    size_t R = 0;
-    for (int g = 0; g < G; ++g) R += (size_t)(Ws[g].M + 15) / 16;
+PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S) {
+    using tl_internal::round256;
     PrefillLayout L;
-    L.cnt = kStatusBytes + (R * 8 + 255) / 256 * 256;
-    L.conv = L.cnt + (S > 1 ? ((size_t)tiles * 8 + 255) / 256 * 256 : 0);
-    L.part = L.conv + (mode == TL_MODE_I8 ? ((size_t)N * K * 2 + 255) / 256 * 256 : 0);
-    L.total = L.part + (S > 1 ? (size_t)tiles * S * tlp::BN * tlp::BM * 4 : 0);
+    L.cnt = 0;
+    L.conv = L.cnt + (S > 1 ? round256((size_t)tiles * 8) : 0);
+    L.part = L.conv + (mode == TL_MODE_I8 ? round256((size_t)N * K * 2) : 0);
+    L.back = L.part + (S > 1 ? (size_t)tiles * S * tlp::BN * tlp::BM * 4 : 0);
     return L;
 }
 int prefill_tiles(const tl_weight *Ws, int G, int N) {
@@ -501,7 +501,7 @@ size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mod
     int S = prefill_splits(tiles, (K + 127) / 128, sms);
     const int KBS = ((K + 127) / 128 + S - 1) / S;
     S = ((K + 127) / 128 + KBS - 1) / KBS;
-    return prefill_layout(Ws, G, N, K, mode, tiles, S).total;
+    return workspace_need(kStatusBytes, prefill_layout(N, K, mode, tiles, S).back);
 }
 
 bool prefill_supported(int N, int K) { return N >= kPrefillMinN && (K % 8) == 0; }
@@ -546,8 +546,8 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     a.z = z;
     a.status = static_cast<int *>(ws);
 
-    const PrefillLayout L = prefill_layout(Ws, G, N, K, mode, tiles, a.S);
-    char *wsc = static_cast<char *>(ws);
+    const PrefillLayout L = prefill_layout(N, K, mode, tiles, a.S);
+    char *wsc = static_cast<char *>(ws) + scratch_offset(ws_bytes, L.back);
     const void *xb = X;
     __nv_bfloat16 *conv = reinterpret_cast<__nv_bfloat16 *>(wsc + L.conv);
     const long long n = (long long)N * K;

@@ -122,11 +122,12 @@ TL_API tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K
 
 /* Device workspace needed by tl_linear / tl_linear_group for these shapes
  * and this N (all matrices in Ws share K).  The workspace holds a status word,
- * per-row-tile arrival counters and split-K partial sums.  It must be
- * zero-filled before its first use; every call leaves the status word and the
- * arrival counters zero again when it completes (the rest is scratch).  One
- * workspace may serve any sequence of calls on one stream, but calls that
- * overlap on the GPU must not share it. */
+ * per-row-tile arrival counters and exchange slots at its front, and split-K
+ * partial sums (scratch) at its back, ending at the workspace's end.  It must
+ * be zero-filled before its first use and 256-byte aligned; every call leaves
+ * its front bytes zero again when it completes.  One workspace of the largest
+ * size asked for by a set of calls may serve any sequence of those calls, of
+ * any shapes, on one stream; calls that overlap on the GPU must not share it. */
 TL_API size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N);
 
 /* DEVICE.  Per-token activation quantisation (bf16 -> int8).  X_bf16 [N][K]
@@ -176,8 +177,8 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
  * they run a linear -- code inside another runtime's memory pool, a loop
  * that must not allocate after start-up, or a host that only hands over
  * input and output buffers.  The caller still passes W, X, s, z and Y
- * exactly as for tl_linear; the split-K partial sums and arrival counters
- * that tl_linear keeps in the caller's workspace live instead in a
+ * exactly as for tl_linear; the split-K partial sums, arrival counters and
+ * exchange slots that tl_linear keeps in the caller's workspace live instead in a
  * file-scope __device__ array of TL_NOALLOC_SCRATCH_BYTES bytes, which every
  * GPU that loads the library holds until the process exits.
  *   - Any N >= 1 runs on the decode / verify kernel in chunks of 8 tokens
@@ -185,7 +186,7 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
  *   - Shapes whose scratch would exceed TL_NOALLOC_SCRATCH_BYTES return
  *     TL_ERR_WORKSPACE before anything is launched.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
- *     routine.  Each call clears the array's status word and counters with
+ *     routine.  Each call clears the array's status word, counters and slots with
  *     cudaMemsetAsync on `stream` before its launches.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make

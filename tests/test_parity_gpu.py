@@ -287,8 +287,50 @@ def test_workspace_is_left_zeroed(oracle_mod):
     torch.cuda.synchronize()
     nbytes = tl.tl_workspace_bytes([m.dev], 8)
     R = (4096 + 15) // 16
-    assert int(ws[: 256 + 8 * R].count_nonzero()) == 0     # status word + arrival counters
+    front = 256 + _round256(8 * R) + _round256(R * 8 * 16 * 8)   # status, counters, exchange slots
+    assert int(ws[:front].count_nonzero()) == 0
     assert nbytes <= ws.numel()
+
+
+def _round256(b):
+    return (b + 255) // 256 * 256
+
+
+def test_calls_of_different_shapes_share_one_workspace(oracle_mod):
+    """One workspace serves calls of any shapes in any order: a one-slice
+    group (exchange slots), a three-slice matrix (counters and partial sums),
+    a small one-slice matrix and a split-K prefill, twice over, each result
+    checked against the oracle."""
+    big = [Mat(oracle_mod, 12288, 4096, seed=90), Mat(oracle_mod, 12288, 4096, seed=91)]
+    tall_k = Mat(oracle_mod, 4096, 12288, seed=92)
+    small = Mat(oracle_mod, 1024, 4096, seed=93)
+    groups = [[m.dev for m in big], [tall_k.dev], [small.dev]]
+    ws = tl.make_workspace(groups + [[small.dev]], 8)
+    need = max(ws.numel(), tl.tl_workspace_bytes([small.dev], 300))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    X1 = synth.activations(1, 4096, seed=94)
+    X8 = synth.activations(8, 12288, seed=95)
+    X3 = synth.activations(3, 4096, seed=96)
+    X300 = synth.activations(300, 4096, seed=97)
+    for _ in range(2):
+        y_small = tl.tl_linear(small.dev, bf16_tensor(X3), workspace=ws)
+        y_tall = tl.tl_linear(tall_k.dev, bf16_tensor(X8), workspace=ws)
+        y_big = tl.tl_linear_group([m.dev for m in big], bf16_tensor(X1), workspace=ws)
+        Q, s, z = tl.tl_quantize_act(bf16_tensor(X300))
+        y_pre = tl.tl_linear(small.dev, Q, s, z, mode=tl.TL_MODE_I8, workspace=ws)
+        y_small2 = tl.tl_linear(small.dev, bf16_tensor(X3), workspace=ws)
+        torch.cuda.synchronize()
+        assert rel_err(y_small.cpu().numpy(), oracle_mod.linear_a(small.P, small.scale, 1024, 4096, X3)) <= TOL_A
+        assert rel_err(y_small2.cpu().numpy(), oracle_mod.linear_a(small.P, small.scale, 1024, 4096, X3)) <= TOL_A
+        assert rel_err(y_tall.cpu().numpy(), oracle_mod.linear_a(tall_k.P, tall_k.scale, 4096, 12288, X8)) <= TOL_A
+        for m, y in zip(big, y_big):
+            assert rel_err(y.cpu().numpy(), oracle_mod.linear_a(m.P, m.scale, m.M, m.K, X1)) <= TOL_A
+        Qr, sr, zr = oracle_mod.quant(X300)
+        _, Yr = oracle_mod.linear_b(small.P, small.scale, small.rowsum, 1024, 4096, Qr, sr, zr)
+        assert np.array_equal(y_pre.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+    R_big = 2 * 12288 // 16
+    front = 256 + _round256(8 * R_big) + _round256(R_big * 1 * 16 * 8)
+    assert int(ws[:front].count_nonzero()) == 0
 
 
 def test_pdl_flag_gives_identical_results(oracle_mod):
