@@ -14,13 +14,13 @@
 //     of one mma n8 tile.
 //
 // Kernel tl_mma_kernel (N <= 8, modes A and B):
-//   Work.  K is cut into slices of at most kMaxSlice 128-column blocks.  The
-//   launch's (16-row tile, block) units are ordered slice by slice, then row
-//   tile by row tile; CTA c owns the contiguous range [c*Lc, (c+1)*Lc), so
-//   every CTA streams the same number of bytes, stages only the activations
-//   of the one or two slices it touches, and a (row tile, slice) piece spans
-//   at most two CTAs.  The 16 warps split the CTA's units of a slice into
-//   contiguous ranges.
+//   Work.  K is cut into as few slices of at most kMaxSlice 128-column
+//   blocks as it needs.  The launch's (16-row tile, block) units are ordered
+//   slice by slice, then row tile by row tile; each slice has its own Pps
+//   CTAs, and CTA c owns a contiguous range of Lc units of slice c / Pps, so
+//   the CTAs of a slice stream the same number of bytes, each stages the
+//   activations of one slice only, and a (row tile, slice) piece spans at
+//   most two CTAs.  The 8 warps split the CTA's units into contiguous ranges.
 //   Weights.  Each warp streams its units with cp.async.bulk into its own
 //   ring of shared-memory slots (up to 8 tiles per copy, completing on the
 //   slot's mbarrier), running ahead across slices.  A TL2P v2 tile is in
@@ -189,7 +189,9 @@ struct GroupArgs {
     int NS;         // slices
     int K;
     int U;          // units = R * KB
-    int Lc;         // units per CTA (the last CTAs may get fewer)
+    int Pps;        // CTAs per slice: CTA c works in slice c / Pps only
+    int Lc;         // units per CTA in a full slice (the slice's last CTAs may get fewer)
+    int LcL;        // units per CTA in the last slice
     int rows;       // accumulator rows per CTA
     FastDiv dKW, dKWL;
     const void *X;  // bf16 [N][K] (mode A) or int8 [N][K] (mode B)
@@ -234,11 +236,13 @@ __device__ __forceinline__ void row_span(const Slice &p, int r, int &lo, int &hi
     hi = r == p.r_last ? p.hi_last : p.kw;
 }
 
-// Whether the (row tile r, slice sigma) piece is cut by a CTA boundary.
+// Whether the (row tile r, slice sigma) piece is cut by a CTA boundary (the
+// slice's CTAs own consecutive ranges of lc units from the slice's start).
 __device__ __forceinline__ bool piece_split(const GroupArgs &a, int r, int sigma) {
     const int kw = slice_width(a, sigma);
-    const int u0 = sigma * a.R * a.KW + r * kw;
-    return u0 / a.Lc != (u0 + kw - 1) / a.Lc;
+    const int lc = sigma == a.NS - 1 ? a.LcL : a.Lc;
+    const int u0 = r * kw;
+    return u0 / lc != (u0 + kw - 1) / lc;
 }
 
 // Move c to warp w's first unit in slice c.sigma or a later one before
@@ -478,8 +482,19 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int N = a.N;
-    const int cu0 = (int)min((long long)blockIdx.x * a.Lc, (long long)a.U);
-    const int cu1 = min(cu0 + a.Lc, a.U);
+    // this CTA's units: range c_in of its slice (none past the last slice)
+    int cu0 = a.U, cu1 = a.U;
+    {
+        const int sig_c = (int)blockIdx.x / a.Pps, c_in = (int)blockIdx.x - sig_c * a.Pps;
+        if (sig_c < a.NS) {
+            const int su = a.R * slice_width(a, sig_c);
+            const int lc = sig_c == a.NS - 1 ? a.LcL : a.Lc;
+            const int base = sig_c * a.R * a.KW;
+            const int off = (int)min((long long)c_in * lc, (long long)su);
+            cu0 = base + off;
+            cu1 = base + min(off + lc, su);
+        }
+    }
     const int sunits = a.R * a.KW;
     const int sig0 = cu0 / sunits;
     const int sig1 = cu1 > cu0 ? (cu1 - 1) / sunits + 1 : sig0;
@@ -1080,7 +1095,7 @@ tl_status device_info(DeviceInfo **out) {
 }
 
 struct Plan {
-    int R, KB, KW, KWL, NS, P, Lc, rows;
+    int R, KB, KW, KWL, NS, P, Pps, Lc, LcL, rows;
     long long U;
     size_t smem;       // dynamic shared memory for the given N
     size_t cnt_bytes;  // arrival counters (front of the workspace, after the status word)
@@ -1112,32 +1127,30 @@ tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     p->KB = (int)ceil_div(K, 128);
     p->U = (long long)p->R * p->KB;
     if (p->U >= (1ll << 30)) return TL_ERR_SHAPE;
-    // Slices: as wide as kMaxSlice allows, but narrow enough that every CTA
-    // slot gets a range of at least KW - 1 units (a piece then spans <= 2 CTAs).
-    const long long slots = (long long)sms * kGridPerSm;   // CTAs per launch
-    long long kwt = std::min<long long>(kMaxSlice, p->U / slots + 1);
-    kwt = std::max<long long>(1, std::min<long long>(kwt, p->KB));
-    const int ns0 = (int)ceil_div(p->KB, kwt);
-    p->KW = (int)ceil_div(p->KB, ns0);
+    // Slices: as few as kMaxSlice allows.  Each slice has its own Pps CTAs,
+    // so no CTA crosses a slice boundary; each CTA gets at least KW - 1
+    // units (a (row tile, slice) piece then spans at most two CTAs) and at
+    // most kMaxCtaRows - 2 row tiles' worth.
+    const long long slots = (long long)sms * kGridPerSm;   // CTA slots on the GPU
+    p->NS = (int)ceil_div(p->KB, kMaxSlice);
+    p->KW = (int)ceil_div(p->KB, p->NS);
     p->NS = (int)ceil_div(p->KB, p->KW);
-    const int kwmin = p->KB - (p->NS - 1) * p->KW;   // the last slice's width
-    p->KWL = kwmin;
-    long long P = slots;
-    if (p->KW > 1) P = std::min<long long>(P, std::max<long long>(1, p->U / (p->KW - 1)));
-    else P = std::min<long long>(P, p->U);
-    P = std::max<long long>(1, P);
-    auto rows_for = [&](long long Lc) { return ceil_div(Lc + kwmin - 1, kwmin) + 1; };
-    long long Lc = ceil_div(p->U, P);
-    if (rows_for(Lc) > kMaxCtaRows) {
-        // very tall, short-K groups: more CTAs than slots, each within kMaxCtaRows rows
-        P = ceil_div(p->U, (long long)(kMaxCtaRows - 2) * kwmin);
-        Lc = ceil_div(p->U, P);
-        if (p->KW > 1 && Lc < p->KW - 1) return TL_ERR_SHAPE;
-    }
-    if (P > (1ll << 31) - 1) return TL_ERR_SHAPE;
-    p->P = (int)P;
+    p->KWL = p->KB - (p->NS - 1) * p->KW;             // the last slice's width
+    const long long su = (long long)p->R * p->KW, suL = (long long)p->R * p->KWL;
+    long long pps = std::max<long long>(1, slots / p->NS);    // no CTA beyond the slots
+    pps = std::min<long long>(pps, p->KW > 1 ? std::max<long long>(1, su / (p->KW - 1)) : su);
+    pps = std::max<long long>(pps, ceil_div(p->R, kMaxCtaRows - 2));
+    pps = std::max<long long>(1, pps);
+    const long long Lc = ceil_div(su, pps), LcL = ceil_div(suL, pps);
+    if ((p->KW > 1 && Lc < p->KW - 1) || (p->KWL > 1 && LcL < p->KWL - 1)) return TL_ERR_SHAPE;
+    auto rows_for = [](long long L, long long kw) { return ceil_div(L + kw - 1, kw) + 1; };
+    const long long rows = std::max(rows_for(Lc, p->KW), rows_for(LcL, p->KWL));
+    if ((long long)p->NS * pps > (1ll << 31) - 1) return TL_ERR_SHAPE;
+    p->Pps = (int)pps;
+    p->P = (int)(p->NS * pps);
     p->Lc = (int)Lc;
-    p->rows = (int)std::min<long long>(rows_for(Lc), p->R);
+    p->LcL = (int)LcL;
+    p->rows = (int)std::min<long long>(rows, p->R);
     if (p->rows > kMaxCtaRows) return TL_ERR_SHAPE;
     const int nt = padded_tokens(std::min(std::max(N, 1), kNMax));
     const int n = std::min(std::max(N, 1), kNMax);
@@ -1204,7 +1217,7 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     if (pst != TL_OK) return pst;
     if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
     a.R = p.R; a.KB = p.KB; a.KW = p.KW; a.KWL = p.KWL; a.NS = p.NS; a.K = K; a.U = (int)p.U;
-    a.Lc = p.Lc; a.rows = p.rows;
+    a.Pps = p.Pps; a.Lc = p.Lc; a.LcL = p.LcL; a.rows = p.rows;
     a.dKW = make_fastdiv((uint32_t)p.KW);
     a.dKWL = make_fastdiv((uint32_t)p.KWL);
     const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
