@@ -167,8 +167,8 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
                           unsigned flags, void *stream);
 
 /* Size of the library's fixed scratch array for tl_linear_noalloc (4 MiB):
- * enough for every Qwen3-8B-shaped matrix at up to 8 tokens per chunk, and
- * for any matrix of up to 65,024 rows. */
+ * enough for every 8B-shaped matrix at up to 8 tokens per chunk, and for
+ * matrices of up to 32,496 rows at K <= 4096 (10,912 rows at K = 12288). */
 #define TL_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* DEVICE.  tl_linear for callers that cannot allocate device memory.
