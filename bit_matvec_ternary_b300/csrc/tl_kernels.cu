@@ -66,9 +66,10 @@ constexpr int kCtasPerSm = 2;         // resident CTAs per SM (registers and sha
 constexpr int kGridPerSm = 2;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 2;             // bulk copies in flight per warp
-// Tiles (512 B each) per bulk copy, smaller as the staged activations grow
-// (two CTAs must fit in one SM's shared memory).
-__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 2 ? 8 : nt == 4 ? 4 : 2; }
+// Tiles (512 B each) per bulk copy: 8, or 4 at eight tokens, where the
+// staged activations take 64 KB (two CTAs still fit in one SM's shared
+// memory for plans of up to 8 row tiles per CTA).
+__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 4 ? 8 : 4; }
 __host__ __device__ constexpr int ring_bytes(int nt) { return kWarps * kSlots * chunk_tiles(nt) * 512; }
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
