@@ -428,6 +428,59 @@ __device__ __forceinline__ void store_rotated(uint32_t *dst, const uint32_t (&w)
     dst[4 * ((q + 3) & 3)] = b3;
 }
 
+// One staging group: activation group o (8 bf16 in mode A, 16 int8 in mode
+// B, as one 16-byte word x) of token n in a block whose staged words start
+// at blk.  Writes the group's words in B-fragment order, times 2^kT, and
+// returns the group's sum in a fixed order and (mode A) the mask of halves
+// outside the fixed window.  A zero x writes zeros.
+template <bool kModeA, int NT>
+__device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const uint4 &x,
+                                            float &sum, uint32_t &bad) {
+    const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+    sum = 0.f;
+    bad = 0u;
+    if (kModeA) {
+        const int m = o >> 1, qd = m >> 1;
+        uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1) + (o & 1);
+        uint32_t st[4];
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+            const uint32_t v = wd[tt];
+            sum = __fadd_rn(__fadd_rn(sum, __uint_as_float(v << 16)),
+                            __uint_as_float(v & 0xFFFF0000u));
+            // per half: nonzero, and exponent outside [kWinLo, kWinHi]
+            const uint32_t nz = __vcmpne2(v & 0x7FFF7FFFu, 0u);
+            const uint32_t off = __vsub2(v & 0x7F807F80u, (uint32_t)kWinLo * 0x00800080u);
+            bad |= __vcmpgtu2(off, (uint32_t)(kWinHi - kWinLo) * 0x00800080u) & nz;
+            st[tt] = v + ((uint32_t)kT * 0x00800080u & nz);
+        }
+        // store word tt = (it + qd) % 4 at step it: the lanes of one block
+        // quarter apart then write different banks
+        store_rotated(dst, st, qd);
+    } else {
+        const int m = o, qd = m >> 1;
+        uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1);
+        const float two_t = __int_as_float((kT + 127) << 23);
+        int isum = 0;
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+            uint32_t st[4];
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                const uint32_t word = wd[2 * h8 + (tt >> 1)] >> (16 * (tt & 1));
+                const int qlo = (int)(int8_t)(word & 0xFFu);
+                const int qhi = (int)(int8_t)((word >> 8) & 0xFFu);
+                isum += qlo + qhi;
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn((float)qlo, two_t),
+                                                                __fmul_rn((float)qhi, two_t));
+                st[tt] = *reinterpret_cast<const uint32_t *>(&b2);
+            }
+            store_rotated(dst + h8, st, qd);
+        }
+        sum = (float)isum;
+    }
+}
+
 // The activation groups of one slice: VPL activations per group, LB groups
 // per 128-column block, N * kw * LB groups in all, taken SB * kThreads at a
 // time starting at `base`.
@@ -465,6 +518,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     constexpr int VPL = kModeA ? 8 : 16;        // activations per staging group
     constexpr int LB = 128 / VPL;               // staging groups per block
     constexpr int SB = stage_batch(NT, kModeA); // staging loads in flight per thread
+    constexpr bool kAsyncX = NT >= 4;           // stage X with cp.async (when X allows 16-byte copies)
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;                                                // [kWarps][kSlots][SLOT]
     uint4 *xs = reinterpret_cast<uint4 *>(smem + ring_bytes(NT));      // one slice of X
@@ -500,6 +554,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     const int sig0 = cu0 / sunits;
     const int sig1 = cu1 > cu0 ? (cu1 - 1) / sunits + 1 : sig0;
     uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
+    const uint32_t xs_s = smem_u32(xs);
 
     // The dependent launch may be scheduled at once; it only streams weights
     // until this grid has finished.
@@ -610,7 +665,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     // Now the activations, written by the previous kernel.
     griddep_wait();
     uint4 xv[SB];
-    stage_load<kModeA, SB>(a, P, 0, xv);
+    if (!(kAsyncX && a.xvec)) stage_load<kModeA, SB>(a, P, 0, xv);
 
     Cursor cc;
     cc.sigma = sig0;
@@ -633,6 +688,54 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         {
             const int total = N * P.kw * LB;
             const FastDiv dv = sigma == a.NS - 1 ? a.dKWL : a.dKW;
+            if (kAsyncX && a.xvec) {
+                // Four or more tokens: every 16 bytes of the slice's rows are
+                // copied at once (cp.async, zero past K) into their block's own
+                // region, row n at byte n * RB; then each warp rewrites its
+                // blocks in place, group by group as below.
+                constexpr int EB = kModeA ? 2 : 1;
+                constexpr int RB = 128 * EB;               // bytes of one token's block row
+                constexpr int CPR = RB / 16;                // 16-byte copies per block row
+                const int nch = N * P.kw * CPR;
+                for (int i = threadIdx.x; i < nch; i += kThreads) {
+                    const int c = i % CPR, q = i / CPR;     // q = n * kw + jb
+                    const int n = fdiv(q, dv), jb = q - n * P.kw;
+                    const int k0 = (P.kb0 + jb) * 128 + c * (16 / EB);
+                    const uint32_t full = k0 < a.K ? 16u : 0u;
+                    const char *src = reinterpret_cast<const char *>(a.X) +
+                                      ((long long)n * a.K + (full ? k0 : 0)) * EB;
+                    const uint32_t dst = xs_s + (uint32_t)(jb * (NT * 256) + n * RB + c * 16);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                                 "r"(full)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+                __syncthreads();
+                constexpr int J = NT * LB / 32 > 0 ? NT * LB / 32 : 1;   // groups per lane in one block
+                for (int jb = warp; jb < P.kw; jb += kWarps) {
+                    uint32_t *blk = xw + jb * NT * 64;
+                    uint4 v[J];
+#pragma unroll
+                    for (int j = 0; j < J; ++j) {
+                        const int g = lane + 32 * j, n = g / LB, o = g % LB;
+                        v[j] = n < N ? *reinterpret_cast<const uint4 *>(blk + n * (RB / 4) + o * 4)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < J; ++j) {
+                        const int g = lane + 32 * j, n = g / LB, o = g % LB;
+                        float sum;
+                        uint32_t bad;
+                        stage_group<kModeA, NT>(blk, n, o, v[j], sum, bad);
+#pragma unroll
+                        for (int off = LB / 2; off > 0; off >>= 1)
+                            sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
+                        if (n < N && o == 0) osum[jb][n] = sum;
+                        if (kModeA && n < N && bad) atomicOr(&redo, 1 << n);
+                    }
+                }
+            } else
             for (int base = 0; base < total; base += kThreads * SB) {
                 if (sigma != sig0 || base != 0) stage_load<kModeA, SB>(a, P, base, xv);
 #pragma unroll
@@ -644,49 +747,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                     const int n = valid ? fdiv(q, dv) : 0, jb = q - n * P.kw;
                     float sum = 0.f;
                     uint32_t bad = 0u;
-                    if (valid) {
-                        const uint32_t wd[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-                        if (kModeA) {
-                            const int m = o >> 1, qd = m >> 1;
-                            uint32_t *dst = xw + ((jb * 4 + qd) * NT + n) * 16 + 2 * (m & 1) + (o & 1);
-                            uint32_t st[4];
-#pragma unroll
-                            for (int tt = 0; tt < 4; ++tt) {
-                                const uint32_t v = wd[tt];
-                                sum = __fadd_rn(__fadd_rn(sum, __uint_as_float(v << 16)),
-                                                __uint_as_float(v & 0xFFFF0000u));
-                                // per half: nonzero, and exponent outside [kWinLo, kWinHi]
-                                const uint32_t nz = __vcmpne2(v & 0x7FFF7FFFu, 0u);
-                                const uint32_t off = __vsub2(v & 0x7F807F80u, (uint32_t)kWinLo * 0x00800080u);
-                                bad |= __vcmpgtu2(off, (uint32_t)(kWinHi - kWinLo) * 0x00800080u) & nz;
-                                st[tt] = v + ((uint32_t)kT * 0x00800080u & nz);
-                            }
-                            // store word tt = (it + qd) % 4 at step it: the lanes of one
-                            // block quarter apart then write different banks
-                            store_rotated(dst, st, qd);
-                        } else {
-                            const int m = o, qd = m >> 1;
-                            uint32_t *dst = xw + ((jb * 4 + qd) * NT + n) * 16 + 2 * (m & 1);
-                            const float two_t = __int_as_float((kT + 127) << 23);
-                            int isum = 0;
-#pragma unroll
-                            for (int h8 = 0; h8 < 2; ++h8) {
-                                uint32_t st[4];
-#pragma unroll
-                                for (int tt = 0; tt < 4; ++tt) {
-                                    const uint32_t word = wd[2 * h8 + (tt >> 1)] >> (16 * (tt & 1));
-                                    const int qlo = (int)(int8_t)(word & 0xFFu);
-                                    const int qhi = (int)(int8_t)((word >> 8) & 0xFFu);
-                                    isum += qlo + qhi;
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                        __fmul_rn((float)qlo, two_t), __fmul_rn((float)qhi, two_t));
-                                    st[tt] = *reinterpret_cast<const uint32_t *>(&b2);
-                                }
-                                store_rotated(dst + h8, st, qd);
-                            }
-                            sum = (float)isum;
-                        }
-                    }
+                    if (valid) stage_group<kModeA, NT>(xw + jb * NT * 64, n, o, xv[i], sum, bad);
 #pragma unroll
                     for (int off = LB / 2; off > 0; off >>= 1)
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
