@@ -1358,6 +1358,27 @@ size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N) {
     return workspace_bytes_for(Ws, G, N, sms);
 }
 
+tl_status tl_decode_plan(const tl_weight *Ws, int G, int N, int sms, int32_t *plan) {
+    if (!Ws || !plan) return TL_ERR_NULL;
+    if (G < 1 || G > TL_MAX_GROUP || N < 1 || sms < 1) return TL_ERR_SHAPE;
+    int Ms[TL_MAX_GROUP];
+    for (int g = 0; g < G; ++g) {
+        if (Ws[g].M < 1 || Ws[g].K < 1 || Ws[g].M > TL_MAX_M || Ws[g].K > TL_MAX_K ||
+            Ws[g].K != Ws[0].K)
+            return TL_ERR_SHAPE;
+        Ms[g] = Ws[g].M;
+    }
+    const int n = std::min(N, kNMax);
+    Plan p;
+    const tl_status st = make_plan(Ms, G, Ws[0].K, n, sms, &p);
+    if (st != TL_OK) return st;
+    const int32_t v[TL_PLAN_FIELDS] = {p.R,  p.KB, p.NS,   p.KW,   p.KWL,
+                                       p.Pps, p.P, p.Lc,   p.LcL,  p.rows,
+                                       kWarps, chunk_tiles(padded_tokens(n)), kGridPerSm, kMaxCtaRows};
+    for (int i = 0; i < TL_PLAN_FIELDS; ++i) plan[i] = v[i];
+    return TL_OK;
+}
+
 tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, float *s, int32_t *z,
                           int symmetric, void *stream) {
     if (!X_bf16 || !Q || !s || !z) return TL_ERR_NULL;

@@ -34,8 +34,8 @@ TL_MAX_GROUP = 4
 
 # Every symbol include/tl.h declares.
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
-           "tl_quantize_act", "tl_linear", "tl_linear_group", "tl_linear_noalloc",
-           "tl_status_string", "tl_version")
+           "tl_decode_plan", "tl_quantize_act", "tl_linear", "tl_linear_group",
+           "tl_linear_noalloc", "tl_status_string", "tl_version")
 TL_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -53,6 +53,8 @@ _lib.tl_validate_packed.argtypes = [_p, _i64, _i64, C.POINTER(C.c_int64)]
 _lib.tl_validate_packed.restype = _int
 _lib.tl_workspace_bytes.argtypes = [C.POINTER(tl_weight), _int, _int]
 _lib.tl_workspace_bytes.restype = _sz
+_lib.tl_decode_plan.argtypes = [C.POINTER(tl_weight), _int, _int, _int, C.POINTER(C.c_int32)]
+_lib.tl_decode_plan.restype = _int
 _lib.tl_quantize_act.argtypes = [_p, _int, _int, _p, _p, _p, _int, _p]
 _lib.tl_quantize_act.restype = _int
 _lib.tl_linear.argtypes = [C.POINTER(tl_weight), _p, _p, _p, _p, _int, _int, _int, _p, _sz,
@@ -176,6 +178,18 @@ def _structs(ws):
 def tl_workspace_bytes(weights, N: int) -> int:
     ws = weights if isinstance(weights, (list, tuple)) else [weights]
     return int(_lib.tl_workspace_bytes(_structs(ws), len(ws), N))
+
+
+PLAN_FIELDS = ("R", "KB", "NS", "KW", "KWL", "Pps", "P", "Lc", "LcL", "rows",
+               "warps", "chunk_tiles", "ctas_per_sm", "max_cta_rows")
+
+
+def decode_plan(weights, N: int, sms: int) -> dict:
+    """The decode kernel's work split for these shapes (host only)."""
+    ws = weights if isinstance(weights, (list, tuple)) else [weights]
+    out = (C.c_int32 * len(PLAN_FIELDS))()
+    _check(_lib.tl_decode_plan(_structs(ws), len(ws), N, sms, out), "tl_decode_plan")
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def make_workspace(weights_lists, N: int, device="cuda"):

@@ -130,6 +130,20 @@ TL_API tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K
  * any shapes, on one stream; calls that overlap on the GPU must not share it. */
 TL_API size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N);
 
+/* HOST.  The work split that tl_linear / tl_linear_group use for these
+ * shapes at batch N (N <= 8 per launch) on a GPU with `sms` SMs; runs no GPU
+ * code and needs no GPU.  It exists so that tests and tuning can check the
+ * split against the kernel's invariants; the pages describe no such call.
+ * plan[TL_PLAN_FIELDS] receives, in order: row tiles R, 128-column blocks KB,
+ * K slices NS, slice width KW, last slice width KWL, CTAs per slice Pps,
+ * CTAs P = NS * Pps, units per CTA Lc (last slice LcL), row tiles a CTA may
+ * touch, warps per CTA, tiles per weight copy at this N, CTA slots per SM,
+ * and the row-tile limit per CTA.  Unit u of slice s (u = r * kw + b for row
+ * tile r, block b) belongs to CTA s * Pps + u / Lc (LcL in the last slice).
+ * Returns TL_ERR_NULL, TL_ERR_SHAPE or TL_OK. */
+#define TL_PLAN_FIELDS 14
+TL_API tl_status tl_decode_plan(const tl_weight *Ws, int G, int N, int sms, int32_t *plan);
+
 /* DEVICE.  Per-token activation quantisation (bf16 -> int8).  X_bf16 [N][K]
  * (2-byte aligned), Q [N][K] int8, s [N] fp32, z [N] int32.
  *   symmetric == 0: lo = min(0, min x), hi = max(0, max x),
