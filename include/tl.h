@@ -127,7 +127,13 @@ TL_API tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K
  * be zero-filled before its first use and 256-byte aligned; every call leaves
  * its front bytes zero again when it completes.  One workspace of the largest
  * size asked for by a set of calls may serve any sequence of those calls, of
- * any shapes, on one stream; calls that overlap on the GPU must not share it. */
+ * any shapes, on one stream; calls that overlap on the GPU must not share it.
+ * Device-side errors: the kernels cannot return a status, so a bounded wait
+ * that gives up (about a second) writes a non-zero value into the
+ * workspace's first int32 (the status word), and the call's outputs are then
+ * invalid.  Read that word after the stream has passed the call; if it is
+ * non-zero, treat the call as having failed with TL_ERR_TIMEOUT and zero-fill
+ * the whole workspace before using it again. */
 TL_API size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N);
 
 /* HOST.  The work split that tl_linear / tl_linear_group use for these
