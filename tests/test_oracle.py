@@ -209,6 +209,79 @@ def test_quant_degenerate_zero_token(oracle_mod):
     assert np.all(Q == 0) and np.all(s == 1.0) and np.all(z == 0)
 
 
+def test_quant_ties_round_to_even(oracle_mod):
+    """Hand-derived: with x/s landing exactly on k + 1/2, q rounds to even.
+
+    Asymmetric: a token whose largest value is 255 and smallest is 0 has
+    lo = 0, hi = 255, s = 255/255 = 1 exactly and z = -128 - rint(0) = -128,
+    so q = rint(x) - 128: 2.5 -> 2 - 128, 0.5 -> 0 - 128, 1.5 -> 2 - 128,
+    -> never 3 - 128 or 1 - 128 as rounding half away from zero would give.
+    Symmetric: max|x| = 127 gives s = 127/127 = 1, q = rint(x) with no
+    offset: 2.5 -> 2, -2.5 -> -2, 0.5 -> 0, -0.5 -> 0, 1.5 -> 2, -1.5 -> -2.
+    (Reading: the pages are silent on activation rounding; ties go to even,
+    as for every other rounding in the library.)"""
+    K = 64
+    x = np.zeros((1, K), dtype=np.float32)
+    x[0, :6] = [255.0, 2.5, 0.5, 1.5, 3.5, 4.5]
+    Q, s, z = oracle_mod.quant(synth.to_bf16_bits(x))
+    assert float(s[0]) == 1.0 and int(z[0]) == -128
+    assert list(Q[0, :6]) == [127, 2 - 128, 0 - 128, 2 - 128, 4 - 128, 4 - 128]
+    assert np.all(Q[0, 6:] == -128)
+
+    xs = np.zeros((1, K), dtype=np.float32)
+    xs[0, :7] = [127.0, 2.5, -2.5, 0.5, -0.5, 1.5, -1.5]
+    Q, s, z = oracle_mod.quant(synth.to_bf16_bits(xs), symmetric=True)
+    assert float(s[0]) == 1.0 and int(z[0]) == 0
+    assert list(Q[0, :7]) == [127, 2, -2, 0, 0, 2, -2]
+
+
+def test_quant_range_includes_zero(oracle_mod):
+    """Hand-derived closed forms for one-signed tokens (the range is widened
+    to include 0, so zero stays exactly representable).
+
+    All positive (min x > 0): lo = 0, so z = -128 exactly, s = fl(max/255)
+    and the largest value maps to rint(max/s) - 128 = 255 - 128 = 127.
+    All negative (max x < 0): hi = 0, s = fl(-min/255), z = -128 - rint(min/s)
+    = -128 + 255 = 127, and the smallest value maps to -255 + 127 = -128."""
+    rng = np.random.default_rng(5)
+    K = 300
+    for _ in range(4):
+        pos = rng.uniform(0.25, 4.0, size=(1, K)).astype(np.float32)
+        bits = synth.to_bf16_bits(pos)
+        vals = synth.bf16_bits_to_f32(bits)
+        Q, s, z = oracle_mod.quant(bits)
+        vmax = np.float32(vals.max())
+        assert int(z[0]) == -128
+        assert float(s[0]) == float(np.float32(vmax / np.float32(255.0)))
+        assert Q[0, int(np.argmax(vals))] == 127
+        assert Q.min() > -128          # nothing maps below the zero point's code
+
+        bits_n = synth.to_bf16_bits(-pos)
+        vals_n = synth.bf16_bits_to_f32(bits_n)
+        Q, s, z = oracle_mod.quant(bits_n)
+        vmin = np.float32(vals_n.min())
+        assert int(z[0]) == 127
+        assert float(s[0]) == float(np.float32(np.float32(0.0 - vmin) / np.float32(255.0)))
+        assert Q[0, int(np.argmin(vals_n))] == -128
+        assert Q.max() < 127
+
+
+def test_threaded_oracle_equals_single_thread(oracle_mod):
+    """The host-core timing drivers compute exactly the single-thread rows."""
+    M, K = 77, 1000
+    W, scale = _rand_case(M, K, seed=44)
+    P = oracle_mod.pack(W)
+    rs = oracle_mod.rowsum(P, M, K)
+    X = _x(3, K, seed=45, outlier_frac=0.01)
+    ya = oracle_mod.linear_a(P, scale, M, K, X)
+    for nt in (1, 3, 8):
+        assert np.array_equal(oracle_mod.linear_a_mt(P, scale, M, K, X, nthreads=nt), ya)
+    Q, s, z = oracle_mod.quant(X)
+    _, yb = oracle_mod.linear_b(P, scale, rs, M, K, Q, s, z)
+    for nt in (1, 3, 8):
+        assert np.array_equal(oracle_mod.linear_b_mt(P, scale, rs, M, K, Q, s, z, nthreads=nt), yb)
+
+
 @pytest.mark.parametrize("symmetric", [False, True])
 def test_quant_properties(oracle_mod, symmetric):
     X = _x(8, 1000, seed=2, outlier_frac=0.01)

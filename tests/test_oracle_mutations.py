@@ -38,6 +38,11 @@ MUTATIONS = {
     "sym_divisor": ("s = (a == 0.0f) ? 1.0f : a / 127.0f;", "s = (a == 0.0f) ? 1.0f : a / 128.0f;"),
     "rowsum_dropped": ("for (int64_t k = 0; k < K; ++k) acc += oracle_weight(P, m, k, Kp, NULL);",
                        "for (int64_t k = 1; k < K; ++k) acc += oracle_weight(P, m, k, Kp, NULL);"),
+    "quant_ties_away_asym": ("float r = rintf(bf16_to_float(x[k]) / s) + (float)z;",
+                             "float r = roundf(bf16_to_float(x[k]) / s) + (float)z;"),
+    "quant_ties_away_sym": ("float r = rintf(bf16_to_float(x[k]) / s);",
+                            "float r = roundf(bf16_to_float(x[k]) / s);"),
+    "quant_range_without_zero": ("float lo = 0.0f, hi = 0.0f;", "float lo = 1e30f, hi = -1e30f;"),
     "int_acc_dropped_term": ("for (int64_t k = 0; k < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];",
                              "for (int64_t k = 0; k + 1 < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];"),
 }
@@ -55,6 +60,8 @@ def _pins():
         ("closed_a", lambda: T.test_linear_a_closed_forms(o)),
         ("quant_onehot", lambda: T.test_quant_one_hot_closed_form(o)),
         ("quant_props", lambda: [T.test_quant_properties(o, s) for s in (False, True)]),
+        ("quant_ties", lambda: T.test_quant_ties_round_to_even(o)),
+        ("quant_range", lambda: T.test_quant_range_includes_zero(o)),
         ("int_sums", lambda: [T.test_linear_b_integer_sums_match_numpy(o, M, K) for M, K in T.SHAPES]),
         ("onehot_b", lambda: T.test_linear_b_one_hot_identity(o)),
         ("b_tracks_a", lambda: [T.test_linear_b_tracks_linear_a_within_quant_error(o, s)
