@@ -6,9 +6,12 @@
 One step is one pass of the whole hot path over one batch: all 252
 projection linears of a 36-layer, Qwen3-8B-shaped decoder (hidden 4096,
 q/o 4096x4096, k/v 1024x4096, gate/up 12288x4096, down 4096x12288), as 144
-launches, on seeded synthetic weights with the pages' code statistics.  The
-headline is N = 1 decode in mode A (bf16 activations, fp32 accumulation);
-the N = 8 speculative-verify batch (modes A and B) is reported beside it.
+dependent launch groups run by one persistent launch (a chain: each group
+waits for the previous one before reading its input), on seeded synthetic
+weights with the pages' code statistics.  The headline is N = 1 decode in
+mode A (bf16 activations, fp32 accumulation); the N = 8 speculative-verify
+batch (modes A and B) is reported beside it, and so is the same pass as a
+CUDA graph of 144 launches.
 
 Prints ONE JSON line (rank 0).  Under torchrun each rank runs an
 independent replica (the path has no exchange step); value is the sum of the
@@ -105,14 +108,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def measured_traffic(alg_per_launch):
+def measured_traffic(alg_per_launch, record="tl_chain_kernel_traffic.txt"):
     """DRAM bytes per launch of the decode kernel: the ncu-measured bytes per
-    algorithmic byte (profiles/tl_mma_kernel_traffic.txt) times this run's
-    average algorithmic bytes per launch; None when the record is missing or
-    the kernel's device code changed since it was captured."""
+    algorithmic byte (profiles/<record>) times this run's algorithmic bytes
+    per launch; None when the record is missing or the kernels' device code
+    changed since it was captured."""
     import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
-    rec = os.path.join(here, "profiles", "tl_mma_kernel_traffic.txt")
+    rec = os.path.join(here, "profiles", record)
     src = os.path.join(here, "bit_matvec_ternary_b300", "csrc", "tl_kernels.cu")
     try:
         kv = {}
@@ -148,17 +151,36 @@ def time_graph(stack, steps, warmup, torch):
     return start.elapsed_time(end) / steps
 
 
+def time_chain(chain, steps, warmup, torch):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        chain.run()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        chain.run()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if chain.status() != 0:
+        raise RuntimeError(f"chain reported device status {chain.status()}")
+    return start.elapsed_time(end) / steps
+
+
 def time_e2e(stack, steps, warmup, torch):
-    """Per step: pinned host -> device copy of all inputs, the graph, and a
-    device -> host read of all outputs, inside the timed region."""
+    """Per step: pinned host -> device copy of all inputs, one pass of the
+    chain, and a device -> host read of all outputs, inside the timed region."""
     stream = torch.cuda.current_stream()
     hx = torch.empty(stack.X_flat.shape, dtype=stack.X_flat.dtype, pin_memory=True)
     hx.copy_(stack.X_flat.cpu())
     hy = torch.empty(stack.Y_flat.shape, dtype=stack.Y_flat.dtype, pin_memory=True)
 
+    chain = stack.chain()
+
     def step():
         stack.X_flat.copy_(hx, non_blocking=True)
-        stack.graph.replay()
+        chain.run()
         hy.copy_(stack.Y_flat, non_blocking=True)
 
     for _ in range(warmup):
@@ -294,12 +316,12 @@ def main():
     t_gen = time.perf_counter() - t_gen
     stack = LinearStack(shape, N=1, mode=tl.TL_MODE_BF16, out_dtype=tl.TL_OUT_F32,
                         weights=weights)
-    stack.capture()
+    chain = stack.chain()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ms = time_graph(stack, args.steps, args.warmup, torch)
+        ms = time_chain(chain, args.steps, args.warmup, torch)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -311,13 +333,20 @@ def main():
     tok_s = world * 1.0 / (ms_max / 1e3)
     alg = stack.algorithmic_bytes()
     gbs = alg / (ms_max / 1e3) / 1e9
-    launches = stack.launches_per_step
+    launches = 1
 
     ms_e2e, h2d, d2h = time_e2e(stack, args.steps, args.warmup, torch)
     e2e = {"value": world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "how": "per step: one pinned H2D copy of all 144 inputs, one replay of the graph "
-                  "of C-ABI launches, one D2H copy of all 252 outputs"}
+           "how": "per step: one pinned H2D copy of all 144 inputs, one tl_chain_run "
+                  "(C ABI), one D2H copy of all 252 outputs"}
+    # the same pass as a graph of 144 dependent launches (programmatic
+    # dependent launch between them), for comparison
+    stack.capture()
+    ms_graph = time_graph(stack, args.steps, args.warmup, torch)
+    per_launch = {"ms_per_step": ms_graph, "tokens_s": 1.0 / (ms_graph / 1e3),
+                  "launches_per_step": stack.launches_per_step,
+                  "frac_of_hbm": alg / (ms_graph / 1e3) / 1e9 / hbm_peak}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -333,13 +362,15 @@ def main():
         for mode, name, outl in ((tl.TL_MODE_BF16, "n8_mode_a", 0.01), (tl.TL_MODE_I8, "n8_mode_b", 0.01)):
             st8 = LinearStack(shape, N=8, mode=mode, out_dtype=tl.TL_OUT_F32, outlier_frac=outl,
                               weights=weights)
-            st8.capture()
-            ms8 = time_graph(st8, args.steps, args.warmup, torch)
+            ms8 = time_chain(st8.chain(), args.steps, args.warmup, torch)
             a8 = st8.algorithmic_bytes()
             extra[name] = {"tokens_s": 8 / (ms8 / 1e3), "ms_per_step": ms8,
                            "algorithmic_bytes": a8, "gbs": a8 / (ms8 / 1e3) / 1e9,
                            "frac_of_hbm": a8 / (ms8 / 1e3) / 1e9 / hbm_peak,
-                           "launches_per_step": st8.launches_per_step}
+                           "launches_per_step": 1,
+                           "how": "one tl_chain_run per step" + (
+                               " (each group's activations quantised inside the chain)"
+                               if mode == tl.TL_MODE_I8 else "")}
             del st8
             torch.cuda.empty_cache()
 
@@ -378,12 +409,13 @@ def main():
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "traffic": measured_traffic(alg / launches),
                          "traffic_note": "bytes per launch: ncu DRAM bytes per algorithmic byte "
-                                         "of one gate+up launch, times this step's mean "
-                                         "algorithmic bytes per launch",
-                         "kernel": "tl_mma_kernel",
+                                         "of one chain launch over two 8B-shaped layers, times "
+                                         "this step's algorithmic bytes",
+                         "kernel": "tl_chain_kernel",
                          "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
                          "algorithmic_bytes_per_step": alg, "launches_per_step": launches,
                          "avg_launch_us": ms_max * 1e3 / launches},
+            "launch_per_linear": per_launch,
             "e2e": e2e,
             "gpu_launches": launches * args.steps,
             "clocks": clocks,

@@ -3,8 +3,9 @@
     python -m bit_matvec_ternary_b300.cases --case gate_up --n 1 --mode a --reps 3
 
 Cases are the launch groups of one 8B-shaped decoder layer: qkv (q/k/v
-grouped, K = 4096), o, gate_up (gate/up grouped), down (K = 12288), and quant
-(the activation quantiser, K = 12288).  Each is built from the same seeded
+grouped, K = 4096), o, gate_up (gate/up grouped), down (K = 12288), quant
+(the activation quantiser, K = 12288), and chain (the first `--layers`
+layers of the 8B stack as one persistent chain launch).  Each is built from the same seeded
 synthetic inputs as the benchmark and launched `reps` times back to back
 after `warmup` launches, then the process checks nothing and exits 0.
 """
@@ -22,12 +23,13 @@ CASE_GROUPS = {"qkv": 0, "o": 1, "gate_up": 2, "down": 3}
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant"])
+    ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant", "chain"])
     ap.add_argument("--n", type=int, default=1)
     ap.add_argument("--mode", default="a", choices=["a", "b"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--layer", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=2)
     args = ap.parse_args()
 
     import torch
@@ -38,6 +40,16 @@ def main() -> None:
     shape = synth.NEUTRINO_8B
     shp = shape.linear_shapes()
     mode = tl.TL_MODE_BF16 if args.mode == "a" else tl.TL_MODE_I8
+    if args.case == "chain":
+        from .stack import LinearStack
+        st = LinearStack(shape, N=args.n, mode=mode, layers=args.layers)
+        chain = st.chain()
+        for _ in range(args.warmup + args.reps):
+            chain.run()
+        torch.cuda.synchronize()
+        if chain.status() != 0:
+            raise SystemExit(f"chain status {chain.status()}")
+        return
     if args.case == "quant":
         K = shp["down"][1]
         x = synth.activations(args.n, K, seed=1)

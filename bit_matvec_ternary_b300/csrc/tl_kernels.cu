@@ -29,12 +29,15 @@
 //   a bf16x2 pair whose halves are (1 - w) * 2^(2q - 133), q = m%4 -- bf16
 //   subnormals (or, for field 10 at q == 3, the smallest normal), exactly
 //   linear in the field.  One AND per two weights, plus one shift per word.
-//   Activations.  Staged per slice in shared memory in B-fragment order,
-//   multiplied by 2^67 (an exponent add, exact), so a class-q product is
-//   (1 - w) * x * 2^(2q - 66), exact in fp32; the tensor cores form the sums,
-//   one accumulator chain per class, and each chain is rescaled exactly when
-//   a run of tiles is folded.  The staging also sums x per 128-column block,
-//   and a row's result is (sum of x over its blocks) - sum (1 - w) x.
+//   Activations.  Staged per slice in shared memory in B-fragment order; the
+//   k-steps of class q = m % 4 are multiplied by 2^(67 - 2q) (an exponent
+//   add, exact), so every product is (1 - w) * x * 2^-66, exact in fp32.
+//   The staging also sums x over each half block (64 columns).  A tile's
+//   k-steps 0..3 and 4..7 go to two accumulator chains, alternating, and the
+//   next tile to two others; before its MMAs each chain is given minus its
+//   half block's sum, so a chain holds -sum w x (scaled) and its rounding
+//   tracks the result rather than sum x, whatever the mean of x.  The chains
+//   are folded, with exact power-of-two factors, when a run of tiles ends.
 //   Activations outside [2^-60, 2^61) in magnitude (mode A only) switch that
 //   token's slice to a scale chosen from its largest exponent.  Columns
 //   n >= N are zero and their results are discarded, so no lane is
@@ -56,7 +59,9 @@
 
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 namespace {
 
@@ -174,8 +179,15 @@ struct Cursor {
     int sigma, u, uend, r, b, kw, kb0;
 };
 
+// Kinds of step in a chain of launches run by one persistent kernel.
+constexpr int kStepLinear = 0;   // a (grouped) ternary linear
+constexpr int kStepQuant = 1;    // per-token activation quantisation (mode B chains)
+
 // Everything below reads these launch constants.
 struct GroupArgs {
+    int kind;       // kStepLinear or kStepQuant
+    int P;          // CTAs that take part (the plan's; chunks x tokens for a quantiser step)
+    int kwr, rowsr; // shared-memory regions: slice width and row tiles they are sized for
     const char *packed[TL_MAX_GROUP];
     const float *scale[TL_MAX_GROUP];
     const int32_t *rowsum[TL_MAX_GROUP];
@@ -206,6 +218,20 @@ struct GroupArgs {
     unsigned long long *cnt;  // [R] blocks arrived (NS > 1); zero between launches
     unsigned long long *xslot;  // [R][N][16] exchange slots (NS == 1); zero between launches
     int *status;    // workspace status word
+    // quantiser steps: X (bf16) -> qout (int8), sout, zout; symmetric if sym
+    int8_t *qout;
+    float *sout;
+    int32_t *zout;
+    int sym;
+};
+
+// Header of an encoded chain (device memory), followed by its steps.
+struct ChainHeader {
+    unsigned *cnt;          // [nsteps] CTAs done per step; zero between launches
+    const unsigned *gate;   // when not null, step 0 waits until *gate != 0
+    long long wait_limit;   // SM cycles before a wait for a step's inputs gives up
+    int nsteps;
+    int lookahead;          // steps whose weights are prefetched into L2 ahead of use
 };
 
 __device__ __forceinline__ int slice_width(const GroupArgs &a, int sigma) {
@@ -358,48 +384,100 @@ __device__ __forceinline__ void exchange_row_tile(const GroupArgs &a, int r, con
 }
 
 // One 128-column block of one 16-row tile: 8 MMAs (k-steps m = 0..7) over
-// the lane's 16-byte slice of the tile (w) and the 4 B-fragment quarters (b).
-// Register j of k-step m is word j shifted right by 8*(m/4) and masked to the
-// fields at bits 2*(m%4) and 16 + 2*(m%4).
-__device__ __forceinline__ void tile_mma(float (&c)[4][4], const uint4 &w, const uint4 (&b)[4]) {
+// the lane's 16-byte slice of the tile (w) and the 4 B-fragment quarters (b),
+// k-steps 0..3 into chain c0 and 4..7 into c1, alternating so that
+// consecutive MMAs never share an accumulator.  Register j of k-step m is
+// word j shifted right by 8*(m/4) and masked to the fields at bits 2*(m%4)
+// and 16 + 2*(m%4).
+__device__ __forceinline__ void tile_mma(float (&c0)[4], float (&c1)[4], const uint4 &w,
+                                         const uint4 (&b)[4]) {
     const uint32_t hx = w.x >> 8, hy = w.y >> 8, hz = w.z >> 8, hw = w.w >> 8;
-    // four independent accumulator chains; consecutive MMAs never share one
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const uint32_t F = 0x00030003u << (2 * (m & 3));
-        const uint32_t a0 = (m < 4 ? w.x : hx) & F, a1 = (m < 4 ? w.y : hy) & F;
-        const uint32_t a2 = (m < 4 ? w.z : hz) & F, a3 = (m < 4 ? w.w : hw) & F;
-        const uint4 &q = b[m >> 1];
-        mma_bf16_16816(c[m & 3], a0, a1, a2, a3, (m & 1) ? q.z : q.x, (m & 1) ? q.w : q.y);
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t F = 0x00030003u << (2 * p);
+        const uint4 &q0 = b[p >> 1], &q1 = b[2 + (p >> 1)];
+        mma_bf16_16816(c0, w.x & F, w.y & F, w.z & F, w.w & F, (p & 1) ? q0.z : q0.x,
+                       (p & 1) ? q0.w : q0.y);
+        mma_bf16_16816(c1, hx & F, hy & F, hz & F, hw & F, (p & 1) ? q1.z : q1.x,
+                       (p & 1) ? q1.w : q1.y);
     }
+}
+
+// Position of the (block b, token n, half h) correction of a slice: the
+// tokens 2t', 2t'+1 of both halves of a block are four consecutive floats,
+// so lane (g, t) reads its tile's corrections with one 16-byte load (8 bytes
+// at one token).
+template <int NT>
+__device__ __forceinline__ int xh_index(int b, int n, int h) {
+    return NT == 1 ? b * 2 + h : ((b * (NT / 2) + (n >> 1)) * 2 + h) * 2 + (n & 1);
+}
+// One tile on chains c[2 par] (k-steps 0..3) and c[2 par + 1] (k-steps
+// 4..7), each first given its half block's correction (xc: the lane's four
+// floats, half 0 then half 1, tokens 2t', 2t'+1 each; two floats at one
+// token, where only column 0 is kept).  The chains then hold
+// sum (1 - w) x - sum x = -sum w x, scaled, and never grow with sum x.
+template <int NT>
+__device__ __forceinline__ void tile_corrected(float (&c)[4][4], int par, const uint4 &w,
+                                               const uint4 (&b)[4], const float *xc) {
+    float(&c0)[4] = c[2 * par];
+    float(&c1)[4] = c[2 * par + 1];
+    if (NT == 1) {
+        const float2 cr = *reinterpret_cast<const float2 *>(xc);
+        c0[0] = __fadd_rn(c0[0], cr.x);
+        c0[2] = __fadd_rn(c0[2], cr.x);
+        c1[0] = __fadd_rn(c1[0], cr.y);
+        c1[2] = __fadd_rn(c1[2], cr.y);
+    } else {
+        const float4 cr = *reinterpret_cast<const float4 *>(xc);
+        c0[0] = __fadd_rn(c0[0], cr.x);
+        c0[1] = __fadd_rn(c0[1], cr.y);
+        c0[2] = __fadd_rn(c0[2], cr.x);
+        c0[3] = __fadd_rn(c0[3], cr.y);
+        c1[0] = __fadd_rn(c1[0], cr.z);
+        c1[1] = __fadd_rn(c1[1], cr.w);
+        c1[2] = __fadd_rn(c1[2], cr.z);
+        c1[3] = __fadd_rn(c1[3], cr.w);
+    }
+    tile_mma(c0, c1, w, b);
+}
+
+// -sum * 2^(T - 133), in two exact power-of-two factors: the correction, in
+// chain units, for half a block whose activations sum to `sum` and are
+// staged times 2^(T - 2q).
+__device__ __forceinline__ float chain_units(float sum, int T) {
+    const int d = T - 133, d1 = d / 2;
+    return -__fmul_rn(__fmul_rn(sum, __int_as_float((d1 + 127) << 23)),
+                      __int_as_float((d - d1 + 127) << 23));
 }
 
 // VPL consecutive activations of token n from column k0 (VPL = 8 bf16 in mode
 // A, 16 int8 in mode B; k0 a multiple of VPL): one 16-byte load when X allows
-// it, else element loads; columns >= K read as 0.
+// it, else element loads; columns >= K read as 0.  Loads go to L2 (not the
+// SM's L1), since in a chain X may have been written by other SMs during
+// the launch.
 template <bool kModeA>
 __device__ __forceinline__ uint4 load_group(const GroupArgs &a, int n, int k0) {
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (kModeA) {
         const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K + k0;
         if (a.xvec) {
-            if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4 *>(x));
+            if (k0 < a.K) v = __ldcg(reinterpret_cast<const uint4 *>(x));
         } else {
             uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (k0 + e < a.K) w[e >> 1] |= (uint32_t)x[e] << (16 * (e & 1));
+                if (k0 + e < a.K) w[e >> 1] |= (uint32_t)__ldcg(x + e) << (16 * (e & 1));
             v = make_uint4(w[0], w[1], w[2], w[3]);
         }
     } else {
         const uint8_t *x = reinterpret_cast<const uint8_t *>(a.X) + (long long)n * a.K + k0;
         if (a.xvec) {
-            if (k0 < a.K) v = __ldg(reinterpret_cast<const uint4 *>(x));
+            if (k0 < a.K) v = __ldcg(reinterpret_cast<const uint4 *>(x));
         } else {
             uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                if (k0 + e < a.K) w[e >> 2] |= (uint32_t)x[e] << (8 * (e & 3));
+                if (k0 + e < a.K) w[e >> 2] |= (uint32_t)__ldcg(x + e) << (8 * (e & 3));
             v = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
@@ -430,9 +508,11 @@ __device__ __forceinline__ void store_rotated(uint32_t *dst, const uint32_t (&w)
 
 // One staging group: activation group o (8 bf16 in mode A, 16 int8 in mode
 // B, as one 16-byte word x) of token n in a block whose staged words start
-// at blk.  Writes the group's words in B-fragment order, times 2^kT, and
-// returns the group's sum in a fixed order and (mode A) the mask of halves
-// outside the fixed window.  A zero x writes zeros.
+// at blk.  Writes the group's words in B-fragment order, times 2^(kT - 2q)
+// for k-step class q = m % 4 (the A operand of class q carries 2^(2q - 133),
+// so every product is w-field * x * 2^(kT - 133)), and returns the group's
+// sum in a fixed order and (mode A) the mask of halves outside the fixed
+// window.  A zero x writes zeros.
 template <bool kModeA, int NT>
 __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const uint4 &x,
                                             float &sum, uint32_t &bad) {
@@ -441,6 +521,7 @@ __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const u
     bad = 0u;
     if (kModeA) {
         const int m = o >> 1, qd = m >> 1;
+        const uint32_t ex = (uint32_t)(kT - 2 * (m & 3)) * 0x00800080u;
         uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1) + (o & 1);
         uint32_t st[4];
 #pragma unroll
@@ -452,7 +533,7 @@ __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const u
             const uint32_t nz = __vcmpne2(v & 0x7FFF7FFFu, 0u);
             const uint32_t off = __vsub2(v & 0x7F807F80u, (uint32_t)kWinLo * 0x00800080u);
             bad |= __vcmpgtu2(off, (uint32_t)(kWinHi - kWinLo) * 0x00800080u) & nz;
-            st[tt] = v + ((uint32_t)kT * 0x00800080u & nz);
+            st[tt] = v + (ex & nz);
         }
         // store word tt = (it + qd) % 4 at step it: the lanes of one block
         // quarter apart then write different banks
@@ -460,7 +541,7 @@ __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const u
     } else {
         const int m = o, qd = m >> 1;
         uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1);
-        const float two_t = __int_as_float((kT + 127) << 23);
+        const float two_t = __int_as_float((kT - 2 * (m & 3) + 127) << 23);
         int isum = 0;
 #pragma unroll
         for (int h8 = 0; h8 < 2; ++h8) {
@@ -503,13 +584,190 @@ __device__ __forceinline__ void stage_load(const GroupArgs &a, const Slice &P, i
     }
 }
 
-// Kernel launch helpers shared with the host side.
-// ------------------------------------------------------------ kernel
+// ------------------------------------------------------------ weight pipeline
+// Each warp streams its units into a ring of kSlots shared-memory slots:
+// lane 0 issues one bulk copy of up to CH tiles per slot, completing on the
+// slot's mbarrier, and all lanes consume the slots in the same order.  In a
+// chain of linears the producer runs on into the next step's units while the
+// warp still works on the current step, so weights keep arriving across the
+// wait for the step's inputs.
+struct Pipe {
+    uint32_t ring_w, bar_w;  // this warp's ring and barriers (shared-window addresses)
+    int slot;                // next slot to consume
+    uint32_t phases;         // parity to wait for, one bit per slot
+    uint32_t inflight;       // (lane 0) slots with a copy in flight
+    // (lane 0) the next chunk to copy: step pstep, cursor pc
+    const GroupArgs *steps;
+    int nsteps, pstep;
+    int pcu0, pcu1, psig1;   // this CTA's units of step pstep
+    Cursor pc;
+    int pgi;
+    const char *prow;
+    bool pc_on;
+};
+
+// This CTA's units of a launch -- a contiguous range of one slice, none for
+// CTAs past the plan's -- and the slices [sig0, sig1) it touches.
+__device__ __forceinline__ void cta_units(const GroupArgs &a, int cta, int &cu0, int &cu1,
+                                          int &sig0, int &sig1) {
+    cu0 = cu1 = a.U;
+    const int sig_c = cta / a.Pps, c_in = cta - sig_c * a.Pps;
+    if (sig_c < a.NS) {
+        const int su = a.R * slice_width(a, sig_c);
+        const int lc = sig_c == a.NS - 1 ? a.LcL : a.Lc;
+        const int base = sig_c * a.R * a.KW;
+        const int off = (int)min((long long)c_in * lc, (long long)su);
+        cu0 = base + off;
+        cu1 = base + min(off + lc, su);
+    }
+    const int sunits = a.R * a.KW;
+    sig0 = cu0 / sunits;
+    sig1 = cu1 > cu0 ? (cu1 - 1) / sunits + 1 : sig0;
+}
+
+// Producer: move to the first linear step from p.pstep on in which this
+// warp has units.
+__device__ __forceinline__ void pipe_seek(Pipe &p, int cta, int warp) {
+    for (; p.pstep < p.nsteps; ++p.pstep) {
+        const GroupArgs &a = p.steps[p.pstep];
+        if (a.kind != kStepLinear || cta >= a.P) continue;
+        int sig0;
+        cta_units(a, cta, p.pcu0, p.pcu1, sig0, p.psig1);
+        p.pc.sigma = sig0;
+        if (cursor_enter(a, p.pcu0, p.pcu1, p.psig1, warp, p.pc)) {
+            p.prow = row_base(a, p.pc.r, p.pgi);
+            p.pc_on = true;
+            return;
+        }
+    }
+    p.pc_on = false;
+}
+
+// Producer (lane 0, p.pc_on): copy the next chunk into `slot` and advance.
+template <int NT>
+__device__ __forceinline__ void pipe_produce(Pipe &p, int slot, int cta, int warp) {
+    constexpr int CH = chunk_tiles(NT);
+    const GroupArgs &a = p.steps[p.pstep];
+    const int n = min(CH, min(p.pc.uend - p.pc.u, p.pc.kw - p.pc.b));
+    bulk_load(p.ring_w + slot * (CH * 512), p.prow + (long long)(p.pc.kb0 + p.pc.b) * 512, n * 512,
+              p.bar_w + 8u * slot);
+    p.inflight |= 1u << slot;
+    p.pc.u += n;
+    p.pc.b += n;
+    if (p.pc.b == p.pc.kw) {
+        p.pc.b = 0;
+        ++p.pc.r;
+        if (p.pgi + 1 < a.G && p.pc.r == a.rt_off[p.pgi + 1]) p.prow = a.packed[++p.pgi];
+        else p.prow += (long long)a.KB * 512;
+    }
+    if (p.pc.u == p.pc.uend) {
+        ++p.pc.sigma;
+        if (cursor_enter(a, p.pcu0, p.pcu1, p.psig1, warp, p.pc)) {
+            p.prow = row_base(a, p.pc.r, p.pgi);
+        } else {
+            ++p.pstep;
+            pipe_seek(p, cta, warp);
+        }
+    }
+}
+
+// Lane 0: bring this warp's tiles of one linear step into L2 (bulk
+// prefetches of up to CH tiles; they return no data).
+template <int NT>
+__device__ __forceinline__ void prefetch_l2(const GroupArgs &a, int cta, int warp) {
+    constexpr int CH = chunk_tiles(NT);
+    if (a.kind != kStepLinear || cta >= a.P) return;
+    int cu0, cu1, sig0, sig1;
+    cta_units(a, cta, cu0, cu1, sig0, sig1);
+    Cursor q;
+    q.sigma = sig0;
+    if (!cursor_enter(a, cu0, cu1, sig1, warp, q)) return;
+    int qg = 0;
+    const char *qr = row_base(a, q.r, qg);
+    for (bool on = true; on;) {
+        const int n = min(CH, min(q.uend - q.u, q.kw - q.b));
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qr + (long long)(q.kb0 + q.b) * 512),
+                     "r"(n * 512)
+                     : "memory");
+        q.u += n;
+        q.b += n;
+        if (q.b == q.kw) {
+            q.b = 0;
+            ++q.r;
+            if (qg + 1 < a.G && q.r == a.rt_off[qg + 1]) qr = a.packed[++qg];
+            else qr += (long long)a.KB * 512;
+        }
+        if (q.u == q.uend) {
+            ++q.sigma;
+            on = cursor_enter(a, cu0, cu1, sig1, warp, q);
+            if (on) qr = row_base(a, q.r, qg);
+        }
+    }
+}
+
+// Lane 0, after a wait gave up: let the copies still in flight land
+// (bounded) before the CTA leaves.
+__device__ __forceinline__ void pipe_drain(const Pipe &p, int *status) {
+    for (int k = 0; k < kSlots; ++k)
+        if (p.inflight >> k & 1) mbar_wait(p.bar_w + 8u * k, (p.phases >> k) & 1u, status);
+}
+
+// Lane 0: barriers of this warp's ring, then the first kSlots copies.
+template <int NT>
+__device__ __forceinline__ void pipe_start(Pipe &p, int cta, int warp) {
+    for (int k = 0; k < kSlots; ++k) mbar_init(p.bar_w + 8u * k, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    pipe_seek(p, cta, warp);
+    for (int k = 0; k < kSlots && p.pc_on; ++k) pipe_produce<NT>(p, k, cta, warp);
+}
+
+// Bounded wait of one thread until *word == target (or, with `nonzero`,
+// until *word != 0), with acquire semantics.  Gives up, returning false,
+// when another CTA has set the status word or after `limit` SM cycles (and
+// then sets the status word itself).
+__device__ __forceinline__ bool wait_word(const unsigned *word, unsigned target, bool nonzero,
+                                          long long limit, int *status) {
+    const long long t0 = clock64();
+    for (unsigned it = 0;; ++it) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+        if (nonzero ? v != 0u : v == target) return true;
+        if ((it & 15u) == 15u) {
+            int st;
+            asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(st) : "l"(status) : "memory");
+            if (st != 0) return false;
+            if (clock64() - t0 > limit) {
+                atomicExch(status, TL_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Per-CTA shared state of a linear step.
+template <int NT>
+struct StepSmem {
+    float bslot[kWarps][2][16 * NT];   // boundary pieces of the current slice
+    int bslot_row[kWarps][2];
+    // per (block, token, half block): -(sum of x) * 2^(T - 133), added to the
+    // half's chain once per tile (see xh_index)
+    float xh[kMaxSlice * NT * 2];
+    int texp[NT];                      // T per token: X is staged times 2^(T - 2q)
+    int emax[NT];
+    int redo;                          // tokens outside the fixed window (bit mask)
+    int go;                            // the step's inputs are ready
+};
+
+// ------------------------------------------------------------ one linear step
 // kModeA: bf16 activations (else int8 from the quantiser).  NT: token
-// columns staged (a power of two >= N).
-template <bool kModeA, int NT>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-tl_mma_kernel(const __grid_constant__ GroupArgs a) {
+// columns staged (a power of two >= N).  kChain: the step is one of a chain
+// run by one persistent launch; it waits for step - 1 (prevP CTAs) through
+// the chain's counters instead of for the previous kernel.  Returns, the
+// same in every thread of the CTA, whether every wait succeeded.
+template <bool kModeA, int NT, bool kChain>
+__device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *smem,
+                                         StepSmem<NT> &sh, Pipe &pipe, const ChainHeader *ch,
+                                         int step, unsigned prevP) {
     constexpr int CH = chunk_tiles(NT);         // tiles per bulk copy
     constexpr int SLOT = CH * 512;
     constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
@@ -517,110 +775,32 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     constexpr int RV = 16 * NT;                 // floats per row-tile result
     constexpr int VPL = kModeA ? 8 : 16;        // activations per staging group
     constexpr int LB = 128 / VPL;               // staging groups per block
+    constexpr int HB = LB / 2;                  // staging groups per half block
+    constexpr int XHB = 2 * NT;                 // correction floats per block
     constexpr int SB = stage_batch(NT, kModeA); // staging loads in flight per thread
     constexpr bool kAsyncX = NT >= 4;           // stage X with cp.async (when X allows 16-byte copies)
-    extern __shared__ __align__(128) uint8_t smem[];
+    // dynamic shared memory, at offsets fixed for every step of a launch
     uint8_t *ring = smem;                                                // [kWarps][kSlots][SLOT]
     uint4 *xs = reinterpret_cast<uint4 *>(smem + ring_bytes(NT));      // one slice of X
-    float *acc = reinterpret_cast<float *>(smem + ring_bytes(NT) + a.KW * XB * 16);  // [rows][RV]
-    float *scl = acc + a.rows * RV;                                      // [rows][16] scales
-    int *rsm = reinterpret_cast<int *>(scl + a.rows * 16);               // [rows][16] row sums
-    __shared__ float bslot[kWarps][2][RV];      // boundary pieces of the current slice
-    __shared__ int bslot_row[kWarps][2];
-    __shared__ float osum[kMaxSlice][NT];       // sum of x per block of the slice
-    __shared__ float opre[kMaxSlice + 1][NT];   // prefix sums of osum
-    __shared__ int texp[NT];                    // T per token: X is staged times 2^T
-    __shared__ int redo;                        // tokens outside the fixed window (bit mask)
-    __shared__ int emax[NT];
-    __shared__ __align__(8) unsigned long long bars[kWarps][kSlots];
+    float *acc = reinterpret_cast<float *>(smem + ring_bytes(NT) + a.kwr * XB * 16);  // [rows][RV]
+    float *scl = acc + a.rowsr * RV;                                     // [rows][16] scales
+    int *rsm = reinterpret_cast<int *>(scl + a.rowsr * 16);              // [rows][16] row sums
+    auto &bslot = sh.bslot;
+    auto &bslot_row = sh.bslot_row;
+    float *xh = sh.xh;
+    int *texp = sh.texp;
+    int *emax = sh.emax;
+    int &redo = sh.redo;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int N = a.N;
     // this CTA's units: range c_in of its slice (none past the last slice)
-    int cu0 = a.U, cu1 = a.U;
-    {
-        const int sig_c = (int)blockIdx.x / a.Pps, c_in = (int)blockIdx.x - sig_c * a.Pps;
-        if (sig_c < a.NS) {
-            const int su = a.R * slice_width(a, sig_c);
-            const int lc = sig_c == a.NS - 1 ? a.LcL : a.Lc;
-            const int base = sig_c * a.R * a.KW;
-            const int off = (int)min((long long)c_in * lc, (long long)su);
-            cu0 = base + off;
-            cu1 = base + min(off + lc, su);
-        }
-    }
-    const int sunits = a.R * a.KW;
-    const int sig0 = cu0 / sunits;
-    const int sig1 = cu1 > cu0 ? (cu1 - 1) / sunits + 1 : sig0;
+    int cu0, cu1, sig0, sig1;
+    cta_units(a, cta, cu0, cu1, sig0, sig1);
     uint32_t *xw = reinterpret_cast<uint32_t *>(xs);
     const uint32_t xs_s = smem_u32(xs);
 
-    // The dependent launch may be scheduled at once; it only streams weights
-    // until this grid has finished.
-    griddep_launch();
-
-    // Weights do not depend on the previous kernel: each warp's lane 0 sets up
-    // its ring and starts its first copies before waiting for it.  The
-    // producer then runs kSlots chunks ahead of the warp's consumer, across
-    // slices.
-    const uint32_t ring_w = smem_u32(ring) + warp * (kSlots * SLOT);
-    const uint32_t bar_w = smem_u32(&bars[warp][0]);
-    Cursor pc;
-    pc.sigma = sig0;
-    bool pc_on = cursor_enter(a, cu0, cu1, sig1, warp, pc);
-    int pgi = 0;
-    const char *prow = pc_on ? row_base(a, pc.r, pgi) : nullptr;
-    auto produce = [&](int slot_) {
-        const int n = min(CH, min(pc.uend - pc.u, pc.kw - pc.b));
-        bulk_load(ring_w + slot_ * SLOT, prow + (long long)(pc.kb0 + pc.b) * 512, n * 512,
-                  bar_w + 8u * slot_);
-        pc.u += n;
-        pc.b += n;
-        if (pc.b == pc.kw) {
-            pc.b = 0;
-            ++pc.r;
-            if (pgi + 1 < a.G && pc.r == a.rt_off[pgi + 1]) prow = a.packed[++pgi];
-            else prow += (long long)a.KB * 512;
-        }
-        if (pc.u == pc.uend) {
-            ++pc.sigma;
-            pc_on = cursor_enter(a, cu0, cu1, sig1, warp, pc);
-            if (pc_on) prow = row_base(a, pc.r, pgi);
-        }
-    };
-    if (lane == 0) {
-        for (int k = 0; k < kSlots; ++k) mbar_init(bar_w + 8u * k, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int k = 0; k < kSlots && pc_on; ++k) produce(k);
-        // and the rest of this warp's tiles into L2, while the previous
-        // launch may still be running
-        if (pc_on) {
-            Cursor q = pc;
-            int qg = pgi;
-            const char *qr = prow;
-            for (bool on = true; on;) {
-                const int n = min(CH, min(q.uend - q.u, q.kw - q.b));
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                                 qr + (long long)(q.kb0 + q.b) * 512),
-                             "r"(n * 512)
-                             : "memory");
-                q.u += n;
-                q.b += n;
-                if (q.b == q.kw) {
-                    q.b = 0;
-                    ++q.r;
-                    if (qg + 1 < a.G && q.r == a.rt_off[qg + 1]) qr = a.packed[++qg];
-                    else qr += (long long)a.KB * 512;
-                }
-                if (q.u == q.uend) {
-                    ++q.sigma;
-                    on = cursor_enter(a, cu0, cu1, sig1, warp, q);
-                    if (on) qr = row_base(a, q.r, qg);
-                }
-            }
-        }
-    }
     // this CTA's scales (and row sums) of its first slice, one per thread
     Slice P;
     slice_of(a, cu0, cu1, sig0, P);
@@ -642,9 +822,11 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     if (threadIdx.x == 0) redo = 0;
     if (threadIdx.x < NT) emax[threadIdx.x] = 0;
     for (int i = threadIdx.x; i < a.rows * RV; i += kThreads) acc[i] = 0.f;
-    if (N < NT)   // the columns past the batch stay zero in every slice
-        for (int i = threadIdx.x; i < a.KW * 64 * NT; i += kThreads)
+    if (N < NT) {  // the columns past the batch stay zero in every slice
+        for (int i = threadIdx.x; i < a.kwr * 64 * NT; i += kThreads)
             if (((i >> 4) % NT) >= N) xw[i] = 0u;
+        for (int i = threadIdx.x; i < kMaxSlice * NT * 2; i += kThreads) xh[i] = 0.f;
+    }
     // Warm L2 (and the address translation) for this CTA's activations; a
     // prefetch returns no data, so it may run before the previous kernel has
     // written them.  One 128-byte line per thread per step, addresses inside
@@ -662,16 +844,26 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     }
     __syncthreads();
 
-    // Now the activations, written by the previous kernel.
-    griddep_wait();
+    // Now the activations, written by the previous kernel or step.
+    if (!kChain) {
+        griddep_wait();
+    } else {
+        if (threadIdx.x == 0)
+            sh.go = step == 0 ? (ch->gate == nullptr ||
+                                 wait_word(ch->gate, 0u, true, ch->wait_limit, a.status))
+                              : wait_word(ch->cnt + step - 1, prevP, false, ch->wait_limit, a.status);
+        __syncthreads();
+        if (!sh.go) return false;
+    }
     uint4 xv[SB];
     if (!(kAsyncX && a.xvec)) stage_load<kModeA, SB>(a, P, 0, xv);
 
     Cursor cc;
     cc.sigma = sig0;
     bool cc_on = cursor_enter(a, cu0, cu1, sig1, warp, cc);
-    int slot = 0;
-    uint32_t phases = 0;                        // parity bit per slot
+    int &slot = pipe.slot;
+    uint32_t &phases = pipe.phases;             // parity bit per slot
+    const uint32_t bar_w = pipe.bar_w;
     bool ok = true;
     float c[4][4];
 
@@ -729,9 +921,9 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                         uint32_t bad;
                         stage_group<kModeA, NT>(blk, n, o, v[j], sum, bad);
 #pragma unroll
-                        for (int off = LB / 2; off > 0; off >>= 1)
+                        for (int off = HB / 2; off > 0; off >>= 1)
                             sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
-                        if (n < N && o == 0) osum[jb][n] = sum;
+                        if (n < N && (o % HB) == 0) xh[xh_index<NT>(jb, n, o / HB)] = chain_units(sum, kT);
                         if (kModeA && n < N && bad) atomicOr(&redo, 1 << n);
                     }
                 }
@@ -749,9 +941,9 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                     uint32_t bad = 0u;
                     if (valid) stage_group<kModeA, NT>(xw + jb * NT * 64, n, o, xv[i], sum, bad);
 #pragma unroll
-                    for (int off = LB / 2; off > 0; off >>= 1)
+                    for (int off = HB / 2; off > 0; off >>= 1)
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
-                    if (valid && (lane % LB) == 0) osum[jb][n] = sum;
+                    if (valid && (o % HB) == 0) xh[xh_index<NT>(jb, n, o / HB)] = chain_units(sum, kT);
                     if (kModeA && valid && bad) atomicOr(&redo, 1 << n);
                 }
             }
@@ -794,7 +986,8 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 if (!(mask >> n & 1)) continue;
                 const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
                 uint32_t e = 0;
-                for (int k = klo + threadIdx.x; k < khi; k += kThreads) e = max(e, ((uint32_t)x[k] >> 7) & 0xFFu);
+                for (int k = klo + threadIdx.x; k < khi; k += kThreads)
+                    e = max(e, ((uint32_t)__ldcg(x + k) >> 7) & 0xFFu);
                 e = __reduce_max_sync(0xffffffffu, e);
                 if (lane == 0) atomicMax(&emax[n], (int)e);
             }
@@ -808,37 +1001,36 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 const int m = 2 * qd + (w >> 1);
                 const int k = (P.kb0 + j) * 128 + 16 * m + 2 * tt + 8 * (w & 1);
                 const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
-                const uint32_t lo = k < a.K ? x[k] : 0u, hi = k + 1 < a.K ? x[k + 1] : 0u;
-                const int d = 254 - emax[n];
+                const uint32_t lo = k < a.K ? __ldcg(x + k) : 0u, hi = k + 1 < a.K ? __ldcg(x + k + 1) : 0u;
+                const int d = 254 - emax[n] - 2 * (m & 3);
                 xw[idx] = scale_any(lo, d) | (scale_any(hi, d) << 16);
+            }
+            // and the token's corrections at its new scale: one warp per
+            // (token, block, half), 64 activations summed in a fixed order
+            for (int p = warp; p < N * P.kw * 2; p += kWarps) {
+                const int h = p & 1, j = (p >> 1) % P.kw, n = (p >> 1) / P.kw;
+                if (!(mask >> n & 1)) continue;
+                const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K;
+                const int k = (P.kb0 + j) * 128 + 64 * h + 2 * lane;
+                float sm = __fadd_rn(k < a.K ? bf16f(__ldcg(x + k)) : 0.f,
+                                     k + 1 < a.K ? bf16f(__ldcg(x + k + 1)) : 0.f);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, off));
+                if (lane == 0) xh[xh_index<NT>(j, n, h)] = chain_units(sm, 254 - emax[n]);
             }
             __syncthreads();
             if (threadIdx.x == 0) redo = 0;
             if (threadIdx.x < NT) emax[threadIdx.x] = 0;
         }
 
-        // prefix sums of the block sums, one warp per token column
-        if (warp < NT) {
-            const int n = warp;
-            float v0 = lane < P.kw ? osum[lane][n] : 0.f;
-            float v1 = lane + 32 < P.kw ? osum[lane + 32][n] : 0.f;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y0 = __shfl_up_sync(0xffffffffu, v0, off);
-                const float y1 = __shfl_up_sync(0xffffffffu, v1, off);
-                if (lane >= off) { v0 = __fadd_rn(v0, y0); v1 = __fadd_rn(v1, y1); }
-            }
-            v1 = __fadd_rn(v1, __shfl_sync(0xffffffffu, v0, 31));
-            if (lane == 0) opre[0][n] = 0.f;
-            if (lane < P.kw) opre[lane + 1][n] = v0;
-            if (lane + 32 < P.kw) opre[lane + 33][n] = v1;
-        }
-        // this lane's tokens 2t, 2t+1: chain q holds the products of k-step
-        // class q, (1 - w) x 2^(2q - 133 + T); undo 2^(2q - 133 + T) with two
-        // exact factors each
+        // this lane's tokens 2t, 2t+1: the chains hold sum (1 - w) x 2^(T - 133)
+        // minus the corrections sum x 2^(T - 133), i.e. -sum w x 2^(T - 133);
+        // undo 2^(T - 133) with two exact factors
         int tx[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) tx[e] = texp[min(2 * t + e, NT - 1)];
+        for (int e = 0; e < 2; ++e) tx[e] = texp[(2 * t + e) % NT];
+        const float *xhl = xh + (NT == 1 ? 0 : xh_index<NT>(0, 2 * (t % (NT > 1 ? NT / 2 : 1)), 0));
 
         // ---- this warp's units of the slice
         int run_lo = cc.b, nslot = 0;
@@ -852,6 +1044,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
             phases ^= 1u << slot;
             const uint4 *tiles = reinterpret_cast<const uint4 *>(ring + warp * (kSlots * SLOT) + slot * SLOT) + lane;
             const uint4 *xb = xs + cc.b * XB + (g % NT) * 4 + t;
+            const float *xc = xhl + cc.b * XHB;
             if (n == CH) {
                 // full chunk: load tile i+1 while tile i is multiplied
                 uint4 w = tiles[0];
@@ -866,18 +1059,20 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
 #pragma unroll
                         for (int qd = 0; qd < 4; ++qd) bn[qd] = xb[(i + 1) * XB + qd * XQ];
                     }
-                    tile_mma(c, w, bq);
+                    tile_corrected<NT>(c, i & 1, w, bq, xc + i * XHB);
                     w = wn;
 #pragma unroll
                     for (int qd = 0; qd < 4; ++qd) bq[qd] = bn[qd];
                 }
             } else {
-                for (int i = 0; i < n; ++i) {
+#pragma unroll
+                for (int i = 0; i < CH; ++i) {
+                    if (i >= n) break;
                     const uint4 w = tiles[i * 32];
                     uint4 bq[4];
 #pragma unroll
                     for (int qd = 0; qd < 4; ++qd) bq[qd] = xb[i * XB + qd * XQ];
-                    tile_mma(c, w, bq);
+                    tile_corrected<NT>(c, i & 1, w, bq, xc + i * XHB);
                 }
             }
             // end of a run of one row tile: this chunk ends the row or the warp's range
@@ -886,14 +1081,10 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 float v[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float s = 0.f;
-#pragma unroll
-                    for (int cl = 0; cl < 4; ++cl) {
-                        const int d = 133 - tx[q & 1] - 2 * cl, d1 = d / 2;
-                        s = __fadd_rn(s, __fmul_rn(__fmul_rn(c[cl][q], __int_as_float((d1 + 127) << 23)),
-                                                   __int_as_float((d - d1 + 127) << 23)));
-                    }
-                    v[q] = s;
+                    const float sm = __fadd_rn(__fadd_rn(c[0][q], c[1][q]), __fadd_rn(c[2][q], c[3][q]));
+                    const int d = 133 - tx[q & 1], d1 = d / 2;
+                    v[q] = -__fmul_rn(__fmul_rn(sm, __int_as_float((d1 + 127) << 23)),
+                                      __int_as_float((d - d1 + 127) << 23));
                 }
                 int lo, hi;
                 row_span(P, cc.r, lo, hi);
@@ -920,9 +1111,12 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
             }
             // refill this slot with the chunk kSlots ahead
             __syncwarp();
-            if (lane == 0 && pc_on) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                produce(slot);
+            if (lane == 0) {
+                pipe.inflight &= ~(1u << slot);
+                if (pipe.pc_on) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    pipe_produce<NT>(pipe, slot, cta, warp);
+                }
             }
             cc.u += n;
             cc.b += n;
@@ -959,11 +1153,6 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 int lo, hi;
                 row_span(P, r, lo, hi);
                 float *v = acc + rho * RV;
-                for (int e = lane; e < N * 16; e += 32) {
-                    const int n = e >> 4;
-                    v[e] = __fsub_rn(__fsub_rn(opre[hi][n], opre[lo][n]), v[e]);
-                }
-                __syncwarp();
                 if (a.NS == 1 && lo == 0 && hi == P.kw) {
                     store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
                 } else if (a.NS == 1) {
@@ -1026,13 +1215,43 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
                 for (int e = lane; e < RV; e += 32) v[e] = 0.f;   // ready for the next slice
             }
         }
-        // (the next slice's staging barrier orders these reads of opre, acc
+        // (the next slice's staging barrier orders these reads of xh, acc
         // and scl before they are rewritten)
     }
-    if (!ok) {
-        // a copy never landed: drain what is still in flight (bounded), then leave
-        for (int k = 0; k < kSlots; ++k) mbar_wait(bar_w + 8u * k, (phases >> k) & 1u, a.status);
+    return __syncthreads_and(ok) != 0;
+}
+
+
+// ------------------------------------------------------------ kernels
+// One (grouped) linear per launch.
+template <bool kModeA, int NT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+tl_mma_kernel(const __grid_constant__ GroupArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(16) StepSmem<NT> sh;
+    __shared__ __align__(8) unsigned long long bars[kWarps][kSlots];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The dependent launch may be scheduled at once; it only streams weights
+    // until this grid has finished.
+    griddep_launch();
+    Pipe pipe;
+    pipe.ring_w = smem_u32(smem) + warp * (kSlots * chunk_tiles(NT) * 512);
+    pipe.bar_w = smem_u32(&bars[warp][0]);
+    pipe.slot = 0;
+    pipe.phases = 0;
+    pipe.inflight = 0;
+    pipe.steps = &a;
+    pipe.nsteps = 1;
+    pipe.pstep = 0;
+    // Weights do not depend on the previous kernel: each warp's lane 0 starts
+    // its first copies, and brings the rest of its tiles into L2, before the
+    // launch waits for it.
+    if (lane == 0) {
+        pipe_start<NT>(pipe, blockIdx.x, warp);
+        prefetch_l2<NT>(a, blockIdx.x, warp);
     }
+    const bool ok = run_step<kModeA, NT, false>(a, blockIdx.x, smem, sh, pipe, nullptr, 0, 0u);
+    if (!ok && lane == 0) pipe_drain(pipe, a.status);
 }
 
 using KernelFn = void (*)(GroupArgs);
@@ -1050,23 +1269,66 @@ KernelFn kernel_for(int mode, int nt) {
 inline int padded_tokens(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
 // ------------------------------------------------------------------ quant
-__global__ void __launch_bounds__(256)
-tl_quant_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Q,
-                float *__restrict__ s_out, int32_t *__restrict__ z_out, int symmetric) {
-    const int n = blockIdx.x;
+// Per-token activation quantisation as a grid of (K chunk, token) CTAs.
+// Every CTA of a token reduces the token's whole row to its minimum and
+// maximum (exact and independent of order, so all of them derive the same s
+// and z), then quantises its own chunk.  q = rint(x / s) needs the correctly
+// rounded quotient only where it decides the rounding: x * (1/s) is within
+// three units in the last place of fl(x / s), so it gives the same integer
+// unless it lies that close to a half-integer (or is not finite), and only
+// then is the IEEE division taken.
+constexpr int kQThreads = 256;
+constexpr int kQChunk = 4096;          // activations quantised per CTA
+
+__device__ __forceinline__ float quant_round(float v, float s, float r) {
+    const float t = __fmul_rn(v, r);
+    const float d = fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f));
+    // |t| <= 2^9 here when the fast path is taken, so t - floor(t) is exact
+    if (d > __fmul_rn(fabsf(t), 0x1p-20f) && fabsf(t) < 512.f) return rintf(t);
+    return rintf(__fdiv_rn(v, s));
+}
+
+// Token n, chunk c (kQThreads threads).  kLaunch: a launch of its own, which
+// waits for the previous kernel on the stream and lets the next one start.
+template <bool kLaunch>
+__device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int K, int vec,
+                                            int8_t *__restrict__ Q, float *__restrict__ s_out,
+                                            int32_t *__restrict__ z_out, int symmetric, int n,
+                                            int c) {
+    const int k0 = c * kQChunk;
     const uint16_t *x = X + (long long)n * K;
     int8_t *q = Q + (long long)n * K;
+    // the previous kernel on the stream may still be writing X
+    if (kLaunch) griddep_wait();
     float lo = 0.f, hi = 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        const float v = __uint_as_float((uint32_t)x[k] << 16);
-        if (symmetric) {
-            hi = fmaxf(hi, fabsf(v));
-        } else {
-            lo = fminf(lo, v);
-            hi = fmaxf(hi, v);
+    if (vec) {
+        const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+        for (int i = threadIdx.x; i < K / 8; i += kQThreads) {
+            const uint4 u = __ldcg(xv + i);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(w[j] << 16), b = __uint_as_float(w[j] & 0xFFFF0000u);
+                if (symmetric) {
+                    hi = fmaxf(hi, fmaxf(fabsf(a), fabsf(b)));
+                } else {
+                    lo = fminf(lo, fminf(a, b));
+                    hi = fmaxf(hi, fmaxf(a, b));
+                }
+            }
+        }
+    } else {
+        for (int k = threadIdx.x; k < K; k += kQThreads) {
+            const float v = __uint_as_float((uint32_t)__ldcg(x + k) << 16);
+            if (symmetric) {
+                hi = fmaxf(hi, fabsf(v));
+            } else {
+                lo = fminf(lo, v);
+                hi = fmaxf(hi, v);
+            }
         }
     }
-    __shared__ float slo[32], shi[32];
+    __shared__ float slo[kQThreads / 32], shi[kQThreads / 32];
     __shared__ float s_sh;
     __shared__ int z_sh;
     for (int o = 16; o > 0; o >>= 1) {
@@ -1077,7 +1339,7 @@ tl_quant_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Q,
     if (ln == 0) { slo[wid] = lo; shi[wid] = hi; }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+        for (int w = 1; w < kQThreads / 32; ++w) {
             lo = fminf(lo, slo[w]);
             hi = fmaxf(hi, shi[w]);
         }
@@ -1095,28 +1357,142 @@ tl_quant_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Q,
         }
         s_sh = s;
         z_sh = z;
-        s_out[n] = s;
-        z_out[n] = z;
+        if (c == 0) {
+            s_out[n] = s;
+            z_out[n] = z;
+        }
     }
     __syncthreads();
+    // the next kernel may start its prologue; it waits for this grid before
+    // reading Q, s and z
+    if (kLaunch) griddep_launch();
     const float s = s_sh;
+    const float r = __frcp_rn(s);
     const float zf = (float)z_sh;
     const float qlo = symmetric ? -127.f : -128.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        const float v = __uint_as_float((uint32_t)x[k] << 16);
-        float r = __fadd_rn(rintf(__fdiv_rn(v, s)), zf);
-        r = fminf(fmaxf(r, qlo), 127.f);
-        q[k] = (int8_t)(int)r;
+    const int k1 = min(K, k0 + kQChunk);
+    auto one = [&](float v) {
+        const float t = fminf(fmaxf(__fadd_rn(quant_round(v, s, r), zf), qlo), 127.f);
+        return (uint32_t)(uint8_t)(int8_t)(int)t;
+    };
+    if (vec) {
+        // 8 activations per step: one 16-byte load, one 8-byte store
+        const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+        for (int i = k0 / 8 + threadIdx.x; i < k1 / 8; i += kQThreads) {
+            const uint4 u = __ldcg(xv + i);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[2] = {0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo8 = one(__uint_as_float(w[j] << 16));
+                const uint32_t hi8 = one(__uint_as_float(w[j] & 0xFFFF0000u));
+                o[j >> 1] |= (lo8 | (hi8 << 8)) << (16 * (j & 1));
+            }
+            reinterpret_cast<uint2 *>(q)[i] = make_uint2(o[0], o[1]);
+        }
+    } else {
+        for (int k = k0 + threadIdx.x; k < k1; k += kQThreads)
+            q[k] = (int8_t)one(__uint_as_float((uint32_t)__ldcg(x + k) << 16));
+    }
+}
+
+__global__ void __launch_bounds__(kQThreads)
+tl_quant_kernel(const uint16_t *__restrict__ X, int K, int vec, int8_t *__restrict__ Q,
+                float *__restrict__ s_out, int32_t *__restrict__ z_out, int symmetric) {
+    quant_chunk<true>(X, K, vec, Q, s_out, z_out, symmetric, blockIdx.y, blockIdx.x);
+}
+
+// ------------------------------------------------------------------ chains
+// A chain of linears (and, in mode B, quantiser steps) in one persistent
+// launch: every CTA works through the steps in order, waiting before each
+// for the previous step's CTAs to have finished (a release/acquire counter
+// per step, bounded waits), while its warps' weight pipelines run ahead into
+// later steps and prefetch their weights into L2.  The CTA that completes a
+// step's counter clears the previous step's, and the last step's, so the
+// counters are zero again when the launch ends.
+template <bool kModeA, int NT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict__ steps) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(16) StepSmem<NT> sh;
+    __shared__ __align__(8) unsigned long long bars[kWarps][kSlots];
+    __shared__ __align__(16) GroupArgs sa;      // the current step's constants
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, cta = blockIdx.x;
+    const int nsteps = ch->nsteps, ahead = ch->lookahead;
+    Pipe pipe;
+    pipe.ring_w = smem_u32(smem) + warp * (kSlots * chunk_tiles(NT) * 512);
+    pipe.bar_w = smem_u32(&bars[warp][0]);
+    pipe.slot = 0;
+    pipe.phases = 0;
+    pipe.inflight = 0;
+    pipe.steps = steps;
+    pipe.nsteps = nsteps;
+    pipe.pstep = 0;
+    if (lane == 0) {
+        pipe_start<NT>(pipe, cta, warp);
+        for (int k = 0; k < ahead && k < nsteps; ++k) prefetch_l2<NT>(steps[k], cta, warp);
+    }
+    bool ok = true;
+    int *status = nullptr;
+    for (int step = 0; step < nsteps; ++step) {
+        if (lane == 0 && step + ahead < nsteps) prefetch_l2<NT>(steps[step + ahead], cta, warp);
+        __syncthreads();                         // everyone is done with the last step's constants
+        for (int i = threadIdx.x; i < (int)(sizeof(GroupArgs) / 4); i += kThreads)
+            reinterpret_cast<uint32_t *>(&sa)[i] = reinterpret_cast<const uint32_t *>(steps + step)[i];
+        __syncthreads();
+        status = sa.status;
+        if (cta >= sa.P) continue;
+        const unsigned prevP = step > 0 ? (unsigned)steps[step - 1].P : 0u;
+        if (sa.kind == kStepLinear) {
+            ok = run_step<kModeA, NT, true>(sa, cta, smem, sh, pipe, ch, step, prevP);
+        } else {
+            if (threadIdx.x == 0)
+                sh.go = step == 0 ? (ch->gate == nullptr ||
+                                     wait_word(ch->gate, 0u, true, ch->wait_limit, sa.status))
+                                  : wait_word(ch->cnt + step - 1, prevP, false, ch->wait_limit, sa.status);
+            __syncthreads();
+            ok = sh.go != 0;
+            if (ok) {
+                const int chunks = (sa.K + kQChunk - 1) / kQChunk;
+                quant_chunk<false>(reinterpret_cast<const uint16_t *>(sa.X), sa.K, sa.xvec, sa.qout,
+                                   sa.sout, sa.zout, sa.sym, cta / chunks, cta % chunks);
+            }
+        }
+        if (!ok) break;
+        // the step's results are written: count this CTA in
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const unsigned done = atomicAdd(ch->cnt + step, 1u) + 1u;
+            if (done == (unsigned)sa.P) {
+                if (step > 0) atomicExch(ch->cnt + step - 1, 0u);
+                if (step == nsteps - 1) atomicExch(ch->cnt + step, 0u);
+            }
+        }
+    }
+    if (!ok && lane == 0) pipe_drain(pipe, status);
+}
+
+using ChainFn = void (*)(const ChainHeader *, const GroupArgs *);
+
+ChainFn chain_kernel_for(int mode, int nt) {
+    const bool A = mode == TL_MODE_BF16;
+    switch (nt) {
+        case 1: return A ? tl_chain_kernel<true, 1> : tl_chain_kernel<false, 1>;
+        case 2: return A ? tl_chain_kernel<true, 2> : tl_chain_kernel<false, 2>;
+        case 4: return A ? tl_chain_kernel<true, 4> : tl_chain_kernel<false, 4>;
+        default: return A ? tl_chain_kernel<true, 8> : tl_chain_kernel<false, 8>;
     }
 }
 
 // ------------------------------------------------------------------ host side
 
 struct DeviceInfo {
-    int init;     // 0 = unknown, 1 = ok, -1 = unsupported
-    int sms;
+    std::atomic<int> init;   // 0 = unknown, 1 = ok, -1 = unsupported
+    int sms;                 // written before init is set to 1
 };
 DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;      // serialises first-time set-up across host threads
 
 // Dynamic shared memory: weight ring, one slice of X, row accumulators, and
 // the rows' scales and row sums.
@@ -1125,33 +1501,47 @@ constexpr size_t dyn_smem(int nt, int kw, int rows) {
            (size_t)rows * 16 * 8;
 }
 
+// Attributes of the current device, looked up (and the kernels' shared
+// memory limits raised) once per device; host threads may race to do it.
+tl_status init_device(int dev, DeviceInfo &d) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TL_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+        d.init.store(-1, std::memory_order_release);
+        return TL_OK;
+    }
+    for (int mode = 0; mode < 2; ++mode)
+        for (int nt = 1; nt <= 8; nt *= 2)
+            if (cudaFuncSetAttribute(kernel_for(mode, nt),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess ||
+                cudaFuncSetAttribute(chain_kernel_for(mode, nt),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess)
+                return TL_ERR_CUDA;
+    const tl_status pst = tl_internal::prefill_init_device();
+    if (pst != TL_OK) return pst;
+    d.sms = sms;
+    d.init.store(1, std::memory_order_release);
+    return TL_OK;
+}
+
 tl_status device_info(DeviceInfo **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TL_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return TL_ERR_UNSUPPORTED;
     DeviceInfo &d = g_dev[dev];
-    if (d.init == 0) {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return TL_ERR_CUDA;
-        if (major != 10 || minor != 3) {
-            d.init = -1;
-        } else {
-            for (int mode = 0; mode < 2; ++mode)
-                for (int nt = 1; nt <= 8; nt *= 2)
-                    if (cudaFuncSetAttribute(kernel_for(mode, nt),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess)
-                        return TL_ERR_CUDA;
-            const tl_status pst = tl_internal::prefill_init_device();
-            if (pst != TL_OK) return pst;
-            d.sms = sms;
-            d.init = 1;
+    if (d.init.load(std::memory_order_acquire) == 0) {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (d.init.load(std::memory_order_acquire) == 0) {
+            const tl_status st = init_device(dev, d);
+            if (st != TL_OK) return st;
         }
     }
-    if (d.init < 0) return TL_ERR_UNSUPPORTED;
+    if (d.init.load(std::memory_order_acquire) < 0) return TL_ERR_UNSUPPORTED;
     *out = &d;
     return TL_OK;
 }
@@ -1255,13 +1645,13 @@ size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
     return p.ws_bytes;
 }
 
-tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s,
-                       const int32_t *z, void *const *Ys, int n0, int n, int mode, int out,
-                       void *ws, size_t ws_bytes, unsigned flags, cudaStream_t stream,
-                       const DeviceInfo &dev) {
-    GroupArgs a;
+// Launch constants of one (grouped) linear over tokens [n0, n0 + n) with
+// plan p; the workspace pieces are given by the caller.
+void fill_linear(GroupArgs &a, const tl_weight *Ws, int G, const void *X, const float *s,
+                 const int32_t *z, void *const *Ys, int n0, int n, int mode, int out,
+                 const Plan &p, int *status, void *cnt, void *xslot, void *part) {
     std::memset(&a, 0, sizeof a);
-    int Ms[TL_MAX_GROUP];
+    a.kind = kStepLinear;
     a.G = G;
     a.rt_off[0] = 0;
     const int K = Ws[0].K;
@@ -1269,17 +1659,14 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
         a.packed[g] = reinterpret_cast<const char *>(Ws[g].packed);
         a.scale[g] = Ws[g].scale;
         a.rowsum[g] = Ws[g].rowsum;
-        a.M[g] = Ms[g] = Ws[g].M;
+        a.M[g] = Ws[g].M;
         const size_t esz = out == TL_OUT_BF16 ? 2 : 4;
         a.Y[g] = static_cast<char *>(Ys[g]) + (size_t)n0 * Ws[g].M * esz;
         a.rt_off[g + 1] = a.rt_off[g] + (int)ceil_div(Ws[g].M, 16);
     }
-    Plan p;
-    const tl_status pst = make_plan(Ms, G, K, n, dev.sms, &p);
-    if (pst != TL_OK) return pst;
-    if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
     a.R = p.R; a.KB = p.KB; a.KW = p.KW; a.KWL = p.KWL; a.NS = p.NS; a.K = K; a.U = (int)p.U;
-    a.Pps = p.Pps; a.Lc = p.Lc; a.LcL = p.LcL; a.rows = p.rows;
+    a.Pps = p.Pps; a.Lc = p.Lc; a.LcL = p.LcL; a.rows = p.rows; a.P = p.P;
+    a.kwr = p.KW; a.rowsr = p.rows;
     a.dKW = make_fastdiv((uint32_t)p.KW);
     a.dKWL = make_fastdiv((uint32_t)p.KWL);
     const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
@@ -1288,12 +1675,27 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     a.z = z ? z + n0 : nullptr;
     a.N = n; a.mode = mode; a.out = out;
     a.xvec = aligned(a.X, 16) && (K % (mode == TL_MODE_BF16 ? 8 : 16)) == 0;
+    a.cnt = static_cast<unsigned long long *>(cnt);
+    a.xslot = static_cast<unsigned long long *>(xslot);
+    a.part = static_cast<float *>(part);
+    a.status = status;
+}
+
+tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s,
+                       const int32_t *z, void *const *Ys, int n0, int n, int mode, int out,
+                       void *ws, size_t ws_bytes, unsigned flags, cudaStream_t stream,
+                       const DeviceInfo &dev) {
+    int Ms[TL_MAX_GROUP];
+    for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
+    Plan p;
+    const tl_status pst = make_plan(Ms, G, Ws[0].K, n, dev.sms, &p);
+    if (pst != TL_OK) return pst;
+    if (!ws || ws_bytes < p.ws_bytes) return TL_ERR_WORKSPACE;
     char *wsb = static_cast<char *>(ws) + tl_internal::kStatusBytes;
-    a.cnt = reinterpret_cast<unsigned long long *>(wsb);
-    a.xslot = reinterpret_cast<unsigned long long *>(wsb + p.cnt_bytes);
-    a.part = reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                       tl_internal::scratch_offset(ws_bytes, p.back));
-    a.status = static_cast<int *>(ws);
+    GroupArgs a;
+    fill_linear(a, Ws, G, X, s, z, Ys, n0, n, mode, out, p, static_cast<int *>(ws), wsb,
+                wsb + p.cnt_bytes,
+                static_cast<char *>(ws) + tl_internal::scratch_offset(ws_bytes, p.back));
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -1308,6 +1710,87 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
     const cudaError_t le = cudaLaunchKernelEx(&cfg, kernel_for(mode, padded_tokens(n)), a);
     if (le != cudaSuccess) return TL_ERR_CUDA;
+    return TL_OK;
+}
+
+
+// ------------------------------------------------------------------ chains (host)
+constexpr uint32_t kChainMagic = 0x544C4348u;   // "TLCH"
+constexpr size_t kChainHead = 256;              // image bytes before the steps
+constexpr int kChainLookahead = 3;              // steps prefetched into L2 ahead of use
+
+// The image's first bytes: the device-side header, then what tl_chain_run
+// reads on the host.
+struct ChainHostHead {
+    ChainHeader hdr;
+    uint32_t magic;
+    int32_t grid, smem, nt, mode, total;
+};
+static_assert(sizeof(ChainHostHead) <= kChainHead, "chain head");
+static_assert(sizeof(GroupArgs) % 4 == 0, "steps are copied as words");
+
+// Workspace of a chain: status word, per-step counters, the row-tile
+// counters and exchange slots every linear step shares (all zero between
+// launches), then scratch: split-K pieces and, in mode B, the quantised
+// activations of the current step.
+struct ChainLayout {
+    size_t steps_off, cnt_off, xslot_off, part_off, q_off, s_off, z_off, bytes, front;
+    int kwr, rowsr, grid, total;
+};
+
+tl_status chain_layout(const tl_chain_step *st, int nsteps, int N, int mode, int sms,
+                       ChainLayout *L) {
+    using tl_internal::round256;
+    size_t cnt_b = 0, xslot_b = 0, part_b = 0;
+    int kmax = 0;
+    L->kwr = 1;
+    L->rowsr = 1;
+    L->grid = 1;
+    for (int i = 0; i < nsteps; ++i) {
+        int Ms[TL_MAX_GROUP];
+        for (int g = 0; g < st[i].G; ++g) Ms[g] = st[i].Ws[g].M;
+        Plan p;
+        const tl_status ps = make_plan(Ms, st[i].G, st[i].Ws[0].K, N, sms, &p);
+        if (ps != TL_OK) return ps;
+        cnt_b = std::max(cnt_b, p.cnt_bytes);
+        if (p.NS == 1) xslot_b = std::max(xslot_b, round256((size_t)p.R * N * 16 * 8));
+        part_b = std::max(part_b, round256(p.back));
+        L->kwr = std::max(L->kwr, p.KW);
+        L->rowsr = std::max(L->rowsr, p.rows);
+        L->grid = std::max(L->grid, p.P);
+        kmax = std::max(kmax, st[i].Ws[0].K);
+        if (mode == TL_MODE_I8)
+            L->grid = std::max(L->grid, (int)ceil_div(st[i].Ws[0].K, kQChunk) * N);
+    }
+    L->total = mode == TL_MODE_I8 ? 2 * nsteps : nsteps;
+    L->steps_off = tl_internal::kStatusBytes;
+    L->cnt_off = L->steps_off + round256((size_t)L->total * 4);
+    L->xslot_off = L->cnt_off + cnt_b;
+    L->front = L->xslot_off + xslot_b;
+    L->part_off = L->front;
+    L->q_off = L->part_off + part_b;
+    L->s_off = L->q_off + (mode == TL_MODE_I8 ? round256((size_t)N * kmax) : 0);
+    L->z_off = L->s_off + (mode == TL_MODE_I8 ? 256 : 0);
+    L->bytes = L->z_off + (mode == TL_MODE_I8 ? 256 : 0);
+    return TL_OK;
+}
+
+tl_status check_chain(const tl_chain_step *st, int nsteps, int N, int mode, int out) {
+    if (!st) return TL_ERR_NULL;
+    if (nsteps < 1 || nsteps > TL_MAX_CHAIN || N < 1 || N > kNMax) return TL_ERR_SHAPE;
+    if (mode != TL_MODE_BF16 && mode != TL_MODE_I8) return TL_ERR_MODE;
+    if (out != TL_OUT_F32 && out != TL_OUT_BF16 && out != TL_OUT_I32_RAW) return TL_ERR_MODE;
+    if (out == TL_OUT_I32_RAW && mode != TL_MODE_I8) return TL_ERR_MODE;
+    for (int i = 0; i < nsteps; ++i) {
+        const tl_status ws = check_weights(st[i].Ws, st[i].G, mode);
+        if (ws != TL_OK) return ws;
+        if (!st[i].X || !st[i].Ys) return TL_ERR_NULL;
+        if (!aligned(st[i].X, 2)) return TL_ERR_ALIGN;
+        for (int g = 0; g < st[i].G; ++g) {
+            if (!st[i].Ys[g]) return TL_ERR_NULL;
+            if (!aligned(st[i].Ys[g], out == TL_OUT_BF16 ? 2 : 4)) return TL_ERR_ALIGN;
+        }
+    }
     return TL_OK;
 }
 
@@ -1387,9 +1870,23 @@ tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, float *s,
     DeviceInfo *dev = nullptr;
     const tl_status st = device_info(&dev);
     if (st != TL_OK) return st;
-    tl_quant_kernel<<<N, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(X_bf16), K, Q, s, z, symmetric ? 1 : 0);
-    return cudaGetLastError() == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+    if (N > 65535) return TL_ERR_SHAPE;
+    // 16-byte rows: vector loads of X and 8-byte stores of Q
+    const int vec = aligned(X_bf16, 16) && aligned(Q, 8) && (K % 8) == 0;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((K + kQChunk - 1) / kQChunk), (unsigned)N);
+    cfg.blockDim = dim3(kQThreads);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, tl_quant_kernel,
+                                              static_cast<const uint16_t *>(X_bf16), K, vec, Q, s, z,
+                                              symmetric ? 1 : 0);
+    return le == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }
 
 tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float *s,
@@ -1429,6 +1926,130 @@ tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float
         if (st != TL_OK) return st;
     }
     return TL_OK;
+}
+
+size_t tl_chain_image_bytes(int nsteps, int mode) {
+    if (nsteps < 1 || nsteps > TL_MAX_CHAIN) return 0;
+    const size_t total = mode == TL_MODE_I8 ? 2 * (size_t)nsteps : (size_t)nsteps;
+    return kChainHead + total * sizeof(GroupArgs);
+}
+
+size_t tl_chain_workspace_bytes(const tl_chain_step *steps, int nsteps, int N, int mode) {
+    if (check_chain(steps, nsteps, N, mode, TL_OUT_F32) != TL_OK) return 0;
+    DeviceInfo *dev = nullptr;
+    int sms = 148;
+    if (device_info(&dev) == TL_OK) sms = dev->sms;
+    ChainLayout L;
+    if (chain_layout(steps, nsteps, N, mode, sms, &L) != TL_OK) return 0;
+    return L.bytes;
+}
+
+tl_status tl_chain_encode(const tl_chain_step *steps, int nsteps, int N, int mode, int out_dtype,
+                          const unsigned *gate, long long wait_limit, void *workspace,
+                          size_t workspace_bytes, void *image, size_t image_bytes) {
+    tl_status st = check_chain(steps, nsteps, N, mode, out_dtype);
+    if (st != TL_OK) return st;
+    if (!image) return TL_ERR_NULL;
+    if (image_bytes < tl_chain_image_bytes(nsteps, mode)) return TL_ERR_SHAPE;
+    if (!workspace) return TL_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TL_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != TL_OK) return st;
+    ChainLayout L;
+    st = chain_layout(steps, nsteps, N, mode, dev->sms, &L);
+    if (st != TL_OK) return st;
+    if (workspace_bytes < L.bytes) return TL_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    char *img = static_cast<char *>(image);
+    std::memset(img, 0, tl_chain_image_bytes(nsteps, mode));
+    GroupArgs *sa = reinterpret_cast<GroupArgs *>(img + kChainHead);
+    int8_t *Q = reinterpret_cast<int8_t *>(ws + L.q_off);
+    float *qs = reinterpret_cast<float *>(ws + L.s_off);
+    int32_t *qz = reinterpret_cast<int32_t *>(ws + L.z_off);
+    int k = 0;
+    for (int i = 0; i < nsteps; ++i) {
+        const tl_chain_step &c = steps[i];
+        const int K = c.Ws[0].K;
+        int Ms[TL_MAX_GROUP];
+        for (int g = 0; g < c.G; ++g) Ms[g] = c.Ws[g].M;
+        Plan p;
+        st = make_plan(Ms, c.G, K, N, dev->sms, &p);
+        if (st != TL_OK) return st;
+        const void *X = c.X;
+        if (mode == TL_MODE_I8) {
+            // the step's activations, quantised per token by the chain itself
+            GroupArgs &q = sa[k++];
+            std::memset(&q, 0, sizeof q);
+            q.kind = kStepQuant;
+            q.K = K;
+            q.N = N;
+            q.X = c.X;
+            q.xvec = aligned(c.X, 16) && (K % 8) == 0;
+            q.qout = Q;
+            q.sout = qs;
+            q.zout = qz;
+            q.P = (int)ceil_div(K, kQChunk) * N;
+            q.status = reinterpret_cast<int *>(ws);
+            X = Q;
+        }
+        GroupArgs &a = sa[k++];
+        fill_linear(a, c.Ws, c.G, X, mode == TL_MODE_I8 ? qs : nullptr,
+                    mode == TL_MODE_I8 ? qz : nullptr, c.Ys, 0, N, mode, out_dtype, p,
+                    reinterpret_cast<int *>(ws), ws + L.cnt_off, ws + L.xslot_off,
+                    ws + L.part_off);
+    }
+    for (int i = 0; i < L.total; ++i) {
+        sa[i].kwr = L.kwr;
+        sa[i].rowsr = L.rowsr;
+    }
+    const int nt = padded_tokens(N);
+    const size_t smem = dyn_smem(nt, L.kwr, L.rowsr);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chain_kernel_for(mode, nt), kThreads,
+                                                      smem) != cudaSuccess)
+        return TL_ERR_CUDA;
+    if ((long long)per_sm * dev->sms < L.grid) return TL_ERR_UNSUPPORTED;
+    ChainHostHead &h = *reinterpret_cast<ChainHostHead *>(img);
+    h.hdr.cnt = reinterpret_cast<unsigned *>(ws + L.steps_off);
+    h.hdr.gate = gate;
+    h.hdr.wait_limit = wait_limit > 0 ? wait_limit : kWaitLimit;
+    h.hdr.nsteps = L.total;
+    h.hdr.lookahead = kChainLookahead;
+    h.magic = kChainMagic;
+    h.grid = L.grid;
+    h.smem = (int32_t)smem;
+    h.nt = nt;
+    h.mode = mode;
+    h.total = L.total;
+    return TL_OK;
+}
+
+tl_status tl_chain_run(const void *image, const void *image_device, void *stream) {
+    if (!image || !image_device) return TL_ERR_NULL;
+    if (!aligned(image_device, 16)) return TL_ERR_ALIGN;
+    ChainHostHead h;
+    std::memcpy(&h, image, sizeof h);
+    if (h.magic != kChainMagic) return TL_ERR_BAD_VALUE;
+    DeviceInfo *dev = nullptr;
+    const tl_status st = device_info(&dev);
+    if (st != TL_OK) return st;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)h.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)h.smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once, or no launch
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const char *dimg = static_cast<const char *>(image_device);
+    const cudaError_t le = cudaLaunchKernelEx(
+        &cfg, chain_kernel_for(h.mode, h.nt), reinterpret_cast<const ChainHeader *>(dimg),
+        reinterpret_cast<const GroupArgs *>(dimg + kChainHead));
+    return le == cudaSuccess ? TL_OK : TL_ERR_CUDA;
 }
 
 tl_status tl_linear(const tl_weight *W, const void *X, const float *s, const int32_t *z, void *Y,

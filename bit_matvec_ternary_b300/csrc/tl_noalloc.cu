@@ -11,34 +11,24 @@
 //
 // The array is a file-scope __device__ variable, so every GPU that loads
 // this library holds TL_NOALLOC_SCRATCH_BYTES of it until the process
-// exits.  Host code cannot use its name as a device address; the first call
-// on each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it.  That first call should therefore come
-// before any stream capture.
+// exits.  Host code cannot use its name as a device address: every call
+// looks the address up with cudaGetSymbolAddress in the current context (a
+// __device__ symbol has its own address in each context), with that device
+// current.  The first call in a context also loads the module there, so it
+// should come before any stream capture.
 #include "tl.h"
 #include "tl_internal.cuh"
 
 #include <cuda_runtime.h>
 
-#include <atomic>
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 __device__ __align__(256) unsigned char g_scratch[TL_NOALLOC_SCRATCH_BYTES];
 
-std::atomic<void *> g_scratch_addr[kMaxDevices];
-
 tl_status scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return TL_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return TL_ERR_UNSUPPORTED;
-    void *p = g_scratch_addr[dev].load();
-    if (!p) {
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return TL_ERR_CUDA;
-        g_scratch_addr[dev].store(p);
-    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return TL_ERR_CUDA;
     *out = p;
     return TL_OK;
 }

@@ -141,6 +141,17 @@ class LinearStack:
                                        out_dtype=self.out_dtype, workspace=self.workspace,
                                        flags=flags, stream=stream)
 
+    def chain(self, gate=None, wait_limit: int = 0) -> "tl.Chain":
+        """The whole pass as one chain: every launch group of every layer, in
+        dependency order, run by one persistent launch (mode B quantises each
+        group's bf16 input inside the chain)."""
+        if getattr(self, "_chain", None) is None:
+            steps = [([self.weights[l][p] for p in grp], self.X[l][gi], self.Y[l][gi])
+                     for l in range(self.layers) for gi, grp in enumerate(GROUPS)]
+            self._chain = tl.Chain(steps, self.N, self.mode, self.out_dtype, gate=gate,
+                                   wait_limit=wait_limit, device=self.device)
+        return self._chain
+
     def capture(self, flags: int = tl.TL_FLAG_PDL):
         """Record one pass as a CUDA graph (kernels launched by the C ABI)."""
         torch = self.torch

@@ -35,13 +35,21 @@ TL_MAX_GROUP = 4
 # Every symbol include/tl.h declares.
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
            "tl_decode_plan", "tl_quantize_act", "tl_linear", "tl_linear_group",
-           "tl_linear_noalloc", "tl_status_string", "tl_version")
+           "tl_chain_image_bytes", "tl_chain_workspace_bytes", "tl_chain_encode",
+           "tl_chain_run", "tl_linear_noalloc", "tl_status_string", "tl_version")
+TL_MAX_CHAIN = 4096
+TL_DEVERR_TIMEOUT = 1
 TL_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class tl_weight(C.Structure):
     _fields_ = [("packed", C.c_void_p), ("scale", C.c_void_p), ("rowsum", C.c_void_p),
                 ("M", C.c_int32), ("K", C.c_int32), ("layout", C.c_uint32)]
+
+
+class tl_chain_step(C.Structure):
+    _fields_ = [("Ws", C.POINTER(tl_weight)), ("G", C.c_int), ("X", C.c_void_p),
+                ("Ys", C.POINTER(C.c_void_p))]
 
 
 _p, _i64, _int, _sz = C.c_void_p, C.c_int64, C.c_int, C.c_size_t
@@ -63,6 +71,15 @@ _lib.tl_linear.restype = _int
 _lib.tl_linear_group.argtypes = [C.POINTER(tl_weight), _int, _p, _p, _p, C.POINTER(_p), _int,
                                  _int, _int, _p, _sz, C.c_uint, _p]
 _lib.tl_linear_group.restype = _int
+_lib.tl_chain_image_bytes.argtypes = [_int, _int]
+_lib.tl_chain_image_bytes.restype = _sz
+_lib.tl_chain_workspace_bytes.argtypes = [C.POINTER(tl_chain_step), _int, _int, _int]
+_lib.tl_chain_workspace_bytes.restype = _sz
+_lib.tl_chain_encode.argtypes = [C.POINTER(tl_chain_step), _int, _int, _int, _int, _p,
+                                 C.c_longlong, _p, _sz, _p, _sz]
+_lib.tl_chain_encode.restype = _int
+_lib.tl_chain_run.argtypes = [_p, _p, _p]
+_lib.tl_chain_run.restype = _int
 _lib.tl_linear_noalloc.argtypes = [C.POINTER(tl_weight), _p, _p, _p, _p, _int, _int, _int,
                                    C.c_uint, _p]
 _lib.tl_linear_noalloc.restype = _int
@@ -274,6 +291,51 @@ def tl_linear_noalloc(weight, X, s=None, z=None, out=None, mode: int = TL_MODE_B
                                 out_dtype, flags, _stream_ptr(stream))
     _check(st, "tl_linear_noalloc")
     return out
+
+
+class Chain:
+    """A chain of (grouped) linears run by one persistent launch per pass.
+
+    ``steps`` is a list of (weights, X, outs): the TernaryWeight objects of a
+    group that reads the bf16 tensor X [N, K], and its output tensors.  A
+    step's X may be an earlier step's output.  Encodes the chain on the host,
+    keeps the image on the device and owns the chain's zero-filled workspace.
+    """
+
+    def __init__(self, steps, N: int, mode: int = TL_MODE_BF16, out_dtype: int = TL_OUT_F32,
+                 gate=None, wait_limit: int = 0, device="cuda"):
+        torch = _torch()
+        self.N, self.mode, self.out_dtype = N, mode, out_dtype
+        self._keep = []
+        arr = (tl_chain_step * len(steps))()
+        for i, (ws, X, outs) in enumerate(steps):
+            ws = list(ws)
+            wa = _structs(ws)
+            ya = (C.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
+            self._keep += [wa, ya, X, outs, ws]
+            arr[i] = tl_chain_step(wa, len(ws), X.data_ptr(), ya)
+        self._steps = arr
+        self.nsteps = len(steps)
+        need = int(_lib.tl_chain_workspace_bytes(arr, len(steps), N, mode))
+        if need == 0:
+            raise TLError(TL_ERR_SHAPE, "tl_chain_workspace_bytes")
+        self.workspace = torch.zeros(need, dtype=torch.uint8, device=device)
+        nimg = int(_lib.tl_chain_image_bytes(len(steps), mode))
+        self.image = np.zeros(nimg, dtype=np.uint8)
+        self.gate = gate
+        st = _lib.tl_chain_encode(arr, len(steps), N, mode, out_dtype,
+                                  None if gate is None else gate.data_ptr(), int(wait_limit),
+                                  self.workspace.data_ptr(), need, _np_ptr(self.image), nimg)
+        _check(st, "tl_chain_encode")
+        self.image_dev = torch.from_numpy(self.image).to(device)
+
+    def run(self, stream=None) -> None:
+        _check(_lib.tl_chain_run(_np_ptr(self.image), self.image_dev.data_ptr(),
+                                 _stream_ptr(stream)), "tl_chain_run")
+
+    def status(self) -> int:
+        """The device status word (0: every wait of the last pass succeeded)."""
+        return int(self.workspace[:4].view(_torch().int32).item())
 
 
 def raw_call(name: str):

@@ -186,6 +186,66 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
                           int out_dtype, void *workspace, size_t workspace_bytes,
                           unsigned flags, void *stream);
 
+/* ---------------------------------------------------------------- chains
+ * A decoder runs its projections one after another, each reading what the
+ * previous layer produced: per layer [q, k, v] -> o -> [gate, up] -> down
+ * ("Neutrino-1 8B" model page, "Architecture": seven linears per layer, 36
+ * layers), and single-stream decode is bound by the bytes it streams per
+ * token (blog, "Serving it: the Neutrino Engine").  A chain runs such a
+ * sequence of (grouped) linears in ONE persistent, cooperative launch: step
+ * i reads its X only after every CTA has finished step i - 1 (so X may be
+ * what step i - 1 wrote), while the weights of later steps keep streaming
+ * into shared memory and L2 during that wait.  Each step computes exactly
+ * what tl_linear_group computes for the same arguments (bit for bit: same
+ * work split, same summation order).  In mode B the chain quantises each
+ * step's bf16 X itself, per token and asymmetrically, exactly as
+ * tl_quantize_act(symmetric = 0), into its workspace.
+ *
+ * Use: tl_chain_encode builds a host image (tl_chain_image_bytes bytes) that
+ * names every pointer of the chain; the caller copies it to device memory
+ * (16-byte aligned) once and calls tl_chain_run(host image, device image,
+ * stream) for every pass.  The workspace (tl_chain_workspace_bytes,
+ * 256-byte aligned, zero-filled before first use) belongs to that chain: it
+ * holds the status word (its first int32), per-step counters and split-K
+ * state, all zero again after each completed pass, and scratch.  Passes of
+ * one chain must not overlap on the GPU.
+ * Errors on the device: a wait for a step's inputs gives up after
+ * wait_limit SM cycles (0: about a second) and writes a non-zero status
+ * word; the other CTAs then stop too.  Read the word after the stream has
+ * passed the run; if it is non-zero the outputs are invalid (treat it as
+ * TL_ERR_TIMEOUT) and the workspace must be zero-filled again. */
+#define TL_MAX_CHAIN 4096
+
+typedef struct {
+    const tl_weight *Ws;   /* host array of G matrices that read X (device pointers inside) */
+    int G;                 /* 1..TL_MAX_GROUP; every Ws[g].K equal */
+    const void *X;         /* device bf16 [N][K] (2-byte aligned; 16-byte for vector loads) */
+    void *const *Ys;       /* host array of G device outputs [N][Ws[g].M], out_dtype */
+} tl_chain_step;
+
+/* Bytes of the image of a chain of nsteps linear steps (0 if out of range). */
+TL_API size_t tl_chain_image_bytes(int nsteps, int mode);
+
+/* Device workspace a chain needs (0 for invalid arguments). */
+TL_API size_t tl_chain_workspace_bytes(const tl_chain_step *steps, int nsteps, int N, int mode);
+
+/* HOST.  Encode a chain of nsteps steps at batch 1 <= N <= 8 into `image`
+ * (host memory, >= tl_chain_image_bytes bytes).  mode, out_dtype as for
+ * tl_linear (mode B: steps read bf16 X, which the chain quantises).
+ * gate: NULL, or a device word that step 0 waits on (bounded) until it is
+ * non-zero -- a producer outside the chain can hold the chain back with it.
+ * wait_limit: SM cycles before a wait for inputs gives up (0: default).
+ * Checks every argument, and that all of the launch's CTAs can be resident
+ * at once (else TL_ERR_UNSUPPORTED); launches nothing. */
+TL_API tl_status tl_chain_encode(const tl_chain_step *steps, int nsteps, int N, int mode,
+                                 int out_dtype, const unsigned *gate, long long wait_limit,
+                                 void *workspace, size_t workspace_bytes, void *image,
+                                 size_t image_bytes);
+
+/* DEVICE.  One pass of an encoded chain: `image` is the host image (read for
+ * the launch shape), `image_device` its copy in device memory. */
+TL_API tl_status tl_chain_run(const void *image, const void *image_device, void *stream);
+
 /* Size of the library's fixed scratch array for tl_linear_noalloc (4 MiB):
  * enough for every 8B-shaped matrix at up to 8 tokens per chunk, and for
  * matrices of up to 32,496 rows at K <= 4096 (10,912 rows at K = 12288). */
@@ -208,12 +268,18 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *     routine.  Each call clears the array's status word, counters and slots with
  *     cudaMemsetAsync on `stream` before its launches.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress, with that device current).  The first call in a
+ *     context also loads the library's kernels there; make it before any
+ *     stream capture.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and give wrong results; serialise
- *     them on one stream. */
+ *     them on one stream.
+ *   - A bounded device-side wait that gives up (see tl_workspace_bytes)
+ *     writes its status word into the library's array, which the caller
+ *     cannot read, and the next call's clearing erases it: a timeout on this
+ *     entry point is not reported.  Callers that must detect one use
+ *     tl_linear with a workspace they own. */
 TL_API tl_status tl_linear_noalloc(const tl_weight *W, const void *X, const float *s,
                                    const int32_t *z, void *Y, int N, int mode, int out_dtype,
                                    unsigned flags, void *stream);

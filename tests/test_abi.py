@@ -145,3 +145,28 @@ def test_workspace_query_without_device_is_well_defined():
     n8 = tl.raw_call("tl_workspace_bytes")(arr, 1, 8)
     assert 0 < n1 <= n8
     assert tl.raw_call("tl_workspace_bytes")(arr, 0, 1) == 0
+
+
+def test_chain_arguments_checked_without_a_gpu():
+    """The chain entry points reject bad arguments before touching a device."""
+    assert tl._lib.tl_chain_image_bytes(0, tl.TL_MODE_BF16) == 0
+    assert tl._lib.tl_chain_image_bytes(tl.TL_MAX_CHAIN + 1, tl.TL_MODE_BF16) == 0
+    one = tl._lib.tl_chain_image_bytes(1, tl.TL_MODE_BF16)
+    assert tl._lib.tl_chain_image_bytes(2, tl.TL_MODE_BF16) > one
+    assert tl._lib.tl_chain_image_bytes(1, tl.TL_MODE_I8) > one   # a quantiser step per linear
+    w = tl.tl_weight(0x1000, 0x2000, 0x3000, 64, 128, tl.TL_LAYOUT_TL2P_V2)
+    wa = (tl.tl_weight * 1)(w)
+    ya = (C.c_void_p * 1)(0x8000)
+    steps = (tl.tl_chain_step * 1)(tl.tl_chain_step(wa, 1, 0x4000, ya))
+    img = np.zeros(one, dtype=np.uint8)
+    enc = tl._lib.tl_chain_encode
+    args = lambda N, mode, out: (steps, 1, N, mode, out, None, 0, 0x100000, 1 << 20,
+                                 img.ctypes.data_as(C.c_void_p), img.size)
+    assert enc(*args(9, tl.TL_MODE_BF16, tl.TL_OUT_F32)) == tl.TL_ERR_SHAPE
+    assert enc(*args(0, tl.TL_MODE_BF16, tl.TL_OUT_F32)) == tl.TL_ERR_SHAPE
+    assert enc(*args(1, 7, tl.TL_OUT_F32)) == tl.TL_ERR_MODE
+    assert enc(*args(1, tl.TL_MODE_BF16, tl.TL_OUT_I32_RAW)) == tl.TL_ERR_MODE
+    assert enc(None, 1, 1, 0, 0, None, 0, 0x100000, 1 << 20,
+               img.ctypes.data_as(C.c_void_p), img.size) == tl.TL_ERR_NULL
+    # an image that was never encoded is refused before any launch
+    assert tl._lib.tl_chain_run(img.ctypes.data_as(C.c_void_p), 0x10000, None) == tl.TL_ERR_BAD_VALUE

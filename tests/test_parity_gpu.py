@@ -127,12 +127,24 @@ def test_quantizer_bit_exact(oracle_mod, K, symmetric):
     X[3] = 0                                # an all-zero token
     if K > 5:
         X[5, :] = synth.to_bf16_bits(-np.abs(synth.bf16_bits_to_f32(X[5])))  # all <= 0
+    if K >= 8:
+        # exact ties of x / s (s = 1): the rounding must go to even
+        X[6] = 0
+        X[6, :6] = synth.to_bf16_bits(np.float32([255.0, 2.5, 0.5, 1.5, 3.5, -4.5]))
+        X[7] = 0
+        X[7, :7] = synth.to_bf16_bits(np.float32([127.0, 2.5, -2.5, 0.5, -0.5, 1.5, -1.5]))
     Qr, sr, zr = oracle_mod.quant(X, symmetric=symmetric)
     Q, s, z = tl.tl_quantize_act(bf16_tensor(X), symmetric=symmetric)
     torch.cuda.synchronize()
     assert np.array_equal(Q.cpu().numpy(), Qr)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), sr.view(np.uint32))
     assert np.array_equal(z.cpu().numpy(), zr)
+    # the same rows from a pointer that is not 16-byte aligned (scalar loads)
+    flat = bf16_tensor(np.concatenate([np.zeros(1, np.uint16), X.reshape(-1)]))[1:].view(8, K)
+    Q2, s2, z2 = tl.tl_quantize_act(flat, symmetric=symmetric)
+    torch.cuda.synchronize()
+    assert np.array_equal(Q2.cpu().numpy(), Qr)
+    assert np.array_equal(s2.cpu().numpy().view(np.uint32), sr.view(np.uint32))
 
 
 @pytest.mark.parametrize("mode", [tl.TL_MODE_BF16, tl.TL_MODE_I8])
@@ -403,3 +415,119 @@ def test_prefill_group_and_workspace_shared_with_decode(oracle_mod, Ms):
             assert np.array_equal(y.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
             ref8 = oracle_mod.linear_a(m.P, m.scale, m.M, m.K, X8)
             assert rel_err(yd.cpu().numpy(), ref8) <= TOL_A
+
+
+# ---------------------------------------------------------------- inputs of one sign
+# The mode-A kernel sums (1 - w) x with the tensor cores and removes sum x;
+# activations of one sign are where the rounding of those partial sums is
+# largest compared with the result, so they are checked on their own.
+
+def _one_signed(N, K, kind, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "abs_normal":
+        x = np.abs(rng.standard_normal((N, K)))
+    elif kind == "lognormal":
+        x = rng.lognormal(0.0, 1.5, size=(N, K))
+    else:                                      # all negative, SwiGLU-like tail
+        x = -np.abs(rng.standard_normal((N, K))) * 0.3
+    return synth.to_bf16_bits(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("kind", ["abs_normal", "lognormal", "negative"])
+@pytest.mark.parametrize("K", [4096, 12288])
+@pytest.mark.parametrize("N", [1, 8])
+def test_mode_a_one_signed_activations(oracle_mod, kind, K, N):
+    M = 2048
+    m = Mat(oracle_mod, M, K, seed=K + N)
+    X = _one_signed(N, K, kind, seed=K * 3 + N)
+    ref = oracle_mod.linear_a_mt(m.P, m.scale, M, K, X)
+    Y = tl.tl_linear(m.dev, bf16_tensor(X)).cpu().numpy()
+    assert rel_err(Y, ref) <= TOL_A
+
+
+# ---------------------------------------------------------------- the groups the bench runs
+
+def _stack_group(oracle_mod, names, seed):
+    shp = synth.NEUTRINO_8B.linear_shapes()
+    return [Mat(oracle_mod, shp[p][0], shp[p][1], seed=seed + i,
+                p0=synth.zero_fraction(synth.NEUTRINO_8B, 2, p)) for i, p in enumerate(names)]
+
+
+@pytest.mark.parametrize("names", [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)])
+@pytest.mark.parametrize("N", [1, 8])
+def test_bench_launch_groups_against_oracle(oracle_mod, names, N):
+    """The four launches of an 8B layer at the batch sizes the bench times,
+    in both modes, as one grouped call each (mode B bit for bit)."""
+    mats = _stack_group(oracle_mod, names, seed=500 + 10 * N)
+    K = mats[0].K
+    X = synth.activations(N, K, seed=501 + N, outlier_frac=0.01 if N == 8 else 0.0)
+    xd = bf16_tensor(X)
+    ys = tl.tl_linear_group([m.dev for m in mats], xd, flags=tl.TL_FLAG_PDL)
+    Q, s, z = tl.tl_quantize_act(xd)
+    yb = tl.tl_linear_group([m.dev for m in mats], Q, s, z, mode=tl.TL_MODE_I8)
+    torch.cuda.synchronize()
+    Qr, sr, zr = oracle_mod.quant(X)
+    assert np.array_equal(Q.cpu().numpy(), Qr)
+    for m, y, y8 in zip(mats, ys, yb):
+        ref = oracle_mod.linear_a_mt(m.P, m.scale, m.M, m.K, X)
+        assert rel_err(y.cpu().numpy(), ref) <= TOL_A
+        refb = oracle_mod.linear_b_mt(m.P, m.scale, m.rowsum, m.M, m.K, Qr, sr, zr)
+        assert np.array_equal(y8.cpu().numpy().view(np.uint32), refb.view(np.uint32))
+
+
+# ---------------------------------------------------------------- dependent launches
+
+@pytest.mark.parametrize("mode", [tl.TL_MODE_BF16, tl.TL_MODE_I8])
+@pytest.mark.parametrize("N", [1, 8])
+def test_chained_pdl_launches_in_a_graph(oracle_mod, mode, N):
+    """Eight 4096 x 4096 linears, each reading the bf16 output the previous
+    one wrote, launched with the programmatic-dependent flag and replayed
+    from a CUDA graph.  Every output is checked against the oracle applied to
+    the GPU's own previous output, so a launch that read its input before the
+    previous one finished writing it would show."""
+    L, K = 8, 4096
+    mats = [Mat(oracle_mod, K, K, seed=600 + i) for i in range(L)]
+    x0 = synth.activations(N, K, seed=601)
+    xs = [bf16_tensor(x0)] + [torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+                              for _ in range(L)]
+    qs = [(torch.empty((N, K), dtype=torch.int8, device="cuda"),
+           torch.empty(N, dtype=torch.float32, device="cuda"),
+           torch.empty(N, dtype=torch.int32, device="cuda")) for _ in range(L)]
+    ws = tl.make_workspace([[m.dev] for m in mats], N)
+
+    def run():
+        for i, m in enumerate(mats):
+            if mode == tl.TL_MODE_I8:
+                q, s, z = qs[i]
+                tl.tl_quantize_act(xs[i], Q=q, s=s, z=z)
+                tl.tl_linear(m.dev, q, s, z, out=xs[i + 1], mode=mode, out_dtype=tl.TL_OUT_BF16,
+                             workspace=ws, flags=tl.TL_FLAG_PDL)
+            else:
+                tl.tl_linear(m.dev, xs[i], out=xs[i + 1], out_dtype=tl.TL_OUT_BF16,
+                             workspace=ws, flags=tl.TL_FLAG_PDL)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for rep in range(2):
+        for t in xs[1:]:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for i, m in enumerate(mats):
+            xin = xs[i].cpu().view(torch.int16).numpy().view(np.uint16)
+            got = xs[i + 1].cpu().view(torch.int16).numpy().view(np.uint16)
+            if mode == tl.TL_MODE_I8:
+                Qr, sr, zr = oracle_mod.quant(xin)
+                refb = oracle_mod.linear_b_mt(m.P, m.scale, m.rowsum, K, K, Qr, sr, zr)
+                assert np.array_equal(got, oracle_mod.bf16_rne(refb)), (rep, i)
+            else:
+                ref = oracle_mod.linear_a_mt(m.P, m.scale, K, K, xin)
+                y = synth.bf16_bits_to_f32(got)
+                assert rel_err(y, ref) <= TOL_A + 2.0 ** -8, (rep, i)

@@ -66,6 +66,42 @@ def test_noalloc_matches_workspace_entry_point_twice(M, K, N):
         assert torch.equal(yb.view(torch.int32), ref_b.view(torch.int32))
 
 
+@pytest.fixture(scope="module")
+def oracle_mod():
+    from oracle import oracle
+    oracle.lib()
+    return oracle
+
+
+def test_noalloc_against_the_oracle(oracle_mod):
+    """The same entry point against the CPU oracle: batches above eight
+    (the array reused by successive 8-token chunks), a prefill-sized batch
+    (which this entry point runs on the decode kernel), and a small matrix
+    right after a large one, so that each call starts from what the previous
+    call of another shape left in the array."""
+    cases = [(12288, 4096, 8), (64, 256, 2), (4096, 12288, 13), (1024, 4096, 300),
+             (33, 4099, 1)]
+    for M, K, N in cases:
+        W = synth.ternary(M, K, 0.626, 7 * M + K)
+        scale = synth.scales(M, 7 * M + K)
+        w = tl.TernaryWeight.from_int8(W, scale)
+        P = oracle_mod.pack(W)
+        rs = oracle_mod.rowsum(P, M, K)
+        Xh = synth.activations(N, K, seed=N + K, outlier_frac=0.01)
+        X = _bf16(Xh)
+        ya = torch.empty((N, M), dtype=torch.float32, device="cuda")
+        assert _noalloc(w, X, None, None, ya, N, tl.TL_MODE_BF16, tl.TL_OUT_F32) == tl.TL_OK
+        Q, s, z = tl.tl_quantize_act(X)
+        yb = torch.empty((N, M), dtype=torch.float32, device="cuda")
+        assert _noalloc(w, Q, s, z, yb, N, tl.TL_MODE_I8, tl.TL_OUT_F32) == tl.TL_OK
+        torch.cuda.synchronize()
+        ref = oracle_mod.linear_a_mt(P, scale, M, K, Xh)
+        assert rel_err(ya.cpu().numpy(), ref) <= TOL_A, (M, K, N)
+        Qr, sr, zr = oracle_mod.quant(Xh)
+        refb = oracle_mod.linear_b_mt(P, scale, rs, M, K, Qr, sr, zr)
+        assert np.array_equal(yb.cpu().numpy().view(np.uint32), refb.view(np.uint32)), (M, K, N)
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     # a matrix whose split-K scratch would not fit the fixed array: refused
     # with TL_ERR_WORKSPACE before anything is launched
