@@ -271,6 +271,46 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def bench_head(args, torch, tl, hbm_peak):
+    """The int8 output head (151,936 x 4,096, one scale per row) with its
+    fused argmax, at one and eight tokens; seeded synthetic table."""
+    V, D = 151_936, 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    H = torch.randint(-128, 128, (V, D), dtype=torch.int8, device="cuda", generator=g)
+    scale = torch.rand(V, device="cuda", generator=g) * 0.045 + 0.005
+    head = tl.Head(H, scale)
+    out = {}
+    from bit_matvec_ternary_b300 import synth
+    import numpy as np
+    for N in (1, 8):
+        x = synth.activations(N, D, seed=55, outlier_frac=0.01)
+        xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        Q, s, z = tl.tl_quantize_act(xt)
+        tok = torch.empty(N, dtype=torch.int32, device="cuda")
+        best = torch.empty(N, dtype=torch.float32, device="cuda")
+        stream = torch.cuda.current_stream()
+        for _ in range(args.warmup):
+            head.argmax(Q, s, z, token=tok, best=best)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            head.argmax(Q, s, z, token=tok, best=best)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        alg = V * D + 4 * V + N * D + 8 * N + 8 * N
+        out[f"n{N}"] = {"us": ms * 1e3, "algorithmic_bytes": alg,
+                        "gbs": alg / (ms / 1e3) / 1e9,
+                        "frac_of_hbm": alg / (ms / 1e3) / 1e9 / hbm_peak,
+                        "tokens_s": N / (ms / 1e3)}
+    out["shape"] = f"int8 {V}x{D}, fp32 scale per row, argmax fused, logits not written"
+    out["kernel"] = "tl_head_kernel"
+    return out
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -281,6 +321,7 @@ def main():
     ap.add_argument("--no-n8", action="store_true", help="skip the N=8 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-prefill", action="store_true", help="skip the N=512 prefill line")
+    ap.add_argument("--no-head", action="store_true", help="skip the int8 head lines")
     ap.add_argument("--layers", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -373,6 +414,10 @@ def main():
                                if mode == tl.TL_MODE_I8 else "")}
             del st8
             torch.cuda.empty_cache()
+
+    if not args.no_head:
+        extra["head_argmax"] = bench_head(args, torch, tl, hbm_peak)
+        torch.cuda.empty_cache()
 
     if not args.no_prefill:
         # prefill-sized batch: 512 tokens, int8 symmetric per-token activations,

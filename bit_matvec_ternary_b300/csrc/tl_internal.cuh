@@ -12,6 +12,20 @@
 
 namespace tl_internal {
 
+#ifdef __CUDACC__
+// rint(v / s) for the per-token quantisers, with r = 1/s rounded to nearest:
+// v * r is within three units in the last place of the IEEE quotient
+// fl(v / s), so it rounds to the same integer unless it lies that close to
+// a half-integer (or is not finite); only then is the quotient formed.
+__device__ __forceinline__ float quant_round(float v, float s, float r) {
+    const float t = __fmul_rn(v, r);
+    const float d = fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f));
+    // |t| < 512 on the fast path, so t - floor(t) is exact
+    if (d > __fmul_rn(fabsf(t), 0x1p-20f) && fabsf(t) < 512.f) return rintf(t);
+    return rintf(__fdiv_rn(v, s));
+}
+#endif
+
 // Batches from this size up run on the tensor-core prefill kernel.
 constexpr int kPrefillMinN = 256;
 // Bytes at the start of every workspace reserved for the status word.
@@ -33,6 +47,12 @@ inline size_t workspace_need(size_t front, size_t back) {
 inline size_t scratch_offset(size_t ws_bytes, size_t back) {
     return (ws_bytes - back) / 256 * 256;
 }
+
+// SM count of the current device (its attributes set up on first use).
+tl_status device_sms(int *sms);
+// Raise the head and fused kernels' shared-memory limits on the current device.
+tl_status head_init_device();
+tl_status fused_init_device();
 
 size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms);
 bool prefill_supported(int N, int K);

@@ -228,6 +228,8 @@ struct GroupArgs {
 // Header of an encoded chain (device memory), followed by its steps.
 struct ChainHeader {
     unsigned *cnt;          // [nsteps] CTAs done per step; zero between launches
+    unsigned *done;         // [nsteps] step complete (set by the CTA that completes cnt);
+                            // on other cache lines than cnt, zero between launches
     const unsigned *gate;   // when not null, step 0 waits until *gate != 0
     long long wait_limit;   // SM cycles before a wait for a step's inputs gives up
     int nsteps;
@@ -721,17 +723,19 @@ __device__ __forceinline__ void pipe_start(Pipe &p, int cta, int warp) {
     for (int k = 0; k < kSlots && p.pc_on; ++k) pipe_produce<NT>(p, k, cta, warp);
 }
 
-// Bounded wait of one thread until *word == target (or, with `nonzero`,
-// until *word != 0), with acquire semantics.  Gives up, returning false,
-// when another CTA has set the status word or after `limit` SM cycles (and
-// then sets the status word itself).
-__device__ __forceinline__ bool wait_word(const unsigned *word, unsigned target, bool nonzero,
-                                          long long limit, int *status) {
+// Bounded wait of one thread until *word != 0, then an acquire fence (the
+// polls are relaxed loads, so waiting CTAs do not order anything until the
+// word is seen).  Gives up, returning false, when another CTA has set the
+// status word or after `limit` SM cycles (and then sets the status word).
+__device__ __forceinline__ bool wait_word(const unsigned *word, long long limit, int *status) {
     const long long t0 = clock64();
     for (unsigned it = 0;; ++it) {
         unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
-        if (nonzero ? v != 0u : v == target) return true;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+        if (v != 0u) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            return true;
+        }
         if ((it & 15u) == 15u) {
             int st;
             asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(st) : "l"(status) : "memory");
@@ -741,6 +745,32 @@ __device__ __forceinline__ bool wait_word(const unsigned *word, unsigned target,
                 return false;
             }
         }
+    }
+}
+
+// Wait (thread 0) for step `step`'s inputs: the gate before step 0, else
+// step - 1's completion flag.
+__device__ __forceinline__ bool wait_inputs(const ChainHeader *ch, int step, int *status) {
+    if (step == 0) return ch->gate == nullptr || wait_word(ch->gate, ch->wait_limit, status);
+    return wait_word(ch->done + step - 1, ch->wait_limit, status);
+}
+
+// Count this CTA into step `step` (thread 0, after a barrier that follows
+// the CTA's last write of the step).  The CTA that completes the count
+// publishes the step's flag, and clears the counter and the flag of the
+// step before, which every CTA of this step has already seen (and, after
+// the last step, that step's own flag), so both are zero when the launch ends.
+__device__ __forceinline__ void signal_step(const ChainHeader *ch, int step, unsigned P) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    const unsigned n = atomicAdd(ch->cnt + step, 1u) + 1u;
+    if (n != P) return;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    ch->cnt[step] = 0u;
+    if (step > 0) ch->done[step - 1] = 0u;
+    if (step + 1 < ch->nsteps) {
+        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ch->done + step), "r"(1u) : "memory");
+    } else {
+        ch->done[step] = 0u;
     }
 }
 
@@ -761,13 +791,13 @@ struct StepSmem {
 // ------------------------------------------------------------ one linear step
 // kModeA: bf16 activations (else int8 from the quantiser).  NT: token
 // columns staged (a power of two >= N).  kChain: the step is one of a chain
-// run by one persistent launch; it waits for step - 1 (prevP CTAs) through
-// the chain's counters instead of for the previous kernel.  Returns, the
+// run by one persistent launch; it waits for step - 1's completion flag
+// instead of for the previous kernel.  Returns, the
 // same in every thread of the CTA, whether every wait succeeded.
 template <bool kModeA, int NT, bool kChain>
 __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *smem,
                                          StepSmem<NT> &sh, Pipe &pipe, const ChainHeader *ch,
-                                         int step, unsigned prevP) {
+                                         int step) {
     constexpr int CH = chunk_tiles(NT);         // tiles per bulk copy
     constexpr int SLOT = CH * 512;
     constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
@@ -848,10 +878,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
     if (!kChain) {
         griddep_wait();
     } else {
-        if (threadIdx.x == 0)
-            sh.go = step == 0 ? (ch->gate == nullptr ||
-                                 wait_word(ch->gate, 0u, true, ch->wait_limit, a.status))
-                              : wait_word(ch->cnt + step - 1, prevP, false, ch->wait_limit, a.status);
+        if (threadIdx.x == 0) sh.go = wait_inputs(ch, step, a.status);
         __syncthreads();
         if (!sh.go) return false;
     }
@@ -1250,7 +1277,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         pipe_start<NT>(pipe, blockIdx.x, warp);
         prefetch_l2<NT>(a, blockIdx.x, warp);
     }
-    const bool ok = run_step<kModeA, NT, false>(a, blockIdx.x, smem, sh, pipe, nullptr, 0, 0u);
+    const bool ok = run_step<kModeA, NT, false>(a, blockIdx.x, smem, sh, pipe, nullptr, 0);
     if (!ok && lane == 0) pipe_drain(pipe, a.status);
 }
 
@@ -1279,14 +1306,6 @@ inline int padded_tokens(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 
 // then is the IEEE division taken.
 constexpr int kQThreads = 256;
 constexpr int kQChunk = 4096;          // activations quantised per CTA
-
-__device__ __forceinline__ float quant_round(float v, float s, float r) {
-    const float t = __fmul_rn(v, r);
-    const float d = fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f));
-    // |t| <= 2^9 here when the fast path is taken, so t - floor(t) is exact
-    if (d > __fmul_rn(fabsf(t), 0x1p-20f) && fabsf(t) < 512.f) return rintf(t);
-    return rintf(__fdiv_rn(v, s));
-}
 
 // Token n, chunk c (kQThreads threads).  kLaunch: a launch of its own, which
 // waits for the previous kernel on the stream and lets the next one start.
@@ -1372,7 +1391,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     const float qlo = symmetric ? -127.f : -128.f;
     const int k1 = min(K, k0 + kQChunk);
     auto one = [&](float v) {
-        const float t = fminf(fmaxf(__fadd_rn(quant_round(v, s, r), zf), qlo), 127.f);
+        const float t = fminf(fmaxf(__fadd_rn(tl_internal::quant_round(v, s, r), zf), qlo), 127.f);
         return (uint32_t)(uint8_t)(int8_t)(int)t;
     };
     if (vec) {
@@ -1442,14 +1461,10 @@ tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict_
         __syncthreads();
         status = sa.status;
         if (cta >= sa.P) continue;
-        const unsigned prevP = step > 0 ? (unsigned)steps[step - 1].P : 0u;
         if (sa.kind == kStepLinear) {
-            ok = run_step<kModeA, NT, true>(sa, cta, smem, sh, pipe, ch, step, prevP);
+            ok = run_step<kModeA, NT, true>(sa, cta, smem, sh, pipe, ch, step);
         } else {
-            if (threadIdx.x == 0)
-                sh.go = step == 0 ? (ch->gate == nullptr ||
-                                     wait_word(ch->gate, 0u, true, ch->wait_limit, sa.status))
-                                  : wait_word(ch->cnt + step - 1, prevP, false, ch->wait_limit, sa.status);
+            if (threadIdx.x == 0) sh.go = wait_inputs(ch, step, sa.status);
             __syncthreads();
             ok = sh.go != 0;
             if (ok) {
@@ -1461,14 +1476,7 @@ tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict_
         if (!ok) break;
         // the step's results are written: count this CTA in
         __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            const unsigned done = atomicAdd(ch->cnt + step, 1u) + 1u;
-            if (done == (unsigned)sa.P) {
-                if (step > 0) atomicExch(ch->cnt + step - 1, 0u);
-                if (step == nsteps - 1) atomicExch(ch->cnt + step, 0u);
-            }
-        }
+        if (threadIdx.x == 0) signal_step(ch, step, (unsigned)sa.P);
     }
     if (!ok && lane == 0) pipe_drain(pipe, status);
 }
@@ -1522,7 +1530,11 @@ tl_status init_device(int dev, DeviceInfo &d) {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess)
                 return TL_ERR_CUDA;
-    const tl_status pst = tl_internal::prefill_init_device();
+    tl_status pst = tl_internal::prefill_init_device();
+    if (pst != TL_OK) return pst;
+    pst = tl_internal::head_init_device();
+    if (pst != TL_OK) return pst;
+    pst = tl_internal::fused_init_device();
     if (pst != TL_OK) return pst;
     d.sms = sms;
     d.init.store(1, std::memory_order_release);
@@ -1734,7 +1746,7 @@ static_assert(sizeof(GroupArgs) % 4 == 0, "steps are copied as words");
 // launches), then scratch: split-K pieces and, in mode B, the quantised
 // activations of the current step.
 struct ChainLayout {
-    size_t steps_off, cnt_off, xslot_off, part_off, q_off, s_off, z_off, bytes, front;
+    size_t steps_off, done_off, cnt_off, xslot_off, part_off, q_off, s_off, z_off, bytes, front;
     int kwr, rowsr, grid, total;
 };
 
@@ -1764,7 +1776,8 @@ tl_status chain_layout(const tl_chain_step *st, int nsteps, int N, int mode, int
     }
     L->total = mode == TL_MODE_I8 ? 2 * nsteps : nsteps;
     L->steps_off = tl_internal::kStatusBytes;
-    L->cnt_off = L->steps_off + round256((size_t)L->total * 4);
+    L->done_off = L->steps_off + round256((size_t)L->total * 4);
+    L->cnt_off = L->done_off + round256((size_t)L->total * 4);
     L->xslot_off = L->cnt_off + cnt_b;
     L->front = L->xslot_off + xslot_b;
     L->part_off = L->front;
@@ -1797,6 +1810,14 @@ tl_status check_chain(const tl_chain_step *st, int nsteps, int N, int mode, int 
 }  // namespace
 
 namespace tl_internal {
+
+tl_status device_sms(int *sms) {
+    DeviceInfo *dev = nullptr;
+    const tl_status st = device_info(&dev);
+    if (st != TL_OK) return st;
+    *sms = dev->sms;
+    return TL_OK;
+}
 
 tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t *zeroed) {
     DeviceInfo *dev = nullptr;
@@ -2012,6 +2033,7 @@ tl_status tl_chain_encode(const tl_chain_step *steps, int nsteps, int N, int mod
     if ((long long)per_sm * dev->sms < L.grid) return TL_ERR_UNSUPPORTED;
     ChainHostHead &h = *reinterpret_cast<ChainHostHead *>(img);
     h.hdr.cnt = reinterpret_cast<unsigned *>(ws + L.steps_off);
+    h.hdr.done = reinterpret_cast<unsigned *>(ws + L.done_off);
     h.hdr.gate = gate;
     h.hdr.wait_limit = wait_limit > 0 ? wait_limit : kWaitLimit;
     h.hdr.nsteps = L.total;

@@ -35,6 +35,8 @@ TL_MAX_GROUP = 4
 # Every symbol include/tl.h declares.
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
            "tl_decode_plan", "tl_quantize_act", "tl_linear", "tl_linear_group",
+           "tl_head_workspace_bytes", "tl_head_argmax", "tl_embed",
+           "tl_rmsnorm_quant", "tl_swiglu_quant",
            "tl_chain_image_bytes", "tl_chain_workspace_bytes", "tl_chain_encode",
            "tl_chain_run", "tl_linear_noalloc", "tl_status_string", "tl_version")
 TL_MAX_CHAIN = 4096
@@ -71,6 +73,17 @@ _lib.tl_linear.restype = _int
 _lib.tl_linear_group.argtypes = [C.POINTER(tl_weight), _int, _p, _p, _p, C.POINTER(_p), _int,
                                  _int, _int, _p, _sz, C.c_uint, _p]
 _lib.tl_linear_group.restype = _int
+_lib.tl_head_workspace_bytes.argtypes = [_i64, _int, _int]
+_lib.tl_head_workspace_bytes.restype = _sz
+_lib.tl_head_argmax.argtypes = [_p, _p, _i64, _int, _p, _p, _p, _int, _p, _p, _p, _p, _sz,
+                                C.c_uint, _p]
+_lib.tl_head_argmax.restype = _int
+_lib.tl_embed.argtypes = [_p, _p, _i64, _int, _p, _int, _p, _p]
+_lib.tl_embed.restype = _int
+_lib.tl_rmsnorm_quant.argtypes = [_p, _p, C.c_float, _int, _int, _p, _p, _p, _p, _int, _p]
+_lib.tl_rmsnorm_quant.restype = _int
+_lib.tl_swiglu_quant.argtypes = [_p, _p, _int, _int, _p, _p, _p, _p, _int, _p]
+_lib.tl_swiglu_quant.restype = _int
 _lib.tl_chain_image_bytes.argtypes = [_int, _int]
 _lib.tl_chain_image_bytes.restype = _sz
 _lib.tl_chain_workspace_bytes.argtypes = [C.POINTER(tl_chain_step), _int, _int, _int]
@@ -291,6 +304,95 @@ def tl_linear_noalloc(weight, X, s=None, z=None, out=None, mode: int = TL_MODE_B
                                 out_dtype, flags, _stream_ptr(stream))
     _check(st, "tl_linear_noalloc")
     return out
+
+
+def _fused_outs(N, K, device, want_y, want_q):
+    torch = _torch()
+    y = torch.empty((N, K), dtype=torch.bfloat16, device=device) if want_y else None
+    if want_q:
+        return (y, torch.empty((N, K), dtype=torch.int8, device=device),
+                torch.empty(N, dtype=torch.float32, device=device),
+                torch.empty(N, dtype=torch.int32, device=device))
+    return y, None, None, None
+
+
+def _ptr_or_none(t):
+    return None if t is None else t.data_ptr()
+
+
+def tl_rmsnorm_quant(X, gamma, eps: float = 1e-6, want_y: bool = True, want_q: bool = True,
+                     symmetric: bool = False, stream=None):
+    """RMSNorm of bf16 X [N, K] -> (bf16 Y or None, int8 Q, s, z or Nones)."""
+    N, K = X.shape
+    y, q, s, z = _fused_outs(N, K, X.device, want_y, want_q)
+    st = _lib.tl_rmsnorm_quant(X.data_ptr(), gamma.data_ptr(), float(eps), N, K, _ptr_or_none(y),
+                               _ptr_or_none(q), _ptr_or_none(s), _ptr_or_none(z),
+                               int(bool(symmetric)), _stream_ptr(stream))
+    _check(st, "tl_rmsnorm_quant")
+    return y, q, s, z
+
+
+def tl_swiglu_quant(G, U, want_y: bool = True, want_q: bool = True, symmetric: bool = False,
+                    stream=None):
+    """silu(G) * U of bf16 [N, M] -> (bf16 H or None, int8 Q, s, z or Nones)."""
+    N, M = G.shape
+    y, q, s, z = _fused_outs(N, M, G.device, want_y, want_q)
+    st = _lib.tl_swiglu_quant(G.data_ptr(), U.data_ptr(), N, M, _ptr_or_none(y), _ptr_or_none(q),
+                              _ptr_or_none(s), _ptr_or_none(z), int(bool(symmetric)),
+                              _stream_ptr(stream))
+    _check(st, "tl_swiglu_quant")
+    return y, q, s, z
+
+
+class Head:
+    """An int8 output head (or embedding table) resident on the device:
+    int8 [V, D] rows and one fp32 scale per row (caller-owned tensors)."""
+
+    def __init__(self, table, scale):
+        self.table, self.scale = table, scale
+        self.V, self.D = table.shape
+        self._ws = {}
+
+    @classmethod
+    def from_host(cls, H: np.ndarray, scale: np.ndarray, device="cuda") -> "Head":
+        torch = _torch()
+        return cls(torch.from_numpy(np.ascontiguousarray(H, dtype=np.int8)).to(device),
+                   torch.from_numpy(np.ascontiguousarray(scale, dtype=np.float32)).to(device))
+
+    def workspace(self, N: int):
+        if N not in self._ws:
+            need = int(_lib.tl_head_workspace_bytes(self.V, self.D, N))
+            if need == 0:
+                raise TLError(TL_ERR_SHAPE, "tl_head_workspace_bytes")
+            self._ws[N] = _torch().zeros(need, dtype=_torch().uint8, device=self.table.device)
+        return self._ws[N]
+
+    def argmax(self, Q, s, z, logits=None, token=None, best=None, flags: int = 0, stream=None):
+        """(token int32 [N], best fp32 [N]); fills `logits` [N, V] when given."""
+        torch = _torch()
+        N = Q.shape[0]
+        dev = self.table.device
+        token = torch.empty(N, dtype=torch.int32, device=dev) if token is None else token
+        best = torch.empty(N, dtype=torch.float32, device=dev) if best is None else best
+        ws = self.workspace(N)
+        st = _lib.tl_head_argmax(self.table.data_ptr(), self.scale.data_ptr(), self.V, self.D,
+                                 Q.data_ptr(), s.data_ptr(), z.data_ptr(), N,
+                                 None if logits is None else logits.data_ptr(), token.data_ptr(),
+                                 best.data_ptr(), ws.data_ptr(), ws.numel(), flags,
+                                 _stream_ptr(stream))
+        _check(st, "tl_head_argmax")
+        return token, best
+
+    def embed(self, tokens, out=None, stream=None):
+        """bf16 [N, D] rows of the table for int32 device tokens [N]."""
+        torch = _torch()
+        N = tokens.shape[0]
+        out = torch.empty((N, self.D), dtype=torch.bfloat16, device=self.table.device) \
+            if out is None else out
+        st = _lib.tl_embed(self.table.data_ptr(), self.scale.data_ptr(), self.V, self.D,
+                           tokens.data_ptr(), N, out.data_ptr(), _stream_ptr(stream))
+        _check(st, "tl_embed")
+        return out
 
 
 class Chain:

@@ -186,6 +186,63 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
                           int out_dtype, void *workspace, size_t workspace_bytes,
                           unsigned flags, void *stream);
 
+/* ---------------------------------------------------------------- int8 head and embedding
+ * The projections are ternary, but the token embedding and the output head
+ * stay int8 with one higher-precision scale per row (blog "Neutrino-1:
+ * quantization is a training decision", "What's actually ternary"; model
+ * page "Neutrino-1 8B", "Architecture": two untied int8 tensors of
+ * vocabulary x hidden, one scale per row).  Greedy decoding reads the
+ * head's argmax. */
+
+/* Device workspace for tl_head_argmax (0 for invalid shapes). */
+TL_API size_t tl_head_workspace_bytes(int64_t V, int D, int N);
+
+/* DEVICE.  Output head with a fused argmax, on activations quantised per
+ * token by tl_quantize_act (Q [N][D] int8, s, z [N]):
+ *     acc[n,v]   = sum_d H[v,d] * Q[n,d]            (exact int32)
+ *     logit[n,v] = ((float)(acc - z[n] * sum_d H[v,d]) * s[n]) * scale[v]
+ *     token[n]   = the smallest v with the largest logit; best[n] = that logit.
+ * H: int8 [V][D] row-major, 16-byte aligned; scale: fp32 [V].  Shapes:
+ * 16 <= D <= 32768, D % 16 == 0, N * D <= 98304, 1 <= N <= 8, V < 2^31 - 1.
+ * logits: fp32 [N][V] or NULL (then only token and best are written).
+ * workspace: >= tl_head_workspace_bytes(V, D, N), 256-byte aligned,
+ * zero-filled before first use; every call leaves its counter zero again.
+ * flags: 0 or TL_FLAG_PDL (as for tl_linear). */
+TL_API tl_status tl_head_argmax(const int8_t *H, const float *scale, int64_t V, int D,
+                                const int8_t *Q, const float *s, const int32_t *z, int N,
+                                float *logits, int32_t *token, float *best, void *workspace,
+                                size_t workspace_bytes, unsigned flags, void *stream);
+
+/* DEVICE.  Embedding lookup: X[n][d] = bf16(E[t][d] * scale[t]) for
+ * t = tokens[n] (the fp32 product rounded to nearest even); E int8 [V][D],
+ * scale fp32 [V], tokens int32 [N] (device), X bf16 [N][D].  A token outside
+ * [0, V) gives a zero row. */
+TL_API tl_status tl_embed(const int8_t *E, const float *scale, int64_t V, int D,
+                          const int32_t *tokens, int N, void *X_bf16, void *stream);
+
+/* ---------------------------------------------------------------- fused neighbours
+ * Each decoder layer normalises its input with RMSNorm (eps 1e-6) before the
+ * q/k/v and gate/up projections, and its feed-forward is SwiGLU ("Neutrino-1
+ * 8B" model page, "Architecture").  These two calls produce a linear's input
+ * in one pass: the op's bf16 output (Y, may be NULL when Q is given) and/or
+ * that output quantised per token (Q int8 [N][K], s, z [N]; NULL to skip),
+ * Q, s and z being bit for bit what tl_quantize_act(Y, symmetric) gives.
+ * One CTA per token row, K <= 32768.  The pages fix neither the rounding
+ * of these ops nor how their outputs are quantised; here the op is computed
+ * in fp32 (IEEE division and square root; exp from the CUDA math library),
+ * rounded once to bf16, and that bf16 row is quantised. */
+
+/* DEVICE.  y[n,k] = bf16(x[n,k] * r[n] * gamma[k]),
+ * r[n] = 1 / sqrt(sum_k x[n,k]^2 / K + eps); X bf16 [N][K], gamma bf16 [K]. */
+TL_API tl_status tl_rmsnorm_quant(const void *X, const void *gamma, float eps, int N, int K,
+                                  void *Y, int8_t *Q, float *s, int32_t *z, int symmetric,
+                                  void *stream);
+
+/* DEVICE.  h[n,m] = bf16(g / (1 + exp(-g)) * u) for the gate and up
+ * projections' outputs G, U (bf16 [N][M]). */
+TL_API tl_status tl_swiglu_quant(const void *G, const void *U, int N, int M, void *H,
+                                 int8_t *Q, float *s, int32_t *z, int symmetric, void *stream);
+
 /* ---------------------------------------------------------------- chains
  * A decoder runs its projections one after another, each reading what the
  * previous layer produced: per layer [q, k, v] -> o -> [gate, up] -> down
@@ -206,8 +263,9 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
  * (16-byte aligned) once and calls tl_chain_run(host image, device image,
  * stream) for every pass.  The workspace (tl_chain_workspace_bytes,
  * 256-byte aligned, zero-filled before first use) belongs to that chain: it
- * holds the status word (its first int32), per-step counters and split-K
- * state, all zero again after each completed pass, and scratch.  Passes of
+ * holds the status word (its first int32), per-step arrival counters and
+ * completion flags and split-K state, all zero again after each completed
+ * pass, and scratch.  Passes of
  * one chain must not overlap on the GPU.
  * Errors on the device: a wait for a step's inputs gives up after
  * wait_limit SM cycles (0: about a second) and writes a non-zero status

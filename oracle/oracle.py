@@ -46,6 +46,14 @@ def load(path: str) -> C.CDLL:
     L.oracle_linear_a_mt.restype = None
     L.oracle_linear_b_mt.argtypes = [p, p, p, i64, i64, p, p, p, i64, p, i32]
     L.oracle_linear_b_mt.restype = None
+    L.oracle_head.argtypes = [p, p, i64, i64, p, p, p, i64, p, p, p, p]
+    L.oracle_head.restype = None
+    L.oracle_embed.argtypes = [p, p, i64, i64, p, i64, p]
+    L.oracle_embed.restype = None
+    L.oracle_rmsnorm.argtypes = [p, p, C.c_double, i64, i64, p]
+    L.oracle_rmsnorm.restype = None
+    L.oracle_swiglu.argtypes = [p, p, i64, i64, p]
+    L.oracle_swiglu.restype = None
     return L
 
 
@@ -152,6 +160,50 @@ def linear_b_mt(P, scale, rsum, M: int, K: int, Q, s, z, nthreads: int | None = 
     lib().oracle_linear_b_mt(_ptr(P), _ptr(scale), _ptr(rsum), M, K, _ptr(Q), _ptr(s),
                              _ptr(z), N, _ptr(Y), nthreads or host_cores())
     return Y
+
+
+def head(H, scale, Q, s, z, return_logits: bool = True):
+    """int8 head on quantised activations: (acc int32 [N, V], logits fp32
+    [N, V], token int32 [N], best fp32 [N]); acc/logits None unless asked."""
+    H = _c(H, np.int8); scale = _c(scale, np.float32)
+    Q = _c(Q, np.int8); s = _c(s, np.float32); z = _c(z, np.int32)
+    V, D = H.shape
+    N = Q.shape[0]
+    acc = np.zeros((N, V), dtype=np.int32) if return_logits else None
+    lg = np.zeros((N, V), dtype=np.float32) if return_logits else None
+    tok = np.zeros(N, dtype=np.int32)
+    best = np.zeros(N, dtype=np.float32)
+    lib().oracle_head(_ptr(H), _ptr(scale), V, D, _ptr(Q), _ptr(s), _ptr(z), N, _ptr(acc),
+                      _ptr(lg), _ptr(tok), _ptr(best))
+    return acc, lg, tok, best
+
+
+def embed(E, scale, tokens):
+    """int8 embedding rows times their scales, as bf16 bits [N, D]."""
+    E = _c(E, np.int8); scale = _c(scale, np.float32); tokens = _c(tokens, np.int32)
+    V, D = E.shape
+    N = tokens.shape[0]
+    X = np.zeros((N, D), dtype=np.uint16)
+    lib().oracle_embed(_ptr(E), _ptr(scale), V, D, _ptr(tokens), N, _ptr(X))
+    return X
+
+
+def rmsnorm(X, gamma, eps: float = 1e-6):
+    """RMSNorm of bf16 rows X [N, K] with bf16 gamma [K], in float64."""
+    X = _c(X, np.uint16); gamma = _c(gamma, np.uint16)
+    N, K = X.shape
+    Y = np.zeros((N, K), dtype=np.float64)
+    lib().oracle_rmsnorm(_ptr(X), _ptr(gamma), float(eps), N, K, _ptr(Y))
+    return Y
+
+
+def swiglu(G, U):
+    """silu(g) * u of bf16 [N, M] gate and up, in float64."""
+    G = _c(G, np.uint16); U = _c(U, np.uint16)
+    N, M = G.shape
+    H = np.zeros((N, M), dtype=np.float64)
+    lib().oracle_swiglu(_ptr(G), _ptr(U), N, M, _ptr(H))
+    return H
 
 
 def host_cores() -> int:

@@ -345,3 +345,101 @@ void oracle_linear_b_mt(const uint32_t *P, const float *scale, const int32_t *ro
     j.N = N; j.Q = Q; j.s = s; j.z = z; j.Y = Y;
     run_threads(j, nthreads);
 }
+
+/* ------------------------------------------------------------------ */
+/* int8 output head and embedding                                       */
+/* ------------------------------------------------------------------ */
+/*
+ * The projections are ternary, but the embedding table and the output head
+ * stay int8 with one higher-precision scale per row (blog "Neutrino-1:
+ * quantization is a training decision", "What's actually ternary"; the model
+ * page "Neutrino-1 8B", "Architecture", lists them as two untied int8 tensors
+ * of vocabulary x hidden, one scale per row).  Greedy decoding -- and the
+ * draft/verify gate, which accepts a drafted token only when it equals the
+ * verifier's own argmax -- reads the head's argmax.
+ *
+ * Head, on activations quantised per token exactly as for the linears
+ * (oracle_quant: q, s, z):
+ *   acc[n,v]   = sum_d H[v,d] * q[n,d]                (exact integers)
+ *   rowsum[v]  = sum_d H[v,d]
+ *   logit[n,v] = ((float)(acc - z[n] * rowsum[v]) * s[n]) * scale[v]
+ *                (the integer rounded once to fp32, then two fp32 products)
+ *   token[n]   = the smallest v whose logit is the largest; best[n] = that logit.
+ * Embedding: x[n,d] = bf16 of the fp32 product E[t,d] * scale[t], t = tokens[n].
+ */
+void oracle_head(const int8_t *H, const float *scale, int64_t V, int64_t D,
+                 const int8_t *Q, const float *s, const int32_t *z, int64_t N,
+                 int32_t *ACC, float *logits, int32_t *token, float *best)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t best_i = -1;
+        float best_y = 0.0f;
+        for (int64_t v = 0; v < V; ++v) {
+            int64_t acc = 0, rs = 0;
+            for (int64_t d = 0; d < D; ++d) {
+                acc += (int64_t)H[v * D + d] * (int64_t)Q[n * D + d];
+                rs += (int64_t)H[v * D + d];
+            }
+            int64_t corrected = acc - (int64_t)z[n] * rs;
+            float per_token = (float)corrected * s[n];
+            float y = per_token * scale[v];
+            if (ACC) ACC[n * V + v] = (int32_t)acc;
+            if (logits) logits[n * V + v] = y;
+            if (best_i < 0 || y > best_y) {
+                best_i = v;
+                best_y = y;
+            }
+        }
+        token[n] = (int32_t)best_i;
+        best[n] = best_y;
+    }
+}
+
+void oracle_embed(const int8_t *E, const float *scale, int64_t V, int64_t D,
+                  const int32_t *tokens, int64_t N, uint16_t *X)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t t = tokens[n];
+        for (int64_t d = 0; d < D; ++d) {
+            float y = (float)E[t * D + d] * scale[t];
+            X[n * D + d] = oracle_bf16_rne(y);
+        }
+        (void)V;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Neighbours of the linears: RMSNorm and SwiGLU                        */
+/* ------------------------------------------------------------------ */
+/*
+ * Each decoder layer normalises its input with RMSNorm (eps 1e-6) before
+ * the q/k/v and gate/up projections, and its feed-forward is SwiGLU
+ * (model page "Neutrino-1 8B", "Architecture": Qwen3 geometry).  In double,
+ * straight from the definitions:
+ *   rmsnorm: y[n,k] = x[n,k] * gamma[k] / sqrt(mean_k x[n,k]^2 + eps)
+ *   swiglu:  h[n,m] = silu(g[n,m]) * u[n,m],  silu(g) = g / (1 + exp(-g))
+ */
+void oracle_rmsnorm(const uint16_t *X, const uint16_t *gamma, double eps, int64_t N,
+                    int64_t K, double *Y)
+{
+    for (int64_t n = 0; n < N; ++n) {
+        const uint16_t *row = X + n * K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double x = (double)bf16_to_float(row[k]);
+            ss += x * x;
+        }
+        double r = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k)
+            Y[n * K + k] = (double)bf16_to_float(row[k]) * r * (double)bf16_to_float(gamma[k]);
+    }
+}
+
+void oracle_swiglu(const uint16_t *G, const uint16_t *U, int64_t N, int64_t M, double *H)
+{
+    for (int64_t i = 0; i < N * M; ++i) {
+        double g = (double)bf16_to_float(G[i]);
+        double u = (double)bf16_to_float(U[i]);
+        H[i] = g / (1.0 + exp(-g)) * u;
+    }
+}

@@ -170,3 +170,16 @@ def test_chain_arguments_checked_without_a_gpu():
                img.ctypes.data_as(C.c_void_p), img.size) == tl.TL_ERR_NULL
     # an image that was never encoded is refused before any launch
     assert tl._lib.tl_chain_run(img.ctypes.data_as(C.c_void_p), 0x10000, None) == tl.TL_ERR_BAD_VALUE
+
+
+def test_head_arguments_checked_without_a_gpu():
+    f = tl._lib.tl_head_argmax
+    p = 0x10000
+    assert tl._lib.tl_head_workspace_bytes(1000, 4096, 9) == 0          # N > 8
+    assert tl._lib.tl_head_workspace_bytes(1000, 4100, 1) == 0          # D % 16
+    assert tl._lib.tl_head_workspace_bytes(1000, 16384, 8) == 0         # N * D too large
+    assert f(None, p, 10, 64, p, p, p, 1, None, p, p, p, 1 << 20, 0, None) == tl.TL_ERR_NULL
+    assert f(p, p, 10, 65, p, p, p, 1, None, p, p, p, 1 << 20, 0, None) == tl.TL_ERR_SHAPE
+    assert f(p + 8, p, 10, 64, p, p, p, 1, None, p, p, p, 1 << 20, 0, None) == tl.TL_ERR_ALIGN
+    assert f(p, p, 10, 64, p, p, p, 1, None, p, p, None, 1 << 20, 0, None) == tl.TL_ERR_WORKSPACE
+    assert tl._lib.tl_embed(None, p, 10, 64, p, 1, p, None) == tl.TL_ERR_NULL

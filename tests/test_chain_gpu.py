@@ -29,7 +29,8 @@ def _front_is_zero(chain):
     # leaves at zero (one counter per step; mode B adds a quantiser step per
     # linear)
     steps = chain.nsteps * (2 if chain.mode == tl.TL_MODE_I8 else 1)
-    return int(chain.workspace[:256 + 4 * steps].count_nonzero()) == 0
+    region = (4 * steps + 255) // 256 * 256           # counters, then completion flags
+    return int(chain.workspace[:256 + 2 * region].count_nonzero()) == 0
 
 
 def _layer_steps(oracle_mod, N, seed):

@@ -363,3 +363,136 @@ def test_bf16_rne_matches_hand_values(oracle_mod):
     vals = np.array([1.0, 1 + 2**-8, 1 + 3 * 2**-8, -2.0, 0.0, 65504.0], dtype=np.float32)
     out = oracle_mod.bf16_rne(vals)
     assert list(out) == [0x3F80, 0x3F80, 0x3F82, 0xC000, 0x0000, 0x4780]
+
+
+# ---------------------------------------------------------------- int8 head and embedding
+
+def _head_case(V, D, seed):
+    rng = np.random.default_rng(seed)
+    H = rng.integers(-128, 128, size=(V, D)).astype(np.int8)
+    scale = rng.uniform(0.005, 0.05, size=V).astype(np.float32)
+    return H, scale
+
+
+@pytest.mark.parametrize("V,D,N", [(37, 64, 1), (100, 160, 3), (5, 16, 8)])
+def test_head_integer_sums_and_argmax(oracle_mod, V, D, N):
+    """acc is numpy's int64 Q @ H^T; the fused argmax is numpy's argmax
+    (first occurrence) over the oracle's own logits."""
+    H, scale = _head_case(V, D, V + D)
+    X = _x(N, D, seed=D)
+    Q, s, z = oracle_mod.quant(X)
+    acc, lg, tok, best = oracle_mod.head(H, scale, Q, s, z)
+    assert np.array_equal(acc, Q.astype(np.int64) @ H.astype(np.int64).T)
+    assert np.array_equal(tok, np.argmax(lg, axis=1))
+    assert np.array_equal(best, lg[np.arange(N), tok])
+
+
+def test_head_ties_go_to_the_smallest_index(oracle_mod):
+    """Two identical rows that both hold the largest logit: the smaller index."""
+    V, D = 50, 64
+    H, scale = _head_case(V, D, 3)
+    for a, b in ((7, 31), (0, V - 1), (12, 13)):
+        Hc, sc = H.copy(), scale.copy()
+        Hc[a] = Hc[b] = 127
+        sc[a] = sc[b] = 1.0
+        X = synth.to_bf16_bits(np.abs(_f(_x(2, D, seed=a))) + 0.5)
+        Q, s, z = oracle_mod.quant(X)
+        _, lg, tok, _ = oracle_mod.head(Hc, sc, Q, s, z)
+        assert lg[0, a] == lg[0, b] == lg.max(axis=1)[0]
+        assert list(tok) == [a, a]
+
+
+def _f(bits):
+    return synth.bf16_bits_to_f32(bits)
+
+
+def test_head_tracks_the_dense_product(oracle_mod):
+    """|logit - scale * sum_d H x| <= scale * sum_d |H| * s / 2 (+ rounding):
+    pins the zero-point sign and the epilogue order against a float64
+    product of the unquantised activations."""
+    V, D = 64, 256
+    H, scale = _head_case(V, D, 11)
+    X = _x(4, D, seed=12, outlier_frac=0.01)
+    Q, s, z = oracle_mod.quant(X)
+    _, lg, _, _ = oracle_mod.head(H, scale, Q, s, z)
+    dense = _f(X).astype(np.float64) @ H.astype(np.float64).T * scale[None, :].astype(np.float64)
+    bound = (scale[None, :].astype(np.float64) * np.abs(H).sum(axis=1)[None, :]
+             * (s[:, None] / 2) * (1 + 1e-4) + 1e-6 * np.abs(dense))
+    assert np.all(np.abs(lg - dense) <= bound)
+
+
+def test_head_one_hot_closed_form(oracle_mod):
+    """One-hot x = v e_k: q_k = 127, the rest -128, z = -128, so
+    acc - z * rowsum = 255 * H[:, k] and logit = scale * H[:, k] * v up to
+    fp32 rounding."""
+    V, D = 40, 128
+    H, scale = _head_case(V, D, 21)
+    x = np.zeros((1, D), dtype=np.float32)
+    x[0, 70] = 2.5
+    Q, s, z = oracle_mod.quant(synth.to_bf16_bits(x))
+    acc, lg, tok, _ = oracle_mod.head(H, scale, Q, s, z)
+    rs = H.astype(np.int64).sum(axis=1)
+    assert np.array_equal(acc[0].astype(np.int64) + 128 * rs, 255 * H[:, 70].astype(np.int64))
+    ref = scale.astype(np.float64) * H[:, 70] * 2.5
+    assert np.all(np.abs(lg[0] - ref) <= 4 * np.spacing(np.abs(ref).astype(np.float32)))
+    assert tok[0] == int(np.argmax(ref))
+
+
+def test_embed_rows_times_scale(oracle_mod):
+    """Powers-of-two scales give exact products (closed form); other scales
+    give the bf16 (ties to even) of the fp32 product."""
+    V, D = 30, 48
+    rng = np.random.default_rng(4)
+    E = rng.integers(-128, 128, size=(V, D)).astype(np.int8)
+    scale = (2.0 ** rng.integers(-8, 3, size=V)).astype(np.float32)
+    toks = np.array([3, 29, 0, 3], dtype=np.int32)
+    X = oracle_mod.embed(E, scale, toks)
+    exact = E[toks].astype(np.float64) * scale[toks, None]
+    assert np.array_equal(_f(X).astype(np.float64), exact)
+    scale2 = rng.uniform(0.001, 0.1, size=V).astype(np.float32)
+    X2 = oracle_mod.embed(E, scale2, toks)
+    prod = E[toks].astype(np.float32) * scale2[toks, None]
+    assert np.array_equal(X2, synth.to_bf16_bits(prod))
+
+
+# ---------------------------------------------------------------- RMSNorm and SwiGLU
+
+def test_rmsnorm_identities(oracle_mod):
+    """mean_k (y/gamma)^2 = ms / (ms + eps); y scales with gamma; a constant
+    row c gives gamma * c / sqrt(c^2 + eps); y(alpha x) = y(x) up to eps."""
+    N, K = 4, 512
+    X = _x(N, K, seed=31)
+    rng = np.random.default_rng(32)
+    gamma = synth.to_bf16_bits(rng.uniform(0.5, 2.0, size=K).astype(np.float32))
+    eps = 1e-6
+    Y = oracle_mod.rmsnorm(X, gamma, eps)
+    xf = _f(X).astype(np.float64)
+    gf = _f(gamma).astype(np.float64)
+    ms = (xf ** 2).mean(axis=1)
+    assert np.allclose(((Y / gf) ** 2).mean(axis=1), ms / (ms + eps), rtol=1e-12)
+    assert np.allclose(Y / gf, xf / np.sqrt(ms + eps)[:, None], rtol=1e-13)
+    c = synth.to_bf16_bits(np.full((1, K), 3.0, dtype=np.float32))
+    ones = synth.to_bf16_bits(np.ones(K, dtype=np.float32))
+    assert np.allclose(oracle_mod.rmsnorm(c, ones, eps), 3.0 / np.sqrt(9.0 + eps), rtol=1e-14)
+    X2 = synth.to_bf16_bits(4.0 * xf.astype(np.float32))      # exact (power of two)
+    assert np.allclose(oracle_mod.rmsnorm(X2, gamma, 0.0), oracle_mod.rmsnorm(X, gamma, 0.0),
+                       rtol=1e-13)
+
+
+def test_swiglu_identities(oracle_mod):
+    """silu(g) - silu(-g) = g (so with u = 1 the two halves sum to g);
+    silu(0) = 0; u = 0 gives 0; silu(g) -> g for large g, -> 0 for very
+    negative g."""
+    rng = np.random.default_rng(33)
+    g = rng.standard_normal((3, 300)).astype(np.float32) * 4
+    G = synth.to_bf16_bits(g)
+    ones = synth.to_bf16_bits(np.ones_like(g))
+    h_pos = oracle_mod.swiglu(G, ones)
+    h_neg = oracle_mod.swiglu(synth.to_bf16_bits(-_f(G)), ones)
+    assert np.allclose(h_pos - h_neg, _f(G).astype(np.float64), rtol=1e-13, atol=1e-15)
+    z = synth.to_bf16_bits(np.zeros((1, 8), dtype=np.float32))
+    assert not oracle_mod.swiglu(z, synth.to_bf16_bits(np.ones((1, 8), np.float32))).any()
+    assert not oracle_mod.swiglu(G, synth.to_bf16_bits(np.zeros_like(g))).any()
+    big = synth.to_bf16_bits(np.float32([[60.0, -60.0]]))
+    h = oracle_mod.swiglu(big, synth.to_bf16_bits(np.float32([[1.0, 1.0]])))
+    assert abs(h[0, 0] - 60.0) < 1e-20 and abs(h[0, 1]) < 1e-24

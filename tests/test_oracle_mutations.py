@@ -43,6 +43,17 @@ MUTATIONS = {
     "quant_ties_away_sym": ("float r = rintf(bf16_to_float(x[k]) / s);",
                             "float r = roundf(bf16_to_float(x[k]) / s);"),
     "quant_range_without_zero": ("float lo = 0.0f, hi = 0.0f;", "float lo = 1e30f, hi = -1e30f;"),
+    "head_argmax_last_of_ties": ("if (best_i < 0 || y > best_y) {", "if (best_i < 0 || y >= best_y) {"),
+    "head_zero_point_sign": ("int64_t corrected = acc - (int64_t)z[n] * rs;",
+                             "int64_t corrected = acc + (int64_t)z[n] * rs;"),
+    "head_rowsum_dropped": ("rs += (int64_t)H[v * D + d];", "rs += 0;"),
+    "head_transposed": ("acc += (int64_t)H[v * D + d] * (int64_t)Q[n * D + d];",
+                        "acc += (int64_t)H[d * V + v % D] * (int64_t)Q[n * D + d];"),
+    "embed_scale_row": ("float y = (float)E[t * D + d] * scale[t];",
+                        "float y = (float)E[t * D + d] * scale[0];"),
+    "rmsnorm_without_eps": ("double r = 1.0 / sqrt(ss / (double)K + eps);",
+                            "double r = 1.0 / sqrt(ss / (double)K);"),
+    "swiglu_sign": ("H[i] = g / (1.0 + exp(-g)) * u;", "H[i] = g / (1.0 + exp(g)) * u;"),
     "int_acc_dropped_term": ("for (int64_t k = 0; k < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];",
                              "for (int64_t k = 0; k + 1 < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];"),
 }
@@ -66,6 +77,14 @@ def _pins():
         ("onehot_b", lambda: T.test_linear_b_one_hot_identity(o)),
         ("b_tracks_a", lambda: [T.test_linear_b_tracks_linear_a_within_quant_error(o, s)
                                 for s in (False, True)]),
+        ("head_sums", lambda: [T.test_head_integer_sums_and_argmax(o, V, D, N)
+                               for V, D, N in ((37, 64, 1), (100, 160, 3), (5, 16, 8))]),
+        ("head_ties", lambda: T.test_head_ties_go_to_the_smallest_index(o)),
+        ("head_dense", lambda: T.test_head_tracks_the_dense_product(o)),
+        ("head_onehot", lambda: T.test_head_one_hot_closed_form(o)),
+        ("embed", lambda: T.test_embed_rows_times_scale(o)),
+        ("rmsnorm", lambda: T.test_rmsnorm_identities(o)),
+        ("swiglu", lambda: T.test_swiglu_identities(o)),
     ]
 
 
