@@ -6,12 +6,13 @@
 One step is one pass of the whole hot path over one batch: all 252
 projection linears of a 36-layer, Qwen3-8B-shaped decoder (hidden 4096,
 q/o 4096x4096, k/v 1024x4096, gate/up 12288x4096, down 4096x12288), as 144
-dependent launch groups run by one persistent launch (a chain: each group
-waits for the previous one before reading its input), on seeded synthetic
-weights with the pages' code statistics.  The headline is N = 1 decode in
-mode A (bf16 activations, fp32 accumulation); the N = 8 speculative-verify
-batch (modes A and B) is reported beside it, and so is the same pass as a
-CUDA graph of 144 launches.
+dependent launches (q/k/v and gate/up grouped) replayed from a CUDA graph
+with programmatic dependent launch, on seeded synthetic weights with the
+pages' code statistics.  The headline is N = 1 decode in mode A (bf16
+activations, fp32 accumulation); beside it: the N = 8 speculative-verify
+batch (modes A and B), the same pass as one persistent chain launch, the
+0.6B-shaped stack, a single 2048 x 1024 linear, the int8 output head with
+its fused argmax, and the N = 512 prefill.
 
 Prints ONE JSON line (rank 0).  Under torchrun each rank runs an
 independent replica (the path has no exchange step); value is the sum of the
@@ -38,7 +39,9 @@ L2_BYTES = 126 * 1024 * 1024
 
 
 def peaks():
-    """(HBM GB/s, kind, bf16 TFLOP/s sustained, kind) from MEASURED_PEAKS.json."""
+    """(HBM GB/s, kind, bf16 TFLOP/s burst, kind) from MEASURED_PEAKS.json.
+    The prefill pass is timed over a few replays of ~13 ms, not seconds, so
+    its denominator is the burst figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
@@ -47,9 +50,9 @@ def peaks():
     except (OSError, KeyError, ValueError):
         d, hbm, hk = {}, 6400.0, "fallback"
     try:
-        bf, bk = float(d["bf16_tflops_sustained"]), "measured (bf16_tflops_sustained)"
+        bf, bk = float(d["bf16_tflops"]), "measured (bf16_tflops, burst)"
     except (KeyError, ValueError):
-        bf, bk = 1400.0, "fallback (sustained)"
+        bf, bk = 1800.0, "fallback (burst)"
     return hbm, hk, bf, bk
 
 
@@ -108,7 +111,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def measured_traffic(alg_per_launch, record="tl_chain_kernel_traffic.txt"):
+def measured_traffic(alg_per_launch, record="tl_mma_kernel_traffic.txt"):
     """DRAM bytes per launch of the decode kernel: the ncu-measured bytes per
     algorithmic byte (profiles/<record>) times this run's algorithmic bytes
     per launch; None when the record is missing or the kernels' device code
@@ -169,18 +172,16 @@ def time_chain(chain, steps, warmup, torch):
 
 
 def time_e2e(stack, steps, warmup, torch):
-    """Per step: pinned host -> device copy of all inputs, one pass of the
-    chain, and a device -> host read of all outputs, inside the timed region."""
+    """Per step: pinned host -> device copy of all inputs, one replay of the
+    graph, and a device -> host read of all outputs, inside the timed region."""
     stream = torch.cuda.current_stream()
     hx = torch.empty(stack.X_flat.shape, dtype=stack.X_flat.dtype, pin_memory=True)
     hx.copy_(stack.X_flat.cpu())
     hy = torch.empty(stack.Y_flat.shape, dtype=stack.Y_flat.dtype, pin_memory=True)
 
-    chain = stack.chain()
-
     def step():
         stack.X_flat.copy_(hx, non_blocking=True)
-        chain.run()
+        stack.graph.replay()
         hy.copy_(stack.Y_flat, non_blocking=True)
 
     for _ in range(warmup):
@@ -252,23 +253,115 @@ def run_reference(args, rank, world):
                         synth.scales(M, seed))
     sampler = OracleSample(host, shape, 1)
     cores = sampler.cores
-    per_step = []
+    sample_s, per_token = [], []
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         v, desc = sampler.run(seconds=0.0)
+        el = time.perf_counter() - t0
         if i >= args.warmup:
-            per_step.append(1.0 / v)           # seconds per token (extrapolated)
-    sec = sum(per_step) / len(per_step)
-    value = 1.0 / sec
+            sample_s.append(el)                # one layer's 7 linears, measured
+            per_token.append(1.0 / v)          # seconds per token, extrapolated x36
+    value = 1.0 / (sum(per_token) / len(per_token))
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "ms_per_step": 1e3 * sum(sample_s) / len(sample_s), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 1,
-                       "parallelism": "none (host threads)"},
+                       "parallelism": "none (host threads)",
+                       "step": "each timed step runs layer 0's 7 linears (1/36 of the stack) on "
+                               "the oracle; ms_per_step is that measured time, and value "
+                               "extrapolates it to the 36-layer stack (x36)"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": "each step: " + desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def flush_l2(torch, buf):
+    buf.zero_()
+
+
+def bench_single_linear(args, torch, tl, hbm_peak, cpu):
+    """A single 2048 x 1024 ternary linear at one token, modes A and B:
+    launch-to-launch latency (back to back, L2-warm) and, with a 256 MiB
+    buffer written between timed launches to flush L2, cold GB/s."""
+    import numpy as np
+    from bit_matvec_ternary_b300 import synth
+    M, K = 2048, 1024
+    W = synth.ternary(M, K, 0.626, 0)
+    scale = synth.scales(M, 0)
+    w = tl.TernaryWeight.from_int8(W, scale)
+    x = synth.activations(1, K, seed=0)
+    xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    q, s, z = tl.tl_quantize_act(xt)
+    ws = tl.make_workspace([[w]], 1)
+    y = torch.empty((1, M), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    out = {"shape": "2048x1024, N=1, seed 0"}
+    for mode, name in ((tl.TL_MODE_BF16, "mode_a"), (tl.TL_MODE_I8, "mode_b")):
+        if mode == tl.TL_MODE_BF16:
+            call = lambda: tl.tl_linear(w, xt, out=y, workspace=ws)
+        else:
+            call = lambda: tl.tl_linear(w, q, s, z, out=y, mode=mode, workspace=ws)
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 200
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        lat_us = e0.elapsed_time(e1) * 1e3 / reps
+        cold = []
+        for _ in range(20):
+            flush_l2(torch, flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            cold.append(a.elapsed_time(b) * 1e3)
+        cold_us = statistics.median(cold)
+        alg = tl.tl_packed_bytes(M, K) + 4 * M + 2 * K + 4 * M + (4 * M + 8 if mode else 0)
+        out[name] = {"latency_us": lat_us, "cold_us": cold_us, "algorithmic_bytes": alg,
+                     "cold_gbs": alg / (cold_us / 1e6) / 1e9,
+                     "cold_frac_of_hbm": alg / (cold_us / 1e6) / 1e9 / hbm_peak}
+    if cpu:
+        from oracle import oracle as O
+        P = O.pack(W)
+        rs = O.rowsum(P, M, K)
+        Qr, sr, zr = O.quant(x)
+        for name, fn in (("oracle_mode_a", lambda nt: O.linear_a_mt(P, scale, M, K, x, nthreads=nt)),
+                         ("oracle_mode_b", lambda nt: O.linear_b_mt(P, scale, rs, M, K, Qr, sr, zr,
+                                                                     nthreads=nt))):
+            res = {}
+            for label, nt in (("single_thread_ms", 1), ("all_cores_ms", O.host_cores())):
+                t = []
+                for _ in range(5):
+                    t0 = time.perf_counter()
+                    fn(nt)
+                    t.append((time.perf_counter() - t0) * 1e3)
+                res[label] = statistics.median(t)
+            res["cores"] = O.host_cores()
+            out[name] = res
+    return out
+
+
+def bench_stack_line(shape, N, mode, args, torch, tl, hbm_peak, weights=None, **kw):
+    from bit_matvec_ternary_b300.stack import LinearStack
+    st = LinearStack(shape, N=N, mode=mode, out_dtype=tl.TL_OUT_F32, weights=weights, **kw)
+    st.capture()
+    ms = time_graph(st, args.steps, args.warmup, torch)
+    a = st.algorithmic_bytes()
+    line = {"tokens_s": N / (ms / 1e3), "ms_per_step": ms, "algorithmic_bytes": a,
+            "gbs": a / (ms / 1e3) / 1e9, "frac_of_hbm": a / (ms / 1e3) / 1e9 / hbm_peak,
+            "launches_per_step": st.launches_per_step}
+    del st
+    torch.cuda.empty_cache()
+    return line
 
 
 def bench_head(args, torch, tl, hbm_peak):
@@ -322,6 +415,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-prefill", action="store_true", help="skip the N=512 prefill line")
     ap.add_argument("--no-head", action="store_true", help="skip the int8 head lines")
+    ap.add_argument("--no-small", action="store_true",
+                    help="skip the 0.6B stack and single-linear lines")
     ap.add_argument("--layers", type=int, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -357,12 +452,12 @@ def main():
     t_gen = time.perf_counter() - t_gen
     stack = LinearStack(shape, N=1, mode=tl.TL_MODE_BF16, out_dtype=tl.TL_OUT_F32,
                         weights=weights)
-    chain = stack.chain()
+    stack.capture()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ms = time_chain(chain, args.steps, args.warmup, torch)
+        ms = time_graph(stack, args.steps, args.warmup, torch)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -374,20 +469,18 @@ def main():
     tok_s = world * 1.0 / (ms_max / 1e3)
     alg = stack.algorithmic_bytes()
     gbs = alg / (ms_max / 1e3) / 1e9
-    launches = 1
+    launches = stack.launches_per_step
 
     ms_e2e, h2d, d2h = time_e2e(stack, args.steps, args.warmup, torch)
     e2e = {"value": world / (ms_e2e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e2e,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "how": "per step: one pinned H2D copy of all 144 inputs, one tl_chain_run "
-                  "(C ABI), one D2H copy of all 252 outputs"}
-    # the same pass as a graph of 144 dependent launches (programmatic
-    # dependent launch between them), for comparison
-    stack.capture()
-    ms_graph = time_graph(stack, args.steps, args.warmup, torch)
-    per_launch = {"ms_per_step": ms_graph, "tokens_s": 1.0 / (ms_graph / 1e3),
-                  "launches_per_step": stack.launches_per_step,
-                  "frac_of_hbm": alg / (ms_graph / 1e3) / 1e9 / hbm_peak}
+           "how": "per step: one pinned H2D copy of all 144 inputs, one replay of the graph "
+                  "of C-ABI launches, one D2H copy of all 252 outputs"}
+    # the same pass as one persistent chain launch (tl_chain_run), for comparison
+    ms_chain = time_chain(stack.chain(), args.steps, args.warmup, torch)
+    chain_line = {"ms_per_step": ms_chain, "tokens_s": 1.0 / (ms_chain / 1e3),
+                  "launches_per_step": 1, "frac_of_hbm": alg / (ms_chain / 1e3) / 1e9 / hbm_peak,
+                  "kernel": "tl_chain_kernel"}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -403,21 +496,31 @@ def main():
         for mode, name, outl in ((tl.TL_MODE_BF16, "n8_mode_a", 0.01), (tl.TL_MODE_I8, "n8_mode_b", 0.01)):
             st8 = LinearStack(shape, N=8, mode=mode, out_dtype=tl.TL_OUT_F32, outlier_frac=outl,
                               weights=weights)
-            ms8 = time_chain(st8.chain(), args.steps, args.warmup, torch)
+            st8.capture()
+            ms8 = time_graph(st8, args.steps, args.warmup, torch)
+            ms8c = time_chain(st8.chain(), args.steps, args.warmup, torch)
             a8 = st8.algorithmic_bytes()
             extra[name] = {"tokens_s": 8 / (ms8 / 1e3), "ms_per_step": ms8,
                            "algorithmic_bytes": a8, "gbs": a8 / (ms8 / 1e3) / 1e9,
                            "frac_of_hbm": a8 / (ms8 / 1e3) / 1e9 / hbm_peak,
-                           "launches_per_step": 1,
-                           "how": "one tl_chain_run per step" + (
-                               " (each group's activations quantised inside the chain)"
-                               if mode == tl.TL_MODE_I8 else "")}
+                           "launches_per_step": st8.launches_per_step,
+                           "chain": {"tokens_s": 8 / (ms8c / 1e3), "ms_per_step": ms8c,
+                                     "frac_of_hbm": a8 / (ms8c / 1e3) / 1e9 / hbm_peak}}
             del st8
             torch.cuda.empty_cache()
 
+    # N = 1 in mode B (a quantiser launch in front of every linear launch)
+    extra["n1_mode_b"] = bench_stack_line(shape, 1, tl.TL_MODE_I8, args, torch, tl, hbm_peak,
+                                          weights=weights)
     if not args.no_head:
         extra["head_argmax"] = bench_head(args, torch, tl, hbm_peak)
         torch.cuda.empty_cache()
+    if not args.no_small:
+        # the 0.6B-shaped stack (28 layers, hidden 1024), unit-RMS inputs
+        extra["stack_06b_n1"] = bench_stack_line(synth.NEUTRINO_06B, 1, tl.TL_MODE_BF16, args,
+                                                 torch, tl, hbm_peak, unit_rms=True)
+        extra["single_linear_2048x1024"] = bench_single_linear(
+            args, torch, tl, hbm_peak, cpu=rank == 0 and not args.no_cpu)
 
     if not args.no_prefill:
         # prefill-sized batch: 512 tokens, int8 symmetric per-token activations,
@@ -454,13 +557,13 @@ def main():
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak, "traffic": measured_traffic(alg / launches),
                          "traffic_note": "bytes per launch: ncu DRAM bytes per algorithmic byte "
-                                         "of one chain launch over two 8B-shaped layers, times "
-                                         "this step's algorithmic bytes",
-                         "kernel": "tl_chain_kernel",
+                                         "of one gate+up launch, times this step's mean "
+                                         "algorithmic bytes per launch",
+                         "kernel": "tl_mma_kernel",
                          "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
                          "algorithmic_bytes_per_step": alg, "launches_per_step": launches,
                          "avg_launch_us": ms_max * 1e3 / launches},
-            "launch_per_linear": per_launch,
+            "chain": chain_line,
             "e2e": e2e,
             "gpu_launches": launches * args.steps,
             "clocks": clocks,

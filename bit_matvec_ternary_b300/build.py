@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libtl.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["tl_host.cpp", "tl_kernels.cu", "tl_prefill.cu", "tl_head.cu", "tl_fused.cu", "tl_noalloc.cu"]
+SOURCES = ["tl_host.cpp", "tl_kernels.cu", "tl_prefill.cu", "tl_head.cu", "tl_fused.cu", "tl_blockscale.cu", "tl_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

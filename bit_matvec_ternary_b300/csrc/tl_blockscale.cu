@@ -1,0 +1,157 @@
+// tl_blockscale.cu -- the block-wise scale variant of the ternary linear.
+//
+// The blog ("Neutrino-1: quantization is a training decision", "What's
+// actually ternary") describes the weights as blocks, each with its own
+// higher-precision scale; the shipped 8B artifact keeps one scale per row
+// (model page "Neutrino-1 8B", "Architecture"), which the main kernels use.
+// This variant takes a scale per (row, 128-column block):
+//     y[n, m] = sum_b scale[m, b] * sum_{k in b} w[m, k] * x[n, k]
+// on the same TL2P v2 codes, bf16 activations, fp32 sums.
+//
+// Kernel: one warp per 16-row tile, over all of K (no split, so no
+// workspace); lane (g, t) loads its 16 bytes of each tile (eight tiles in
+// flight), decodes the eight k-steps' A fragments to bf16 2w (the field
+// 1 - w moved to the sign and top exponent bits), multiplies them by the
+// tokens' bf16 activations on the tensor cores into fresh per-tile
+// accumulators (two chains), and folds each tile's sums into the row's
+// result with that block's scale (times 1/2).  Activations are read from
+// global memory through L1 (all warps of an SM read the same X).
+#include "tl.h"
+#include "tl_internal.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+namespace {
+
+constexpr int kBWarps = 4;
+constexpr int kBUnroll = 8;       // tiles loaded ahead per warp
+
+struct BsArgs {
+    const uint4 *packed;
+    const float *bscale;          // [M][KB]
+    const uint16_t *X;            // bf16 [N][K]
+    void *Y;
+    int M, K, KB, N, out;
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The field pair of k-step m of a TL2P v2 word as bf16x2 2w: 00 -> +2,
+// 01 -> 0, 10 -> -2.
+__device__ __forceinline__ uint32_t dec2w(uint32_t word, int m) {
+    return ((word << (14 - 2 * m)) & 0xC000C000u) ^ 0x40004000u;
+}
+
+// Two consecutive bf16 activations of token n at column k (zero past K or
+// past the batch).
+__device__ __forceinline__ uint32_t xpair(const BsArgs &a, int n, int k) {
+    if (n >= a.N) return 0u;
+    const uint16_t *x = a.X + (long long)n * a.K;
+    const uint32_t lo = k < a.K ? __ldg(x + k) : 0u;
+    const uint32_t hi = k + 1 < a.K ? __ldg(x + k + 1) : 0u;
+    return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(kBWarps * 32)
+tl_blockscale_kernel(const __grid_constant__ BsArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int r = blockIdx.x * kBWarps + warp;           // row tile
+    const int R = (a.M + 15) / 16;
+    if (r >= R) return;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint4 *tiles = a.packed + (long long)r * a.KB * 32 + lane;
+    const int m0 = r * 16 + g, m1 = m0 + 8;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};                   // rows g, g+8 x tokens 2t, 2t+1
+    for (int b0 = 0; b0 < a.KB; b0 += kBUnroll) {
+        uint4 w[kBUnroll];
+#pragma unroll
+        for (int u = 0; u < kBUnroll; ++u)
+            w[u] = b0 + u < a.KB ? tiles[(long long)(b0 + u) * 32] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < kBUnroll; ++u) {
+            const int b = b0 + u;
+            if (b >= a.KB) break;
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int k = b * 128 + 16 * m + 2 * t;
+                const uint32_t b0r = xpair(a, g, k), b1r = xpair(a, g, k + 8);
+                mma16816((m & 1) ? c1 : c0, dec2w(w[u].x, m), dec2w(w[u].y, m), dec2w(w[u].z, m),
+                         dec2w(w[u].w, m), b0r, b1r);
+            }
+            const float s0 = m0 < a.M ? __ldg(a.bscale + (long long)m0 * a.KB + b) : 0.f;
+            const float s1 = m1 < a.M ? __ldg(a.bscale + (long long)m1 * a.KB + b) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float v = __fmul_rn(__fadd_rn(c0[i], c1[i]), 0.5f);
+                y[i] = __fmaf_rn(v, i < 2 ? s0 : s1, y[i]);
+            }
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = i < 2 ? m0 : m1, n = 2 * t + (i & 1);
+        if (m >= a.M || n >= a.N) continue;
+        const long long o = (long long)n * a.M + m;
+        if (a.out == TL_OUT_F32) static_cast<float *>(a.Y)[o] = y[i];
+        else static_cast<__nv_bfloat16 *>(a.Y)[o] = __float2bfloat16_rn(y[i]);
+    }
+}
+
+bool aligned(const void *p, size_t al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+tl_status tl_linear_blockscale(const uint32_t *packed, const float *bscale, int M, int K,
+                               const void *X, int N, void *Y, int out_dtype, unsigned flags,
+                               void *stream) {
+    if (!packed || !bscale || !X || !Y) return TL_ERR_NULL;
+    if (M < 1 || K < 1 || M > TL_MAX_M || K > TL_MAX_K || N < 1) return TL_ERR_SHAPE;
+    if (out_dtype != TL_OUT_F32 && out_dtype != TL_OUT_BF16) return TL_ERR_MODE;
+    if (!aligned(packed, 16) || !aligned(bscale, 4) || !aligned(X, 2) ||
+        !aligned(Y, out_dtype == TL_OUT_BF16 ? 2 : 4))
+        return TL_ERR_ALIGN;
+    int sms = 0;
+    const tl_status st = tl_internal::device_sms(&sms);
+    if (st != TL_OK) return st;
+    const int R = (M + 15) / 16;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((R + kBWarps - 1) / kBWarps));
+    cfg.blockDim = dim3(kBWarps * 32);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
+    const size_t esz = out_dtype == TL_OUT_BF16 ? 2 : 4;
+    for (int n0 = 0; n0 < N; n0 += 8) {
+        BsArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.packed = reinterpret_cast<const uint4 *>(packed);
+        a.bscale = bscale;
+        a.X = static_cast<const uint16_t *>(X) + (size_t)n0 * K;
+        a.Y = static_cast<char *>(Y) + (size_t)n0 * M * esz;
+        a.M = M; a.K = K; a.KB = (K + 127) / 128; a.N = N - n0 < 8 ? N - n0 : 8;
+        a.out = out_dtype;
+        if (cudaLaunchKernelEx(&cfg, tl_blockscale_kernel, a) != cudaSuccess) return TL_ERR_CUDA;
+    }
+    return TL_OK;
+}
+
+}  // extern "C"

@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <thread>
 #include <vector>
@@ -142,6 +143,44 @@ tl_status tl_validate_packed(const uint32_t *packed, int64_t M, int64_t K, int64
         }
     if (bad_codes) *bad_codes = bad;
     return bad ? TL_ERR_BAD_VALUE : TL_OK;
+}
+
+// Block-wise scales (blog "Neutrino-1: quantization is a training
+// decision", "What's actually ternary"): each block of a row has its own
+// scale, the block's mean absolute weight, and its codes are
+// round(clamp(w / scale, -1, 1)).  The mean is taken in double over the
+// block's real columns, in column order, and stored as fp32; the ratio uses
+// that fp32 scale, in double, rounded half to even.
+tl_status tl_ternarize_absmean(const float *W, int64_t M, int64_t K, int8_t *T, float *bscale) {
+    if (!W || !T || !bscale) return TL_ERR_NULL;
+    if (M < 1 || K < 1 || M > TL_MAX_M || K > TL_MAX_K) return TL_ERR_SHAPE;
+    std::atomic<int64_t> bad{0};
+    parallel_rows(M, K, [&](int64_t m0, int64_t m1) {
+        int64_t local = 0;
+        for (int64_t i = m0 * K; i < m1 * K; ++i)
+            if (!std::isfinite(W[i])) ++local;
+        bad += local;
+    });
+    if (bad.load()) return TL_ERR_BAD_VALUE;
+    const int64_t KB = (K + TL_SCALE_BLOCK - 1) / TL_SCALE_BLOCK;
+    parallel_rows(M, K, [&](int64_t m0, int64_t m1) {
+        for (int64_t m = m0; m < m1; ++m) {
+            const float *row = W + m * K;
+            for (int64_t b = 0; b < KB; ++b) {
+                const int64_t k0 = b * TL_SCALE_BLOCK, k1 = std::min(K, k0 + TL_SCALE_BLOCK);
+                double acc = 0.0;
+                for (int64_t k = k0; k < k1; ++k) acc += std::fabs((double)row[k]);
+                const float sc = (float)(acc / (double)(k1 - k0));
+                bscale[m * KB + b] = sc;
+                for (int64_t k = k0; k < k1; ++k) {
+                    const double q = sc > 0.0f ? (double)row[k] / (double)sc : 0.0;
+                    const double c = q > 1.0 ? 1.0 : (q < -1.0 ? -1.0 : q);
+                    T[m * K + k] = (int8_t)std::nearbyint(c);
+                }
+            }
+        }
+    });
+    return TL_OK;
 }
 
 const char *tl_status_string(tl_status s) {

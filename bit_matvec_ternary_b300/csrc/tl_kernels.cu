@@ -227,9 +227,8 @@ struct GroupArgs {
 
 // Header of an encoded chain (device memory), followed by its steps.
 struct ChainHeader {
-    unsigned *cnt;          // [nsteps] CTAs done per step; zero between launches
-    unsigned *done;         // [nsteps] step complete (set by the CTA that completes cnt);
-                            // on other cache lines than cnt, zero between launches
+    unsigned long long *cnt;    // [nsteps] CTAs done per step, over all passes so far
+    unsigned long long *epoch;  // passes completed; [1] counts CTAs leaving the current pass
     const unsigned *gate;   // when not null, step 0 waits until *gate != 0
     long long wait_limit;   // SM cycles before a wait for a step's inputs gives up
     int nsteps;
@@ -454,32 +453,39 @@ __device__ __forceinline__ float chain_units(float sum, int T) {
 
 // VPL consecutive activations of token n from column k0 (VPL = 8 bf16 in mode
 // A, 16 int8 in mode B; k0 a multiple of VPL): one 16-byte load when X allows
-// it, else element loads; columns >= K read as 0.  Loads go to L2 (not the
-// SM's L1), since in a chain X may have been written by other SMs during
-// the launch.
-template <bool kModeA>
+// it, else element loads; columns >= K read as 0.  In a chain (kL2) the
+// loads skip the SM's L1, since X may have been written by other SMs during
+// the launch; a launch of its own reads X written by an earlier kernel and
+// may share it through L1 with the SM's other CTA.
+template <bool kL2>
+__device__ __forceinline__ uint4 ldx(const uint4 *p) { return kL2 ? __ldcg(p) : __ldg(p); }
+template <bool kL2>
+__device__ __forceinline__ uint16_t ldx16(const uint16_t *p) { return kL2 ? __ldcg(p) : __ldg(p); }
+template <bool kL2>
+__device__ __forceinline__ uint8_t ldx8(const uint8_t *p) { return kL2 ? __ldcg(p) : __ldg(p); }
+template <bool kModeA, bool kL2>
 __device__ __forceinline__ uint4 load_group(const GroupArgs &a, int n, int k0) {
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (kModeA) {
         const uint16_t *x = reinterpret_cast<const uint16_t *>(a.X) + (long long)n * a.K + k0;
         if (a.xvec) {
-            if (k0 < a.K) v = __ldcg(reinterpret_cast<const uint4 *>(x));
+            if (k0 < a.K) v = ldx<kL2>(reinterpret_cast<const uint4 *>(x));
         } else {
             uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (k0 + e < a.K) w[e >> 1] |= (uint32_t)__ldcg(x + e) << (16 * (e & 1));
+                if (k0 + e < a.K) w[e >> 1] |= (uint32_t)ldx16<kL2>(x + e) << (16 * (e & 1));
             v = make_uint4(w[0], w[1], w[2], w[3]);
         }
     } else {
         const uint8_t *x = reinterpret_cast<const uint8_t *>(a.X) + (long long)n * a.K + k0;
         if (a.xvec) {
-            if (k0 < a.K) v = __ldcg(reinterpret_cast<const uint4 *>(x));
+            if (k0 < a.K) v = ldx<kL2>(reinterpret_cast<const uint4 *>(x));
         } else {
             uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                if (k0 + e < a.K) w[e >> 2] |= (uint32_t)__ldcg(x + e) << (8 * (e & 3));
+                if (k0 + e < a.K) w[e >> 2] |= (uint32_t)ldx8<kL2>(x + e) << (8 * (e & 3));
             v = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
@@ -567,7 +573,7 @@ __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const u
 // The activation groups of one slice: VPL activations per group, LB groups
 // per 128-column block, N * kw * LB groups in all, taken SB * kThreads at a
 // time starting at `base`.
-template <bool kModeA, int SB>
+template <bool kModeA, int SB, bool kL2>
 __device__ __forceinline__ void stage_load(const GroupArgs &a, const Slice &P, int base,
                                            uint4 (&v)[SB]) {
     constexpr int VPL = kModeA ? 8 : 16;
@@ -581,7 +587,7 @@ __device__ __forceinline__ void stage_load(const GroupArgs &a, const Slice &P, i
         if (idx < total) {
             const int q = idx / LB, o = idx % LB;     // q = n * kw + jb
             const int n = fdiv(q, dv), jb = q - n * P.kw;
-            v[i] = load_group<kModeA>(a, n, (P.kb0 + jb) * 128 + o * VPL);
+            v[i] = load_group<kModeA, kL2>(a, n, (P.kb0 + jb) * 128 + o * VPL);
         }
     }
 }
@@ -645,11 +651,12 @@ __device__ __forceinline__ void pipe_seek(Pipe &p, int cta, int warp) {
     p.pc_on = false;
 }
 
-// Producer (lane 0, p.pc_on): copy the next chunk into `slot` and advance.
+// Producer (lane 0, p.pc_on): copy the next chunk into `slot` and advance;
+// `a` is the constants of step p.pstep.
 template <int NT>
-__device__ __forceinline__ void pipe_produce(Pipe &p, int slot, int cta, int warp) {
+__device__ __forceinline__ void pipe_produce(Pipe &p, const GroupArgs &a, int slot, int cta,
+                                             int warp) {
     constexpr int CH = chunk_tiles(NT);
-    const GroupArgs &a = p.steps[p.pstep];
     const int n = min(CH, min(p.pc.uend - p.pc.u, p.pc.kw - p.pc.b));
     bulk_load(p.ring_w + slot * (CH * 512), p.prow + (long long)(p.pc.kb0 + p.pc.b) * 512, n * 512,
               p.bar_w + 8u * slot);
@@ -673,19 +680,12 @@ __device__ __forceinline__ void pipe_produce(Pipe &p, int slot, int cta, int war
     }
 }
 
-// Lane 0: bring this warp's tiles of one linear step into L2 (bulk
-// prefetches of up to CH tiles; they return no data).
+// Lane 0: bring this warp's tiles of one linear step into L2 with bulk
+// prefetches of up to CH tiles (they return no data), from cursor q on.
 template <int NT>
-__device__ __forceinline__ void prefetch_l2(const GroupArgs &a, int cta, int warp) {
+__device__ __forceinline__ void prefetch_from(const GroupArgs &a, Cursor q, int qg, const char *qr,
+                                              int cu0, int cu1, int sig1, int warp) {
     constexpr int CH = chunk_tiles(NT);
-    if (a.kind != kStepLinear || cta >= a.P) return;
-    int cu0, cu1, sig0, sig1;
-    cta_units(a, cta, cu0, cu1, sig0, sig1);
-    Cursor q;
-    q.sigma = sig0;
-    if (!cursor_enter(a, cu0, cu1, sig1, warp, q)) return;
-    int qg = 0;
-    const char *qr = row_base(a, q.r, qg);
     for (bool on = true; on;) {
         const int n = min(CH, min(q.uend - q.u, q.kw - q.b));
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qr + (long long)(q.kb0 + q.b) * 512),
@@ -707,6 +707,28 @@ __device__ __forceinline__ void prefetch_l2(const GroupArgs &a, int cta, int war
     }
 }
 
+// All of this warp's tiles of a (later) step of a chain.
+template <int NT>
+__device__ __forceinline__ void prefetch_l2(const GroupArgs &a, int cta, int warp) {
+    if (a.kind != kStepLinear || cta >= a.P) return;
+    int cu0, cu1, sig0, sig1;
+    cta_units(a, cta, cu0, cu1, sig0, sig1);
+    Cursor q;
+    q.sigma = sig0;
+    if (!cursor_enter(a, cu0, cu1, sig1, warp, q)) return;
+    int qg = 0;
+    const char *qr = row_base(a, q.r, qg);
+    prefetch_from<NT>(a, q, qg, qr, cu0, cu1, sig1, warp);
+}
+
+// The rest of this warp's tiles of the pipe's current step: those after
+// the chunks its first copies took.
+template <int NT>
+__device__ __forceinline__ void prefetch_rest(const Pipe &p, const GroupArgs &a, int warp) {
+    if (p.pc_on && p.pstep == 0)
+        prefetch_from<NT>(a, p.pc, p.pgi, p.prow, p.pcu0, p.pcu1, p.psig1, warp);
+}
+
 // Lane 0, after a wait gave up: let the copies still in flight land
 // (bounded) before the CTA leaves.
 __device__ __forceinline__ void pipe_drain(const Pipe &p, int *status) {
@@ -720,19 +742,29 @@ __device__ __forceinline__ void pipe_start(Pipe &p, int cta, int warp) {
     for (int k = 0; k < kSlots; ++k) mbar_init(p.bar_w + 8u * k, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     pipe_seek(p, cta, warp);
-    for (int k = 0; k < kSlots && p.pc_on; ++k) pipe_produce<NT>(p, k, cta, warp);
+    for (int k = 0; k < kSlots && p.pc_on; ++k) pipe_produce<NT>(p, p.steps[p.pstep], k, cta, warp);
 }
 
-// Bounded wait of one thread until *word != 0, then an acquire fence (the
-// polls are relaxed loads, so waiting CTAs do not order anything until the
-// word is seen).  Gives up, returning false, when another CTA has set the
+// Bounded wait of one thread until *word reaches `target` (64-bit), or,
+// with `nonzero`, until the 32-bit word is non-zero; then an acquire fence
+// (the polls are relaxed loads, so waiting CTAs order nothing until the
+// value is seen).  Gives up, returning false, when another CTA has set the
 // status word or after `limit` SM cycles (and then sets the status word).
-__device__ __forceinline__ bool wait_word(const unsigned *word, long long limit, int *status) {
+__device__ __forceinline__ bool wait_word(const void *word, unsigned long long target, bool nonzero,
+                                          long long limit, int *status) {
     const long long t0 = clock64();
     for (unsigned it = 0;; ++it) {
-        unsigned v;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
-        if (v != 0u) {
+        bool ok;
+        if (nonzero) {
+            unsigned v;
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+            ok = v != 0u;
+        } else {
+            unsigned long long v;
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(word) : "memory");
+            ok = v >= target;
+        }
+        if (ok) {
             asm volatile("fence.acq_rel.gpu;" ::: "memory");
             return true;
         }
@@ -749,28 +781,28 @@ __device__ __forceinline__ bool wait_word(const unsigned *word, long long limit,
 }
 
 // Wait (thread 0) for step `step`'s inputs: the gate before step 0, else
-// step - 1's completion flag.
-__device__ __forceinline__ bool wait_inputs(const ChainHeader *ch, int step, int *status) {
-    if (step == 0) return ch->gate == nullptr || wait_word(ch->gate, ch->wait_limit, status);
-    return wait_word(ch->done + step - 1, ch->wait_limit, status);
+// all prevP CTAs of step - 1 in this pass.  The counters only grow: after
+// `epoch` completed passes, step i is done in this pass when its counter
+// reaches (epoch + 1) * P_i.
+__device__ __forceinline__ bool wait_inputs(const ChainHeader *ch, int step, unsigned long long epoch,
+                                            unsigned prevP, int *status) {
+    if (step == 0) return ch->gate == nullptr || wait_word(ch->gate, 0ull, true, ch->wait_limit, status);
+    return wait_word(ch->cnt + step - 1, (epoch + 1) * prevP, false, ch->wait_limit, status);
 }
 
 // Count this CTA into step `step` (thread 0, after a barrier that follows
-// the CTA's last write of the step).  The CTA that completes the count
-// publishes the step's flag, and clears the counter and the flag of the
-// step before, which every CTA of this step has already seen (and, after
-// the last step, that step's own flag), so both are zero when the launch ends.
-__device__ __forceinline__ void signal_step(const ChainHeader *ch, int step, unsigned P) {
+// the CTA's last write of the step): one release reduction, no reply awaited.
+__device__ __forceinline__ void signal_step(const ChainHeader *ch, int step) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ch->cnt + step) : "memory");
+}
+
+// Leaving a pass (thread 0 of every CTA): the last CTA out advances the
+// pass count, which the next launch reads at its start.
+__device__ __forceinline__ void leave_pass(const ChainHeader *ch, unsigned long long epoch) {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    const unsigned n = atomicAdd(ch->cnt + step, 1u) + 1u;
-    if (n != P) return;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    ch->cnt[step] = 0u;
-    if (step > 0) ch->done[step - 1] = 0u;
-    if (step + 1 < ch->nsteps) {
-        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ch->done + step), "r"(1u) : "memory");
-    } else {
-        ch->done[step] = 0u;
+    if (atomicAdd(ch->epoch + 1, 1ull) + 1ull == (unsigned long long)gridDim.x) {
+        ch->epoch[1] = 0ull;
+        ch->epoch[0] = epoch + 1ull;
     }
 }
 
@@ -786,18 +818,19 @@ struct StepSmem {
     int emax[NT];
     int redo;                          // tokens outside the fixed window (bit mask)
     int go;                            // the step's inputs are ready
+    unsigned long long epoch;          // chain passes completed before this one
 };
 
 // ------------------------------------------------------------ one linear step
 // kModeA: bf16 activations (else int8 from the quantiser).  NT: token
 // columns staged (a power of two >= N).  kChain: the step is one of a chain
-// run by one persistent launch; it waits for step - 1's completion flag
-// instead of for the previous kernel.  Returns, the
+// run by one persistent launch; it waits for the prevP CTAs of step - 1
+// (the chain's counters) instead of for the previous kernel.  Returns, the
 // same in every thread of the CTA, whether every wait succeeded.
 template <bool kModeA, int NT, bool kChain>
 __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *smem,
                                          StepSmem<NT> &sh, Pipe &pipe, const ChainHeader *ch,
-                                         int step) {
+                                         int step, unsigned prevP) {
     constexpr int CH = chunk_tiles(NT);         // tiles per bulk copy
     constexpr int SLOT = CH * 512;
     constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
@@ -878,12 +911,12 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
     if (!kChain) {
         griddep_wait();
     } else {
-        if (threadIdx.x == 0) sh.go = wait_inputs(ch, step, a.status);
+        if (threadIdx.x == 0) sh.go = wait_inputs(ch, step, sh.epoch, prevP, a.status);
         __syncthreads();
         if (!sh.go) return false;
     }
     uint4 xv[SB];
-    if (!(kAsyncX && a.xvec)) stage_load<kModeA, SB>(a, P, 0, xv);
+    if (!(kAsyncX && a.xvec)) stage_load<kModeA, SB, kChain>(a, P, 0, xv);
 
     Cursor cc;
     cc.sigma = sig0;
@@ -956,7 +989,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                 }
             } else
             for (int base = 0; base < total; base += kThreads * SB) {
-                if (sigma != sig0 || base != 0) stage_load<kModeA, SB>(a, P, base, xv);
+                if (sigma != sig0 || base != 0) stage_load<kModeA, SB, kChain>(a, P, base, xv);
 #pragma unroll
                 for (int i = 0; i < SB; ++i) {
                     if (base + i * kThreads >= total) break;   // uniform over the block
@@ -1142,7 +1175,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                 pipe.inflight &= ~(1u << slot);
                 if (pipe.pc_on) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    pipe_produce<NT>(pipe, slot, cta, warp);
+                    pipe_produce<NT>(pipe, kChain ? pipe.steps[pipe.pstep] : a, slot, cta, warp);
                 }
             }
             cc.u += n;
@@ -1275,9 +1308,9 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     // launch waits for it.
     if (lane == 0) {
         pipe_start<NT>(pipe, blockIdx.x, warp);
-        prefetch_l2<NT>(a, blockIdx.x, warp);
+        prefetch_rest<NT>(pipe, a, warp);
     }
-    const bool ok = run_step<kModeA, NT, false>(a, blockIdx.x, smem, sh, pipe, nullptr, 0);
+    const bool ok = run_step<kModeA, NT, false>(a, blockIdx.x, smem, sh, pipe, nullptr, 0, 0u);
     if (!ok && lane == 0) pipe_drain(pipe, a.status);
 }
 
@@ -1451,6 +1484,11 @@ tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict_
         pipe_start<NT>(pipe, cta, warp);
         for (int k = 0; k < ahead && k < nsteps; ++k) prefetch_l2<NT>(steps[k], cta, warp);
     }
+    if (threadIdx.x == 0) {
+        unsigned long long e;
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(e) : "l"(ch->epoch) : "memory");
+        sh.epoch = e;
+    }
     bool ok = true;
     int *status = nullptr;
     for (int step = 0; step < nsteps; ++step) {
@@ -1461,10 +1499,11 @@ tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict_
         __syncthreads();
         status = sa.status;
         if (cta >= sa.P) continue;
+        const unsigned prevP = step > 0 ? (unsigned)steps[step - 1].P : 0u;
         if (sa.kind == kStepLinear) {
-            ok = run_step<kModeA, NT, true>(sa, cta, smem, sh, pipe, ch, step);
+            ok = run_step<kModeA, NT, true>(sa, cta, smem, sh, pipe, ch, step, prevP);
         } else {
-            if (threadIdx.x == 0) sh.go = wait_inputs(ch, step, sa.status);
+            if (threadIdx.x == 0) sh.go = wait_inputs(ch, step, sh.epoch, prevP, sa.status);
             __syncthreads();
             ok = sh.go != 0;
             if (ok) {
@@ -1476,9 +1515,11 @@ tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict_
         if (!ok) break;
         // the step's results are written: count this CTA in
         __syncthreads();
-        if (threadIdx.x == 0) signal_step(ch, step, (unsigned)sa.P);
+        if (threadIdx.x == 0) signal_step(ch, step);
     }
     if (!ok && lane == 0) pipe_drain(pipe, status);
+    __syncthreads();
+    if (threadIdx.x == 0) leave_pass(ch, sh.epoch);
 }
 
 using ChainFn = void (*)(const ChainHeader *, const GroupArgs *);
@@ -1746,7 +1787,7 @@ static_assert(sizeof(GroupArgs) % 4 == 0, "steps are copied as words");
 // launches), then scratch: split-K pieces and, in mode B, the quantised
 // activations of the current step.
 struct ChainLayout {
-    size_t steps_off, done_off, cnt_off, xslot_off, part_off, q_off, s_off, z_off, bytes, front;
+    size_t epoch_off, steps_off, cnt_off, xslot_off, part_off, q_off, s_off, z_off, bytes, front;
     int kwr, rowsr, grid, total;
 };
 
@@ -1775,9 +1816,9 @@ tl_status chain_layout(const tl_chain_step *st, int nsteps, int N, int mode, int
             L->grid = std::max(L->grid, (int)ceil_div(st[i].Ws[0].K, kQChunk) * N);
     }
     L->total = mode == TL_MODE_I8 ? 2 * nsteps : nsteps;
-    L->steps_off = tl_internal::kStatusBytes;
-    L->done_off = L->steps_off + round256((size_t)L->total * 4);
-    L->cnt_off = L->done_off + round256((size_t)L->total * 4);
+    L->epoch_off = tl_internal::kStatusBytes;
+    L->steps_off = L->epoch_off + 256;
+    L->cnt_off = L->steps_off + round256((size_t)L->total * 8);
     L->xslot_off = L->cnt_off + cnt_b;
     L->front = L->xslot_off + xslot_b;
     L->part_off = L->front;
@@ -2032,8 +2073,8 @@ tl_status tl_chain_encode(const tl_chain_step *steps, int nsteps, int N, int mod
         return TL_ERR_CUDA;
     if ((long long)per_sm * dev->sms < L.grid) return TL_ERR_UNSUPPORTED;
     ChainHostHead &h = *reinterpret_cast<ChainHostHead *>(img);
-    h.hdr.cnt = reinterpret_cast<unsigned *>(ws + L.steps_off);
-    h.hdr.done = reinterpret_cast<unsigned *>(ws + L.done_off);
+    h.hdr.cnt = reinterpret_cast<unsigned long long *>(ws + L.steps_off);
+    h.hdr.epoch = reinterpret_cast<unsigned long long *>(ws + L.epoch_off);
     h.hdr.gate = gate;
     h.hdr.wait_limit = wait_limit > 0 ? wait_limit : kWaitLimit;
     h.hdr.nsteps = L.total;

@@ -36,7 +36,8 @@ TL_MAX_GROUP = 4
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
            "tl_decode_plan", "tl_quantize_act", "tl_linear", "tl_linear_group",
            "tl_head_workspace_bytes", "tl_head_argmax", "tl_embed",
-           "tl_rmsnorm_quant", "tl_swiglu_quant",
+           "tl_rmsnorm_quant", "tl_swiglu_quant", "tl_ternarize_absmean",
+           "tl_linear_blockscale",
            "tl_chain_image_bytes", "tl_chain_workspace_bytes", "tl_chain_encode",
            "tl_chain_run", "tl_linear_noalloc", "tl_status_string", "tl_version")
 TL_MAX_CHAIN = 4096
@@ -84,6 +85,10 @@ _lib.tl_rmsnorm_quant.argtypes = [_p, _p, C.c_float, _int, _int, _p, _p, _p, _p,
 _lib.tl_rmsnorm_quant.restype = _int
 _lib.tl_swiglu_quant.argtypes = [_p, _p, _int, _int, _p, _p, _p, _p, _int, _p]
 _lib.tl_swiglu_quant.restype = _int
+_lib.tl_ternarize_absmean.argtypes = [_p, _i64, _i64, _p, _p]
+_lib.tl_ternarize_absmean.restype = _int
+_lib.tl_linear_blockscale.argtypes = [_p, _p, _int, _int, _p, _int, _p, _int, C.c_uint, _p]
+_lib.tl_linear_blockscale.restype = _int
 _lib.tl_chain_image_bytes.argtypes = [_int, _int]
 _lib.tl_chain_image_bytes.restype = _sz
 _lib.tl_chain_workspace_bytes.argtypes = [C.POINTER(tl_chain_step), _int, _int, _int]
@@ -147,6 +152,18 @@ def tl_pack(W: np.ndarray, scale: np.ndarray | None = None):
     return packed[: tl_packed_bytes(M, K) // 4], scale_out, rowsum
 
 
+def tl_ternarize_absmean(W: np.ndarray):
+    """Host: float W [M, K] -> (int8 ternary codes, fp32 scale per (row,
+    128-column block)) by the block's mean |w|."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    M, K = W.shape
+    T = np.zeros((M, K), dtype=np.int8)
+    bs = np.zeros((M, (K + 127) // 128), dtype=np.float32)
+    _check(_lib.tl_ternarize_absmean(_np_ptr(W), M, K, _np_ptr(T), _np_ptr(bs)),
+           "tl_ternarize_absmean")
+    return T, bs
+
+
 def tl_validate_packed(packed: np.ndarray, M: int, K: int) -> int:
     """Host validator: number of invalid codes / non-zero padding weights."""
     packed = np.ascontiguousarray(packed, dtype=np.uint32)
@@ -196,6 +213,38 @@ class TernaryWeight:
     def struct(self) -> tl_weight:
         return tl_weight(self.packed.data_ptr(), self.scale.data_ptr(), self.rowsum.data_ptr(),
                          self.M, self.K, TL_LAYOUT_TL2P_V2)
+
+
+@dataclass
+class BlockScaledWeight:
+    """Packed ternary codes with one scale per (row, 128-column block)."""
+    packed: "object"   # torch.int32 tensor, tl_packed_bytes(M, K) bytes
+    bscale: "object"   # torch.float32 [M, ceil(K / 128)]
+    M: int
+    K: int
+
+    @classmethod
+    def from_float(cls, W: np.ndarray, device="cuda") -> "BlockScaledWeight":
+        torch = _torch()
+        T, bs = tl_ternarize_absmean(W)
+        packed, _, _ = tl_pack(T)
+        return cls(torch.from_numpy(packed.view(np.int32)).to(device),
+                   torch.from_numpy(bs).to(device), W.shape[0], W.shape[1])
+
+
+def tl_linear_blockscale(weight: BlockScaledWeight, X, out=None, out_dtype: int = TL_OUT_F32,
+                         flags: int = 0, stream=None):
+    """y = sum over blocks of scale[m, b] * block sum, bf16 X [N, K]."""
+    torch = _torch()
+    N = X.shape[0]
+    if out is None:
+        dt = torch.float32 if out_dtype == TL_OUT_F32 else torch.bfloat16
+        out = torch.empty((N, weight.M), dtype=dt, device=X.device)
+    st = _lib.tl_linear_blockscale(weight.packed.data_ptr(), weight.bscale.data_ptr(), weight.M,
+                                   weight.K, X.data_ptr(), N, out.data_ptr(), out_dtype, flags,
+                                   _stream_ptr(stream))
+    _check(st, "tl_linear_blockscale")
+    return out
 
 
 def _structs(ws):

@@ -186,6 +186,31 @@ TL_API tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, cons
                           int out_dtype, void *workspace, size_t workspace_bytes,
                           unsigned flags, void *stream);
 
+/* ---------------------------------------------------------------- block-wise scales
+ * The blog ("Neutrino-1: quantization is a training decision", "What's
+ * actually ternary") describes blocks of weights with one higher-precision
+ * scale each, the codes being round(clamp(w / scale, -1, 1)) with scale the
+ * block's mean |w|.  Here a block is TL_SCALE_BLOCK = 128 consecutive
+ * columns of one row (the TL2P tile width; the pages give no size); the
+ * last block of a row may be shorter. */
+#define TL_SCALE_BLOCK 128
+
+/* HOST.  Ternarise float W [M][K] by blocks: bscale[m][b] = mean of |W| over
+ * the block's columns (taken in double, stored fp32), T[m][k] =
+ * rint(clamp(W / bscale, -1, 1)) (in double, ties to even; 0 where the
+ * block is all zero).  bscale has ceil(K / 128) entries per row.  Pack T
+ * with tl_pack.  TL_ERR_BAD_VALUE for a non-finite weight. */
+TL_API tl_status tl_ternarize_absmean(const float *W, int64_t M, int64_t K, int8_t *T,
+                                      float *bscale);
+
+/* DEVICE.  y[n][m] = sum_b bscale[m][b] * sum_{k in block b} w[m][k] * x[n][k]
+ * on TL2P v2 codes (16-byte aligned), bscale fp32 [M][ceil(K/128)], X bf16
+ * [N][K] (any N, run in chunks of 8), Y fp32 or bf16 [N][M].  fp32 sums
+ * (bf16 products are exact).  Needs no workspace.  flags: 0 or TL_FLAG_PDL. */
+TL_API tl_status tl_linear_blockscale(const uint32_t *packed, const float *bscale, int M, int K,
+                                      const void *X, int N, void *Y, int out_dtype,
+                                      unsigned flags, void *stream);
+
 /* ---------------------------------------------------------------- int8 head and embedding
  * The projections are ternary, but the token embedding and the output head
  * stay int8 with one higher-precision scale per row (blog "Neutrino-1:
@@ -262,16 +287,17 @@ TL_API tl_status tl_swiglu_quant(const void *G, const void *U, int N, int M, voi
  * names every pointer of the chain; the caller copies it to device memory
  * (16-byte aligned) once and calls tl_chain_run(host image, device image,
  * stream) for every pass.  The workspace (tl_chain_workspace_bytes,
- * 256-byte aligned, zero-filled before first use) belongs to that chain: it
- * holds the status word (its first int32), per-step arrival counters and
- * completion flags and split-K state, all zero again after each completed
- * pass, and scratch.  Passes of
- * one chain must not overlap on the GPU.
+ * 256-byte aligned, zero-filled before the first pass) belongs to that
+ * chain: it holds the status word (its first int32), a count of completed
+ * passes and per-step arrival counters that only grow from pass to pass,
+ * split-K state that every pass leaves zero, and scratch.  Passes of one
+ * chain must not overlap on the GPU.
  * Errors on the device: a wait for a step's inputs gives up after
  * wait_limit SM cycles (0: about a second) and writes a non-zero status
  * word; the other CTAs then stop too.  Read the word after the stream has
  * passed the run; if it is non-zero the outputs are invalid (treat it as
- * TL_ERR_TIMEOUT) and the workspace must be zero-filled again. */
+ * TL_ERR_TIMEOUT) and the workspace must be zero-filled again before the
+ * next pass. */
 #define TL_MAX_CHAIN 4096
 
 typedef struct {

@@ -54,6 +54,10 @@ def load(path: str) -> C.CDLL:
     L.oracle_rmsnorm.restype = None
     L.oracle_swiglu.argtypes = [p, p, i64, i64, p]
     L.oracle_swiglu.restype = None
+    L.oracle_absmean_ternarize.argtypes = [p, i64, i64, p, p]
+    L.oracle_absmean_ternarize.restype = None
+    L.oracle_linear_blockscale.argtypes = [p, p, i64, i64, p, i64, p]
+    L.oracle_linear_blockscale.restype = None
     return L
 
 
@@ -204,6 +208,26 @@ def swiglu(G, U):
     H = np.zeros((N, M), dtype=np.float64)
     lib().oracle_swiglu(_ptr(G), _ptr(U), N, M, _ptr(H))
     return H
+
+
+def absmean_ternarize(Wf):
+    """float W [M, K] -> (int8 ternary W, fp32 scale per (row, 128-column block))."""
+    Wf = _c(Wf, np.float32)
+    M, K = Wf.shape
+    KB = (K + 127) // 128
+    T = np.zeros((M, K), dtype=np.int8)
+    bs = np.zeros((M, KB), dtype=np.float32)
+    lib().oracle_absmean_ternarize(_ptr(Wf), M, K, _ptr(T), _ptr(bs))
+    return T, bs
+
+
+def linear_blockscale(P, bscale, M: int, K: int, X):
+    """y = sum over 128-column blocks of scale[m, b] * block sum, fp32 [N, M]."""
+    P = _c(P, np.uint32); bscale = _c(bscale, np.float32); X = _c(X, np.uint16)
+    N = X.shape[0]
+    Y = np.zeros((N, M), dtype=np.float32)
+    lib().oracle_linear_blockscale(_ptr(P), _ptr(bscale), M, K, _ptr(X), N, _ptr(Y))
+    return Y
 
 
 def host_cores() -> int:

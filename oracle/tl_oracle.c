@@ -443,3 +443,61 @@ void oracle_swiglu(const uint16_t *G, const uint16_t *U, int64_t N, int64_t M, d
         H[i] = g / (1.0 + exp(-g)) * u;
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Block-wise scales and the absmean ternariser                         */
+/* ------------------------------------------------------------------ */
+/*
+ * The blog ("Neutrino-1: quantization is a training decision", "What's
+ * actually ternary") describes each block of weights carrying its own
+ * higher-precision scale, the ternary code being round(clamp(w / scale,
+ * -1, 1)) with scale the block's mean absolute value.  Reading: a block is
+ * 128 consecutive columns of one row (the last block of a row may be
+ * shorter); the mean is taken in double over the block's real columns and
+ * stored as fp32; the code is rint(clamp(w / scale, -1, 1)) with that fp32
+ * scale, in double, ties to even; a block of zeros gets scale 0 and codes 0.
+ *   y[n,m] = sum_b scale[m,b] * sum_{k in b} w[m,k] * x[n,k]
+ * taken in double and rounded once to fp32.
+ */
+#define TL_BLOCK 128
+
+void oracle_absmean_ternarize(const float *W, int64_t M, int64_t K, int8_t *T, float *bscale)
+{
+    int64_t KB = (K + TL_BLOCK - 1) / TL_BLOCK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < KB; ++b) {
+            int64_t k0 = b * TL_BLOCK, k1 = k0 + TL_BLOCK < K ? k0 + TL_BLOCK : K;
+            double sum = 0.0;
+            for (int64_t k = k0; k < k1; ++k) sum += fabs((double)W[m * K + k]);
+            float scale = (float)(sum / (double)(k1 - k0));
+            bscale[m * KB + b] = scale;
+            for (int64_t k = k0; k < k1; ++k) {
+                double r = scale > 0.0f ? (double)W[m * K + k] / (double)scale : 0.0;
+                if (r > 1.0) r = 1.0;
+                if (r < -1.0) r = -1.0;
+                T[m * K + k] = (int8_t)rint(r);
+            }
+        }
+}
+
+void oracle_linear_blockscale(const uint32_t *P, const float *bscale, int64_t M, int64_t K,
+                              const uint16_t *X, int64_t N, float *Y)
+{
+    int64_t Kp = pad128(K), KB = (K + TL_BLOCK - 1) / TL_BLOCK;
+    int8_t *w = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) w[k] = (int8_t)oracle_weight(P, m, k, Kp, NULL);
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t *xn = X + n * K;
+            double y = 0.0;
+            for (int64_t b = 0; b < KB; ++b) {
+                int64_t k0 = b * TL_BLOCK, k1 = k0 + TL_BLOCK < K ? k0 + TL_BLOCK : K;
+                double s = 0.0;
+                for (int64_t k = k0; k < k1; ++k) s += (double)w[k] * (double)bf16_to_float(xn[k]);
+                y += (double)bscale[m * KB + b] * s;
+            }
+            Y[n * M + m] = (float)y;
+        }
+    }
+    free(w);
+}

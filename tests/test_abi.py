@@ -183,3 +183,22 @@ def test_head_arguments_checked_without_a_gpu():
     assert f(p + 8, p, 10, 64, p, p, p, 1, None, p, p, p, 1 << 20, 0, None) == tl.TL_ERR_ALIGN
     assert f(p, p, 10, 64, p, p, p, 1, None, p, p, None, 1 << 20, 0, None) == tl.TL_ERR_WORKSPACE
     assert tl._lib.tl_embed(None, p, 10, 64, p, 1, p, None) == tl.TL_ERR_NULL
+
+
+@pytest.mark.parametrize("M,K", [(7, 300), (64, 128), (33, 1000)])
+def test_absmean_ternarizer_matches_oracle(oracle_mod, M, K):
+    """The library's host ternariser gives the oracle's codes and scales bit
+    for bit (both follow the same reading: double mean, fp32 scale, double
+    ratio, ties to even)."""
+    rng = np.random.default_rng(M * K)
+    W = (rng.standard_normal((M, K)) * rng.uniform(0.01, 3.0, size=(M, 1))).astype(np.float32)
+    W[0, :128] = 0.0                                    # an all-zero block
+    W[1, 5] = 1e6                                       # a block dominated by one value
+    T, bs = tl.tl_ternarize_absmean(W)
+    To, bso = oracle_mod.absmean_ternarize(W)
+    assert np.array_equal(T, To)
+    assert np.array_equal(bs.view(np.uint32), bso.view(np.uint32))
+    bad = W.copy()
+    bad[2, 3] = np.nan
+    with pytest.raises(tl.TLError):
+        tl.tl_ternarize_absmean(bad)

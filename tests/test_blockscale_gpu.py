@@ -1,0 +1,46 @@
+"""GPU: the block-wise scale variant (one scale per row and 128-column
+block, codes from the absmean ternariser) against the CPU oracle, within
+the mode-A tolerance of the other parity tests."""
+import numpy as np
+import pytest
+
+from bit_matvec_ternary_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU machine
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from bit_matvec_ternary_b300 import tl  # noqa: E402
+from tests.test_parity_gpu import TOL_A, bf16_tensor, rel_err  # noqa: E402
+
+
+def _weights(oracle_mod, M, K, seed):
+    rng = np.random.default_rng(seed)
+    Wf = (rng.standard_normal((M, K)) * rng.uniform(0.01, 0.1, size=(M, 1))).astype(np.float32)
+    w = tl.BlockScaledWeight.from_float(Wf)
+    T, bs = oracle_mod.absmean_ternarize(Wf)
+    return w, oracle_mod.pack(T), bs
+
+
+@pytest.mark.parametrize("M,K", [(2048, 1024), (4096, 4096), (777, 333), (4096, 12288),
+                                 (12288, 4096), (16, 128), (5, 1000)])
+@pytest.mark.parametrize("N", [1, 8, 13])
+def test_blockscale_against_oracle(oracle_mod, M, K, N):
+    w, P, bs = _weights(oracle_mod, M, K, M + K)
+    X = synth.activations(N, K, seed=N + K, outlier_frac=0.01)
+    Y = tl.tl_linear_blockscale(w, bf16_tensor(X)).cpu().numpy()
+    ref = oracle_mod.linear_blockscale(P, bs, M, K, X)
+    assert rel_err(Y, ref) <= TOL_A
+
+
+def test_blockscale_one_signed_activations_and_bf16_output(oracle_mod):
+    M, K = 2048, 12288
+    w, P, bs = _weights(oracle_mod, M, K, 3)
+    X = synth.to_bf16_bits(np.abs(np.random.default_rng(4).standard_normal((8, K))).astype(np.float32))
+    ref = oracle_mod.linear_blockscale(P, bs, M, K, X)
+    Y = tl.tl_linear_blockscale(w, bf16_tensor(X)).cpu().numpy()
+    assert rel_err(Y, ref) <= TOL_A
+    Yb = tl.tl_linear_blockscale(w, bf16_tensor(X), out_dtype=tl.TL_OUT_BF16).float().cpu().numpy()
+    assert rel_err(Yb, ref) <= TOL_A + 2.0 ** -8

@@ -496,3 +496,51 @@ def test_swiglu_identities(oracle_mod):
     big = synth.to_bf16_bits(np.float32([[60.0, -60.0]]))
     h = oracle_mod.swiglu(big, synth.to_bf16_bits(np.float32([[1.0, 1.0]])))
     assert abs(h[0, 0] - 60.0) < 1e-20 and abs(h[0, 1]) < 1e-24
+
+
+# ---------------------------------------------------------------- block scales
+
+def test_absmean_closed_forms(oracle_mod):
+    """Hand-derived blocks.  +-c everywhere: scale c, codes sign(w).  60 ones
+    and 16 quarters (+-) in 128 columns: scale (60 + 4) / 128 = 0.5 exactly,
+    ones give 2 -> clamped to 1, quarters give +-0.5 -> ties to even: 0.
+    A short last block (44 columns) has its own mean.  Zeros: scale 0,
+    codes 0."""
+    M, K = 3, 300                       # blocks of 128, 128 and 44 columns
+    W = np.zeros((M, K), dtype=np.float32)
+    rng = np.random.default_rng(1)
+    W[0] = np.where(rng.random(K) < 0.5, 2.0, -2.0)
+    W[1, :60] = 1.0
+    W[1, 60:68] = 0.25
+    W[1, 68:76] = -0.25
+    W[1, 256:300] = 3.0                 # the 44-column block: scale 3, codes 1
+    W[1, 299] = -3.0
+    T, bs = oracle_mod.absmean_ternarize(W)
+    assert np.all(bs[0] == 2.0) and np.array_equal(T[0], np.sign(W[0]).astype(np.int8))
+    assert bs[1].tolist() == [0.5, 0.0, 3.0]
+    assert np.all(T[1, :60] == 1) and not T[1, 60:256].any()
+    assert np.all(T[1, 256:299] == 1) and T[1, 299] == -1
+    assert bs[2].tolist() == [0.0, 0.0, 0.0] and not T[2].any()
+    T2, bs2 = oracle_mod.absmean_ternarize(np.float32([[1.0, 0.5, -0.5, 0.0]]))   # scale 0.5
+    assert bs2.tolist() == [[0.5]] and T2.tolist() == [[1, 1, -1, 0]]
+
+
+@pytest.mark.parametrize("M,K,N", [(16, 128, 1), (37, 300, 3), (5, 1000, 2)])
+def test_blockscale_linear_matches_dense(oracle_mod, M, K, N):
+    """Against numpy float64: sum over blocks of scale * (x_block @ w_block)."""
+    rng = np.random.default_rng(M + K)
+    Wf = rng.standard_normal((M, K)).astype(np.float32)
+    T, bs = oracle_mod.absmean_ternarize(Wf)
+    P = oracle_mod.pack(T)
+    X = _x(N, K, seed=K)
+    Y = oracle_mod.linear_blockscale(P, bs, M, K, X)
+    xf = _f(X).astype(np.float64)
+    ref = np.zeros((N, M))
+    for b in range(bs.shape[1]):
+        sl = slice(128 * b, min(K, 128 * b + 128))
+        ref += (xf[:, sl] @ T[:, sl].astype(np.float64).T) * bs[:, b].astype(np.float64)[None, :]
+    assert np.allclose(Y, ref, rtol=1e-6, atol=1e-30)
+    # one scale for every block reduces to the per-row linear
+    ones = np.ones_like(bs)
+    Y1 = oracle_mod.linear_blockscale(P, ones, M, K, X)
+    assert np.array_equal(Y1, oracle_mod.linear_a(P, np.ones(M, np.float32), M, K, X))

@@ -54,6 +54,9 @@ MUTATIONS = {
     "rmsnorm_without_eps": ("double r = 1.0 / sqrt(ss / (double)K + eps);",
                             "double r = 1.0 / sqrt(ss / (double)K);"),
     "swiglu_sign": ("H[i] = g / (1.0 + exp(-g)) * u;", "H[i] = g / (1.0 + exp(g)) * u;"),
+    "absmean_ties_away": ("T[m * K + k] = (int8_t)rint(r);", "T[m * K + k] = (int8_t)round(r);"),
+    "absmean_no_clamp": ("if (r > 1.0) r = 1.0;", "if (r > 2.0) r = 2.0;"),
+    "blockscale_wrong_block": ("y += (double)bscale[m * KB + b] * s;", "y += (double)bscale[m * KB] * s;"),
     "int_acc_dropped_term": ("for (int64_t k = 0; k < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];",
                              "for (int64_t k = 0; k + 1 < K; ++k) acc += (int64_t)w[k] * (int64_t)Q[n * K + k];"),
 }
@@ -85,6 +88,9 @@ def _pins():
         ("embed", lambda: T.test_embed_rows_times_scale(o)),
         ("rmsnorm", lambda: T.test_rmsnorm_identities(o)),
         ("swiglu", lambda: T.test_swiglu_identities(o)),
+        ("absmean", lambda: T.test_absmean_closed_forms(o)),
+        ("blockscale", lambda: [T.test_blockscale_linear_matches_dense(o, M, K, N)
+                                for M, K, N in ((16, 128, 1), (37, 300, 3), (5, 1000, 2))]),
     ]
 
 
