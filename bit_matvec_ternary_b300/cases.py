@@ -4,8 +4,10 @@
 
 Cases are the launch groups of one 8B-shaped decoder layer: qkv (q/k/v
 grouped, K = 4096), o, gate_up (gate/up grouped), down (K = 12288), quant
-(the activation quantiser, K = 12288), and chain (the first `--layers`
-layers of the 8B stack as one persistent chain launch).  Each is built from the same seeded
+(the activation quantiser, K = 12288), chain (the first `--layers`
+layers of the 8B stack as one persistent chain launch), stack (the same
+layers as the benchmark's CUDA graph of per-group launches), and head (the
+151,936 x 4,096 int8 head with its fused argmax).  Each is built from the same seeded
 synthetic inputs as the benchmark and launched `reps` times back to back
 after `warmup` launches, then the process checks nothing and exits 0.
 """
@@ -23,7 +25,7 @@ CASE_GROUPS = {"qkv": 0, "o": 1, "gate_up": 2, "down": 3}
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant", "chain"])
+    ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant", "chain", "stack", "head"])
     ap.add_argument("--n", type=int, default=1)
     ap.add_argument("--mode", default="a", choices=["a", "b"])
     ap.add_argument("--reps", type=int, default=3)
@@ -40,6 +42,28 @@ def main() -> None:
     shape = synth.NEUTRINO_8B
     shp = shape.linear_shapes()
     mode = tl.TL_MODE_BF16 if args.mode == "a" else tl.TL_MODE_I8
+    if args.case == "stack":
+        from .stack import LinearStack
+        st = LinearStack(shape, N=args.n, mode=mode, layers=args.layers)
+        st.capture()
+        for _ in range(args.warmup + args.reps):
+            st.graph.replay()
+        torch.cuda.synchronize()
+        return
+    if args.case == "head":
+        V, D = 151_936, 4096
+        g = torch.Generator(device="cuda")
+        g.manual_seed(1234)
+        H = torch.randint(-128, 128, (V, D), dtype=torch.int8, device="cuda", generator=g)
+        scale = torch.rand(V, device="cuda", generator=g) * 0.045 + 0.005
+        head = tl.Head(H, scale)
+        x = synth.activations(args.n, D, seed=55)
+        xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        q, s, z = tl.tl_quantize_act(xt)
+        for _ in range(args.warmup + args.reps):
+            head.argmax(q, s, z)
+        torch.cuda.synchronize()
+        return
     if args.case == "chain":
         from .stack import LinearStack
         st = LinearStack(shape, N=args.n, mode=mode, layers=args.layers)
