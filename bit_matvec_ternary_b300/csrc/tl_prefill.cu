@@ -284,6 +284,14 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         const int rt_base = mt * 8 + 2 * dw;
         const int rts = (a.M[gi] + 15) / 16;
         const char *pk = a.packed[gi];
+        // The weights do not depend on the previous kernel: bring this warp's
+        // two row tiles' whole K range into L2 first (their tiles are
+        // contiguous along K), so the loads below find them there.
+        if (lane < 2 && rt_base + lane < rts && NKB > 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                             pk + ((long long)(rt_base + lane) * a.KB + kb_lo) * 512),
+                         "r"((uint32_t)NKB * 512u)
+                         : "memory");
         // two TL2P tiles (one per row tile) per 128 columns; prefetch ring of 4
         constexpr int RING = 4;
         uint4 ring[RING][2];
@@ -435,9 +443,13 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     }
 }
 
-// int8 activations -> bf16 (exact) for the TMA operand of mode B.
+// int8 activations to bf16 (exact), the TMA operand of mode B.  It lets the prefill kernel that follows
+// start at once (that kernel decodes weights before it waits), and waits
+// itself for the kernel that wrote q.
 __global__ void tl_i8_to_bf16_kernel(const int8_t *__restrict__ q, __nv_bfloat16 *__restrict__ out,
                                      long long n) {
+    griddep_launch();
+    griddep_wait();
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long k = i; k < n; k += stride) out[k] = __float2bfloat16_rn((float)q[k]);
@@ -555,9 +567,20 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     a.part = reinterpret_cast<float *>(wsc + L.part);
     if (a.S > 1 && cudaMemsetAsync(a.cnt, 0, (size_t)tiles * 8, stream) != cudaSuccess)
         return TL_ERR_CUDA;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
     if (mode == TL_MODE_I8) {
-        tlp::tl_i8_to_bf16_kernel<<<592, 256, 0, stream>>>(static_cast<const int8_t *>(X), conv, n);
-        if (cudaGetLastError() != cudaSuccess) return TL_ERR_CUDA;
+        cudaLaunchConfig_t cc;
+        std::memset(&cc, 0, sizeof cc);
+        cc.gridDim = dim3(592);
+        cc.blockDim = dim3(256);
+        cc.stream = stream;
+        cc.attrs = pdl;
+        cc.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
+        if (cudaLaunchKernelEx(&cc, tlp::tl_i8_to_bf16_kernel, static_cast<const int8_t *>(X), conv,
+                               n) != cudaSuccess)
+            return TL_ERR_CUDA;
         xb = conv;
     }
     CUtensorMap map;
@@ -578,11 +601,9 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     cfg.blockDim = dim3(tlp::THREADS);
     cfg.dynamicSmemBytes = tlp::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (flags & TL_FLAG_PDL) && mode != TL_MODE_I8 ? 1 : 0;
+    // (mode B: the conversion kernel above, PDL-aware, is the one it follows)
+    cfg.attrs = pdl;
+    cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map) != cudaSuccess) return TL_ERR_CUDA;
     return TL_OK;
 }
