@@ -493,8 +493,11 @@ def main():
 
     extra = {}
     if not args.no_n8:
-        for mode, name, outl in ((tl.TL_MODE_BF16, "n8_mode_a", 0.01), (tl.TL_MODE_I8, "n8_mode_b", 0.01)):
-            st8 = LinearStack(shape, N=8, mode=mode, out_dtype=tl.TL_OUT_F32, outlier_frac=outl,
+        # mode B at eight tokens: a quantiser launch before each linear launch
+        # (the faster form here), with the quantisation fused into the linear
+        # launch (TL_MODE_I8_FUSED) and the chain beside it
+        for mode, name in ((tl.TL_MODE_BF16, "n8_mode_a"), (tl.TL_MODE_I8, "n8_mode_b")):
+            st8 = LinearStack(shape, N=8, mode=mode, out_dtype=tl.TL_OUT_F32, outlier_frac=0.01,
                               weights=weights)
             st8.capture()
             ms8 = time_graph(st8, args.steps, args.warmup, torch)
@@ -508,10 +511,16 @@ def main():
                                      "frac_of_hbm": a8 / (ms8c / 1e3) / 1e9 / hbm_peak}}
             del st8
             torch.cuda.empty_cache()
+        extra["n8_mode_b"]["fused"] = bench_stack_line(shape, 8, tl.TL_MODE_I8_FUSED, args, torch,
+                                                       tl, hbm_peak, weights=weights,
+                                                       outlier_frac=0.01)
 
-    # N = 1 in mode B (a quantiser launch in front of every linear launch)
-    extra["n1_mode_b"] = bench_stack_line(shape, 1, tl.TL_MODE_I8, args, torch, tl, hbm_peak,
-                                          weights=weights)
+    # N = 1 in mode B: quantisation inside each linear launch, and the
+    # two-launch form (a quantiser launch in front of every linear launch)
+    extra["n1_mode_b"] = bench_stack_line(shape, 1, tl.TL_MODE_I8_FUSED, args, torch, tl,
+                                          hbm_peak, weights=weights)
+    extra["n1_mode_b"]["two_launch"] = bench_stack_line(shape, 1, tl.TL_MODE_I8, args, torch, tl,
+                                                        hbm_peak, weights=weights)
     if not args.no_head:
         extra["head_argmax"] = bench_head(args, torch, tl, hbm_peak)
         torch.cuda.empty_cache()

@@ -307,7 +307,7 @@ __device__ __forceinline__ const char *row_base(const GroupArgs &a, int r, int &
 // Y[n][m] from acc = sum_k w*x (mode A) or the exact integer sum_k w*q (mode
 // B); sc = scale[m], rs = rowsum[m].
 __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int n, float acc,
-                                          float sc, int rs) {
+                                          float sc, int rs, const float *ts, const int32_t *tz) {
     const int M = a.M[gi];
     float y;
     if (a.mode == TL_MODE_BF16) {
@@ -318,8 +318,8 @@ __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int
             reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * M + m] = iacc;
             return;
         }
-        const int corrected = iacc - a.z[n] * rs;
-        y = __fmul_rn(__fmul_rn((float)corrected, a.s[n]), sc);
+        const int corrected = iacc - tz[n] * rs;
+        y = __fmul_rn(__fmul_rn((float)corrected, ts[n]), sc);
     }
     if (a.out == TL_OUT_F32)
         reinterpret_cast<float *>(a.Y[gi])[(long long)n * M + m] = y;
@@ -328,10 +328,12 @@ __device__ __forceinline__ void store_out(const GroupArgs &a, int gi, int m, int
 }
 
 // The 16 x N results of row tile r held as v[n * 16 + row], with the row
-// tile's scales and row sums in sc[16], rs[16].  One warp; lane (g, t)
-// stores rows g, g+8 of tokens 2t, 2t+1.
+// tile's scales and row sums in sc[16], rs[16] and (integer modes) the
+// tokens' steps and zero points in ts, tz.  One warp; lane (g, t) stores
+// rows g, g+8 of tokens 2t, 2t+1.
 __device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const float *v,
-                                               const float *sc, const int *rs, int lane) {
+                                               const float *sc, const int *rs, const float *ts,
+                                               const int32_t *tz, int lane) {
     const int g = lane >> 2, t = lane & 3;
     int gi = 0;
     while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
@@ -341,7 +343,7 @@ __device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const 
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int i = g + 8 * h, m = rl * 16 + i, n = 2 * t + e;
-            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, v[n * 16 + i], sc[i], rs[i]);
+            if (m < a.M[gi] && n < a.N) store_out(a, gi, m, n, v[n * 16 + i], sc[i], rs[i], ts, tz);
         }
 }
 
@@ -352,7 +354,8 @@ __device__ __forceinline__ void store_row_tile(const GroupArgs &a, int r, const 
 // empty and is done.  One atomic round trip, and the sum does not depend on
 // which CTA comes second (a + b == b + a in floating point).
 __device__ __forceinline__ void exchange_row_tile(const GroupArgs &a, int r, const float *v,
-                                                  const float *sc, const int *rs, int lane) {
+                                                  const float *sc, const int *rs, const float *ts,
+                                                  const int32_t *tz, int lane) {
     const int g = lane >> 2, t = lane & 3;
     int gi = 0;
     while (gi + 1 < a.G && a.rt_off[gi + 1] <= r) ++gi;
@@ -379,7 +382,7 @@ __device__ __forceinline__ void exchange_row_tile(const GroupArgs &a, int r, con
                 if (m < a.M[gi])
                     store_out(a, gi, m, n,
                               __fadd_rn(__uint_as_float((uint32_t)old[h][e]), v[n * 16 + i]),
-                              sc[i], rs[i]);
+                              sc[i], rs[i], ts, tz);
             }
         }
 }
@@ -521,13 +524,36 @@ __device__ __forceinline__ void store_rotated(uint32_t *dst, const uint32_t (&w)
 // so every product is w-field * x * 2^(kT - 133)), and returns the group's
 // sum in a fixed order and (mode A) the mask of halves outside the fixed
 // window.  A zero x writes zeros.
-template <bool kModeA, int NT>
+// kQ: the group is 8 bf16 activations that are first quantised with the
+// token's step s (r = 1/s) and zero point z, exactly as the quantiser
+// kernel does; the codes are then staged and summed like mode B's.
+template <bool kModeA, int NT, bool kQ = false>
 __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const uint4 &x,
-                                            float &sum, uint32_t &bad) {
+                                            float &sum, uint32_t &bad, const float *qs = nullptr,
+                                            const float *qr = nullptr, const int *qz = nullptr,
+                                            int sym = 0) {
     const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
     sum = 0.f;
     bad = 0u;
-    if (kModeA) {
+    if (kQ) {
+        const int m = o >> 1, qd = m >> 1;
+        const float f = __int_as_float((kT - 2 * (m & 3) + 127) << 23);
+        const float sv = qs[n], rv = qr[n], zf = (float)qz[n], qlo = sym ? -127.f : -128.f;
+        uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1) + (o & 1);
+        uint32_t st[4];
+        int isum = 0;
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+            const float x0 = __uint_as_float(wd[tt] << 16), x1 = __uint_as_float(wd[tt] & 0xFFFF0000u);
+            const float q0 = fminf(fmaxf(__fadd_rn(tl_internal::quant_round(x0, sv, rv), zf), qlo), 127.f);
+            const float q1 = fminf(fmaxf(__fadd_rn(tl_internal::quant_round(x1, sv, rv), zf), qlo), 127.f);
+            isum += (int)q0 + (int)q1;
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(q0, f), __fmul_rn(q1, f));
+            st[tt] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+        store_rotated(dst, st, qd);
+        sum = (float)isum;
+    } else if (kModeA) {
         const int m = o >> 1, qd = m >> 1;
         const uint32_t ex = (uint32_t)(kT - 2 * (m & 3)) * 0x00800080u;
         uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1) + (o & 1);
@@ -819,15 +845,19 @@ struct StepSmem {
     int redo;                          // tokens outside the fixed window (bit mask)
     int go;                            // the step's inputs are ready
     unsigned long long epoch;          // chain passes completed before this one
+    float qs[NT], qr[NT];              // fused quantisation: each token's step and 1/step
+    int qz[NT];                        // and zero point
 };
 
 // ------------------------------------------------------------ one linear step
-// kModeA: bf16 activations (else int8 from the quantiser).  NT: token
-// columns staged (a power of two >= N).  kChain: the step is one of a chain
+// kModeA: bf16 activations (else int8 from the quantiser).  kQ (with
+// !kModeA): bf16 activations quantised per token by the step itself, as the
+// quantiser kernel would, then mode B's arithmetic.  NT: token columns
+// staged (a power of two >= N).  kChain: the step is one of a chain
 // run by one persistent launch; it waits for the prevP CTAs of step - 1
 // (the chain's counters) instead of for the previous kernel.  Returns, the
 // same in every thread of the CTA, whether every wait succeeded.
-template <bool kModeA, int NT, bool kChain>
+template <bool kModeA, int NT, bool kChain, bool kQ = false>
 __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *smem,
                                          StepSmem<NT> &sh, Pipe &pipe, const ChainHeader *ch,
                                          int step, unsigned prevP) {
@@ -836,11 +866,12 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
     constexpr int XQ = NT * 4;                  // uint4 per 32-column quarter
     constexpr int XB = 4 * XQ;                  // uint4 per 128-column block
     constexpr int RV = 16 * NT;                 // floats per row-tile result
-    constexpr int VPL = kModeA ? 8 : 16;        // activations per staging group
+    constexpr bool kBf = kModeA || kQ;          // X is bf16
+    constexpr int VPL = kBf ? 8 : 16;           // activations per staging group
     constexpr int LB = 128 / VPL;               // staging groups per block
     constexpr int HB = LB / 2;                  // staging groups per half block
     constexpr int XHB = 2 * NT;                 // correction floats per block
-    constexpr int SB = stage_batch(NT, kModeA); // staging loads in flight per thread
+    constexpr int SB = stage_batch(NT, kBf);    // staging loads in flight per thread
     constexpr bool kAsyncX = NT >= 4;           // stage X with cp.async (when X allows 16-byte copies)
     // dynamic shared memory, at offsets fixed for every step of a launch
     uint8_t *ring = smem;                                                // [kWarps][kSlots][SLOT]
@@ -895,7 +926,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
     // written them.  One 128-byte line per thread per step, addresses inside
     // each row's columns [k_lo, k_hi).
     if (sig1 > sig0) {
-        constexpr int EB = kModeA ? 2 : 1;
+        constexpr int EB = kBf ? 2 : 1;
         const long long k_lo = (long long)sig0 * a.KW * 128;
         const long long k_hi = min((long long)a.K, (long long)sig1 * a.KW * 128);
         const int lines = (int)((k_hi - k_lo) * EB + 127) / 128;
@@ -915,8 +946,111 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
         __syncthreads();
         if (!sh.go) return false;
     }
+    // the token scales the epilogue of an integer mode uses
+    const float *ts = kQ ? sh.qs : a.s;
+    const int32_t *tz = kQ ? sh.qz : a.z;
+    if (kQ) {
+        // Fused quantisation: every CTA reduces each token's whole row to its
+        // minimum and maximum (widened to include 0; exact in any order, so
+        // every CTA derives the same step and zero point) and forms them as
+        // the quantiser kernel does; padding past K is staged as the
+        // quantised zero, whose products with the padded weights cancel in
+        // the chains' integer sums.
+        // R rows' worth of loads per token in flight per thread (eight in all)
+        constexpr int R = NT >= 8 ? 1 : 8 / NT;
+        float lo[NT], hi[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) lo[n] = hi[n] = 0.f;
+        const uint16_t *x0 = reinterpret_cast<const uint16_t *>(a.X);
+        if (a.xvec) {
+            const int nv = a.K / 8;
+            for (int i0 = threadIdx.x; i0 < nv; i0 += kThreads * R) {
+                uint4 u[R][NT];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const int i = i0 + r * kThreads;
+                        u[r][n] = (n < N && i < nv)
+                                      ? ldx<kChain>(reinterpret_cast<const uint4 *>(x0 + (long long)n * a.K) + i)
+                                      : make_uint4(0u, 0u, 0u, 0u);   // zero: inside every range
+                    }
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const uint32_t w4[4] = {u[r][n].x, u[r][n].y, u[r][n].z, u[r][n].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float e0 = __uint_as_float(w4[j] << 16),
+                                        e1 = __uint_as_float(w4[j] & 0xFFFF0000u);
+                            lo[n] = fminf(lo[n], fminf(e0, e1));
+                            hi[n] = fmaxf(hi[n], fmaxf(e0, e1));
+                        }
+                    }
+            }
+        } else {
+            for (int k0 = threadIdx.x; k0 < a.K; k0 += kThreads * R) {
+                uint32_t u[R][NT];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const int k = k0 + r * kThreads;
+                        u[r][n] = (n < N && k < a.K) ? (uint32_t)ldx16<kChain>(x0 + (long long)n * a.K + k) : 0u;
+                    }
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const float e = __uint_as_float(u[r][n] << 16);
+                        lo[n] = fminf(lo[n], e);
+                        hi[n] = fmaxf(hi[n], e);
+                    }
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                lo[n] = fminf(lo[n], __shfl_xor_sync(0xffffffffu, lo[n], off));
+                hi[n] = fmaxf(hi[n], __shfl_xor_sync(0xffffffffu, hi[n], off));
+            }
+            if (lane == 0) {
+                bslot[warp][0][n] = lo[n];       // the boundary slots are free until the main loop
+                bslot[warp][1][n] = hi[n];
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < NT) {
+            // columns past the batch: step 1, zero point 0, so they stage zeros
+            const int n = threadIdx.x;
+            float l = 0.f, h = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                l = fminf(l, bslot[w][0][n]);
+                h = fmaxf(h, bslot[w][1][n]);
+            }
+            float sv;
+            int zv;
+            if (a.sym) {
+                const float m = fmaxf(-l, h);   // max |x|, the row's range including 0
+                sv = m == 0.f ? 1.f : __fdiv_rn(m, 127.f);
+                zv = 0;
+            } else if (h == l) {
+                sv = 1.f;
+                zv = 0;
+            } else {
+                sv = __fdiv_rn(__fsub_rn(h, l), 255.f);
+                zv = -128 - (int)rintf(__fdiv_rn(l, sv));
+            }
+            sh.qs[n] = sv;
+            sh.qr[n] = __frcp_rn(sv);
+            sh.qz[n] = zv;
+        }
+        __syncthreads();
+    }
     uint4 xv[SB];
-    if (!(kAsyncX && a.xvec)) stage_load<kModeA, SB, kChain>(a, P, 0, xv);
+    if (!(kAsyncX && a.xvec)) stage_load<kBf, SB, kChain>(a, P, 0, xv);
 
     Cursor cc;
     cc.sigma = sig0;
@@ -945,7 +1079,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                 // copied at once (cp.async, zero past K) into their block's own
                 // region, row n at byte n * RB; then each warp rewrites its
                 // blocks in place, group by group as below.
-                constexpr int EB = kModeA ? 2 : 1;
+                constexpr int EB = kBf ? 2 : 1;
                 constexpr int RB = 128 * EB;               // bytes of one token's block row
                 constexpr int CPR = RB / 16;                // 16-byte copies per block row
                 const int nch = N * P.kw * CPR;
@@ -979,7 +1113,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                         const int g = lane + 32 * j, n = g / LB, o = g % LB;
                         float sum;
                         uint32_t bad;
-                        stage_group<kModeA, NT>(blk, n, o, v[j], sum, bad);
+                        stage_group<kModeA, NT, kQ>(blk, n, o, v[j], sum, bad, sh.qs, sh.qr, sh.qz, a.sym);
 #pragma unroll
                         for (int off = HB / 2; off > 0; off >>= 1)
                             sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
@@ -989,7 +1123,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                 }
             } else
             for (int base = 0; base < total; base += kThreads * SB) {
-                if (sigma != sig0 || base != 0) stage_load<kModeA, SB, kChain>(a, P, base, xv);
+                if (sigma != sig0 || base != 0) stage_load<kBf, SB, kChain>(a, P, base, xv);
 #pragma unroll
                 for (int i = 0; i < SB; ++i) {
                     if (base + i * kThreads >= total) break;   // uniform over the block
@@ -999,7 +1133,9 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                     const int n = valid ? fdiv(q, dv) : 0, jb = q - n * P.kw;
                     float sum = 0.f;
                     uint32_t bad = 0u;
-                    if (valid) stage_group<kModeA, NT>(xw + jb * NT * 64, n, o, xv[i], sum, bad);
+                    if (valid)
+                        stage_group<kModeA, NT, kQ>(xw + jb * NT * 64, n, o, xv[i], sum, bad, sh.qs, sh.qr,
+                                                    sh.qz, a.sym);
 #pragma unroll
                     for (int off = HB / 2; off > 0; off >>= 1)
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, off));
@@ -1214,9 +1350,9 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                 row_span(P, r, lo, hi);
                 float *v = acc + rho * RV;
                 if (a.NS == 1 && lo == 0 && hi == P.kw) {
-                    store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
+                    store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, ts, tz, lane);
                 } else if (a.NS == 1) {
-                    exchange_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
+                    exchange_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, ts, tz, lane);
                 } else {
                     const int half = lo == 0 ? 0 : 1;   // 0: holds the slice's first block
                     float *dst = a.part + (((long long)r * a.NS + sigma) * 2 + half) * N * 16;
@@ -1267,7 +1403,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                         for (int j = 0; j < kE; ++j)
                             if (lane + 32 * j < N * 16) v[lane + 32 * j] = y[j];
                         __syncwarp();
-                        store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, lane);
+                        store_row_tile(a, r, v, scl + rho * 16, rsm + rho * 16, ts, tz, lane);
                         if (lane == 0) a.cnt[r] = 0ull;
                     }
                 }
@@ -1283,8 +1419,8 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
 
 
 // ------------------------------------------------------------ kernels
-// One (grouped) linear per launch.
-template <bool kModeA, int NT>
+// One (grouped) linear per launch; kQ quantises bf16 X per token itself.
+template <bool kModeA, int NT, bool kQ = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 tl_mma_kernel(const __grid_constant__ GroupArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1310,7 +1446,7 @@ tl_mma_kernel(const __grid_constant__ GroupArgs a) {
         pipe_start<NT>(pipe, blockIdx.x, warp);
         prefetch_rest<NT>(pipe, a, warp);
     }
-    const bool ok = run_step<kModeA, NT, false>(a, blockIdx.x, smem, sh, pipe, nullptr, 0, 0u);
+    const bool ok = run_step<kModeA, NT, false, kQ>(a, blockIdx.x, smem, sh, pipe, nullptr, 0, 0u);
     if (!ok && lane == 0) pipe_drain(pipe, a.status);
 }
 
@@ -1318,6 +1454,12 @@ using KernelFn = void (*)(GroupArgs);
 
 KernelFn kernel_for(int mode, int nt) {
     const bool A = mode == TL_MODE_BF16;
+    if (mode == TL_MODE_I8_FUSED) switch (nt) {
+            case 1: return tl_mma_kernel<false, 1, true>;
+            case 2: return tl_mma_kernel<false, 2, true>;
+            case 4: return tl_mma_kernel<false, 4, true>;
+            default: return tl_mma_kernel<false, 8, true>;
+        }
     switch (nt) {
         case 1: return A ? tl_mma_kernel<true, 1> : tl_mma_kernel<false, 1>;
         case 2: return A ? tl_mma_kernel<true, 2> : tl_mma_kernel<false, 2>;
@@ -1562,14 +1704,14 @@ tl_status init_device(int dev, DeviceInfo &d) {
         d.init.store(-1, std::memory_order_release);
         return TL_OK;
     }
-    for (int mode = 0; mode < 2; ++mode)
+    for (int mode = 0; mode < 3; ++mode)
         for (int nt = 1; nt <= 8; nt *= 2)
             if (cudaFuncSetAttribute(kernel_for(mode, nt),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess ||
-                cudaFuncSetAttribute(chain_kernel_for(mode, nt),
+                (mode < 2 && cudaFuncSetAttribute(chain_kernel_for(mode, nt),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess)
+                                     (int)dyn_smem(nt, kMaxSlice, kMaxCtaRows)) != cudaSuccess))
                 return TL_ERR_CUDA;
     tl_status pst = tl_internal::prefill_init_device();
     if (pst != TL_OK) return pst;
@@ -1676,12 +1818,12 @@ tl_status check_weights(const tl_weight *Ws, int G, int mode) {
     for (int g = 0; g < G; ++g) {
         const tl_weight &w = Ws[g];
         if (!w.packed || !w.scale) return TL_ERR_NULL;
-        if (mode == TL_MODE_I8 && !w.rowsum) return TL_ERR_NULL;
+        if (mode != TL_MODE_BF16 && !w.rowsum) return TL_ERR_NULL;
         if (w.layout != TL_LAYOUT_TL2P_V2) return TL_ERR_UNSUPPORTED;
         if (w.M < 1 || w.K < 1 || w.M > TL_MAX_M || w.K > TL_MAX_K) return TL_ERR_SHAPE;
         if (w.K != Ws[0].K) return TL_ERR_SHAPE;
         if (!aligned(w.packed, 16) || !aligned(w.scale, 4)) return TL_ERR_ALIGN;
-        if (mode == TL_MODE_I8 && !aligned(w.rowsum, 4)) return TL_ERR_ALIGN;
+        if (mode != TL_MODE_BF16 && !aligned(w.rowsum, 4)) return TL_ERR_ALIGN;
     }
     return TL_OK;
 }
@@ -1690,11 +1832,12 @@ size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
     int Ms[TL_MAX_GROUP];
     for (int g = 0; g < G; ++g) Ms[g] = Ws[g].M;
     const int K = Ws[0].K;
-    if (tl_internal::prefill_supported(N, K))
-        return std::max(tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_BF16, sms),
-                        tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_I8, sms));
     Plan p;
     if (make_plan(Ms, G, K, N, sms, &p) != TL_OK) return 0;
+    if (tl_internal::prefill_supported(N, K))   // the fused mode runs these N in chunks of 8
+        return std::max({tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_BF16, sms),
+                         tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_I8, sms),
+                         p.ws_bytes});
     return p.ws_bytes;
 }
 
@@ -1722,12 +1865,12 @@ void fill_linear(GroupArgs &a, const tl_weight *Ws, int G, const void *X, const 
     a.kwr = p.KW; a.rowsr = p.rows;
     a.dKW = make_fastdiv((uint32_t)p.KW);
     a.dKWL = make_fastdiv((uint32_t)p.KWL);
-    const size_t xsz = mode == TL_MODE_BF16 ? 2 : 1;
+    const size_t xsz = mode == TL_MODE_I8 ? 1 : 2;
     a.X = static_cast<const char *>(X) + (size_t)n0 * K * xsz;
     a.s = s ? s + n0 : nullptr;
     a.z = z ? z + n0 : nullptr;
     a.N = n; a.mode = mode; a.out = out;
-    a.xvec = aligned(a.X, 16) && (K % (mode == TL_MODE_BF16 ? 8 : 16)) == 0;
+    a.xvec = aligned(a.X, 16) && (K % (mode == TL_MODE_I8 ? 16 : 8)) == 0;
     a.cnt = static_cast<unsigned long long *>(cnt);
     a.xslot = static_cast<unsigned long long *>(xslot);
     a.part = static_cast<float *>(part);
@@ -1749,6 +1892,7 @@ tl_status launch_chunk(const tl_weight *Ws, int G, const void *X, const float *s
     fill_linear(a, Ws, G, X, s, z, Ys, n0, n, mode, out, p, static_cast<int *>(ws), wsb,
                 wsb + p.cnt_bytes,
                 static_cast<char *>(ws) + tl_internal::scratch_offset(ws_bytes, p.back));
+    a.sym = mode == TL_MODE_I8_FUSED && (flags & TL_FLAG_SYMMETRIC) ? 1 : 0;
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -1955,16 +2099,16 @@ tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float
                           const int32_t *z, void *const *Ys, int N, int mode, int out_dtype,
                           void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream) {
+    if (mode != TL_MODE_BF16 && mode != TL_MODE_I8 && mode != TL_MODE_I8_FUSED) return TL_ERR_MODE;
     tl_status st = check_weights(Ws, G, mode);
     if (st != TL_OK) return st;
-    if (mode != TL_MODE_BF16 && mode != TL_MODE_I8) return TL_ERR_MODE;
     if (out_dtype != TL_OUT_F32 && out_dtype != TL_OUT_BF16 && out_dtype != TL_OUT_I32_RAW)
         return TL_ERR_MODE;
     if (out_dtype == TL_OUT_I32_RAW && mode != TL_MODE_I8) return TL_ERR_MODE;
     if (!X || !Ys) return TL_ERR_NULL;
     if (N < 1) return TL_ERR_SHAPE;
     if (mode == TL_MODE_I8 && (!s || !z)) return TL_ERR_NULL;
-    if (mode == TL_MODE_BF16 && !aligned(X, 2)) return TL_ERR_ALIGN;
+    if (mode != TL_MODE_I8 && !aligned(X, 2)) return TL_ERR_ALIGN;
     if (mode == TL_MODE_I8 && (!aligned(s, 4) || !aligned(z, 4))) return TL_ERR_ALIGN;
     for (int g = 0; g < G; ++g) {
         if (!Ys[g]) return TL_ERR_NULL;
@@ -1976,7 +2120,7 @@ tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float
     st = device_info(&dev);
     if (st != TL_OK) return st;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (tl_internal::prefill_supported(N, Ws[0].K)) {
+    if (mode != TL_MODE_I8_FUSED && tl_internal::prefill_supported(N, Ws[0].K)) {
         if (mode == TL_MODE_BF16 && !aligned(X, 16)) return TL_ERR_ALIGN;
         return tl_internal::launch_prefill(Ws, G, X, s, z, Ys, N, mode, out_dtype, workspace,
                                            workspace_bytes, flags, cs);

@@ -10,7 +10,8 @@ streaming its weights while the previous one drains.  ``capture()`` records
 one pass as a CUDA graph.
 
 Mode B adds one activation-quantisation launch in front of every linear
-launch (four per layer).
+launch (four per layer); the fused mode B (``TL_MODE_I8_FUSED``) quantises
+inside the linear's own launch instead.
 """
 from __future__ import annotations
 
@@ -121,6 +122,10 @@ class LinearStack:
 
     # ------------------------------------------------------------------ run
     @property
+    def integer(self) -> bool:
+        return self.mode in (tl.TL_MODE_I8, tl.TL_MODE_I8_FUSED)
+
+    @property
     def launches_per_step(self) -> int:
         per_layer = len(GROUPS) * (2 if self.mode == tl.TL_MODE_I8 else 1)
         return per_layer * self.layers
@@ -137,6 +142,8 @@ class LinearStack:
                                        out_dtype=self.out_dtype, workspace=self.workspace,
                                        flags=flags, stream=stream)
                 else:
+                    if self.mode == tl.TL_MODE_I8_FUSED and self.symmetric:
+                        flags |= tl.TL_FLAG_SYMMETRIC
                     tl.tl_linear_group(ws, x, outs=self.Y[l][gi], mode=self.mode,
                                        out_dtype=self.out_dtype, workspace=self.workspace,
                                        flags=flags, stream=stream)
@@ -145,6 +152,8 @@ class LinearStack:
         """The whole pass as one chain: every launch group of every layer, in
         dependency order, run by one persistent launch (mode B quantises each
         group's bf16 input inside the chain)."""
+        if self.mode not in (tl.TL_MODE_BF16, tl.TL_MODE_I8):
+            raise ValueError("a chain runs mode A or mode B (its quantiser steps are its own)")
         if getattr(self, "_chain", None) is None:
             steps = [([self.weights[l][p] for p in grp], self.X[l][gi], self.Y[l][gi])
                      for l in range(self.layers) for gi, grp in enumerate(GROUPS)]
@@ -182,7 +191,7 @@ class LinearStack:
             for p in grp:
                 M = shp[p][0]
                 per_layer += tl.tl_packed_bytes(M, K) + 4 * M + self.N * M * yb
-                if self.mode == tl.TL_MODE_I8:
+                if self.integer:
                     per_layer += 4 * M
         if self.mode == tl.TL_MODE_I8:
             per_layer += len(GROUPS) * self.N * 8      # s and z

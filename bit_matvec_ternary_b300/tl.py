@@ -26,9 +26,9 @@ _lib = C.CDLL(LIB_PATH)
 TL_OK = 0
 TL_ERR_NULL, TL_ERR_SHAPE, TL_ERR_ALIGN, TL_ERR_BAD_VALUE = 1, 2, 3, 4
 TL_ERR_MODE, TL_ERR_UNSUPPORTED, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_WORKSPACE = 5, 6, 7, 8, 9
-TL_MODE_BF16, TL_MODE_I8 = 0, 1
+TL_MODE_BF16, TL_MODE_I8, TL_MODE_I8_FUSED = 0, 1, 2
 TL_OUT_F32, TL_OUT_BF16, TL_OUT_I32_RAW = 0, 1, 2
-TL_FLAG_PDL = 1
+TL_FLAG_PDL, TL_FLAG_SYMMETRIC = 1, 2
 TL_LAYOUT_TL2P_V2 = 2
 TL_MAX_GROUP = 4
 

@@ -16,6 +16,11 @@
  *   TL_MODE_I8   (mode B): x was quantised per token by tl_quantize_act into
  *       int8 q with step s[n] and zero point z[n]; acc = sum_k w*q is exact
  *       (int32) and y = ((float)(acc - z[n]*rowsum[m]) * s[n]) * scale[m].
+ *   TL_MODE_I8_FUSED: mode B with the quantisation done inside the linear's
+ *       own launch: x is bf16, and every token is quantised exactly as
+ *       tl_quantize_act would (asymmetric, or symmetric with
+ *       TL_FLAG_SYMMETRIC), so Y is bit for bit what tl_quantize_act
+ *       followed by TL_MODE_I8 gives, with one launch instead of two.
  *
  * Batch sizes: 1 <= N <= 8 is the decode / speculative-verify path (one
  * token plus up to seven drafted ones verified "in one batched pass", wiki
@@ -78,7 +83,7 @@ typedef enum {
     TL_ERR_WORKSPACE = 9    /* workspace NULL or smaller than tl_workspace_bytes() */
 } tl_status;
 
-enum { TL_MODE_BF16 = 0, TL_MODE_I8 = 1 };
+enum { TL_MODE_BF16 = 0, TL_MODE_I8 = 1, TL_MODE_I8_FUSED = 2 };
 enum { TL_OUT_F32 = 0, TL_OUT_BF16 = 1, TL_OUT_I32_RAW = 2 };
 
 /* tl_linear flags */
@@ -87,6 +92,9 @@ enum { TL_OUT_F32 = 0, TL_OUT_BF16 = 1, TL_OUT_I32_RAW = 2 };
                            previous kernel on the stream has finished.  Only set
                            it when that previous kernel does not write this call's
                            weights, scales or row sums (it may write X). */
+#define TL_FLAG_SYMMETRIC 2u /* TL_MODE_I8_FUSED: quantise symmetrically (as
+                                tl_quantize_act with symmetric != 0); ignored in
+                                the other modes */
 
 #define TL_LAYOUT_TL2P_V2 2u
 #define TL_MAX_GROUP 4
@@ -167,11 +175,17 @@ TL_API tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, fl
  *   mode TL_MODE_BF16: X is bf16 [N][K]; s, z ignored (may be NULL).
  *   mode TL_MODE_I8:   X is int8 [N][K] from tl_quantize_act; s, z [N] required;
  *                      W->rowsum required.
+ *   mode TL_MODE_I8_FUSED: X is bf16 [N][K]; s, z ignored (may be NULL);
+ *                      W->rowsum required.  Every N runs on the decode
+ *                      kernel (in chunks of 8 tokens, each CTA reducing
+ *                      each token's whole row for its step and zero point):
+ *                      meant for decode and verify batches; prefill-sized N
+ *                      is faster as tl_quantize_act + TL_MODE_I8.
  *   out_dtype: TL_OUT_F32 (fp32 Y), TL_OUT_BF16 (bf16 Y, round to nearest
- *              even of the fp32 result), TL_OUT_I32_RAW (mode B only: the
- *              exact int32 acc = sum_k w*q, before any correction).
+ *              even of the fp32 result), TL_OUT_I32_RAW (mode TL_MODE_I8
+ *              only: the exact int32 acc = sum_k w*q, before any correction).
  *   workspace: device, >= tl_workspace_bytes(W, 1, N) bytes, 256-byte aligned.
- *   flags: 0 or TL_FLAG_PDL.
+ *   flags: 0, or TL_FLAG_PDL and / or TL_FLAG_SYMMETRIC.
  * Y must not alias X.  Deterministic: the same call gives the same bits. */
 TL_API tl_status tl_linear(const tl_weight *W, const void *X, const float *s, const int32_t *z,
                     void *Y, int N, int mode, int out_dtype, void *workspace,

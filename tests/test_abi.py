@@ -120,6 +120,15 @@ def test_linear_argument_errors():
     assert _linear(_w(), ws=0x8010) == tl.TL_ERR_ALIGN
 
 
+def test_fused_quant_mode_argument_errors():
+    F = tl.TL_MODE_I8_FUSED
+    assert _linear(_w(rowsum=0), mode=F) == tl.TL_ERR_NULL       # needs the row sums
+    assert _linear(_w(rowsum=0x3002), mode=F) == tl.TL_ERR_ALIGN
+    assert _linear(_w(), mode=F, out=tl.TL_OUT_I32_RAW) == tl.TL_ERR_MODE
+    assert _linear(_w(), mode=F, X=0x4001) == tl.TL_ERR_ALIGN     # bf16 X
+    assert _linear(_w(), mode=3) == tl.TL_ERR_MODE
+
+
 def test_group_argument_errors():
     f = tl.raw_call("tl_linear_group")
     ys = (C.c_void_p * 5)(0x7000, 0x7100, 0x7200, 0x7300, 0x7400)
@@ -165,6 +174,7 @@ def test_chain_arguments_checked_without_a_gpu():
     assert enc(*args(9, tl.TL_MODE_BF16, tl.TL_OUT_F32)) == tl.TL_ERR_SHAPE
     assert enc(*args(0, tl.TL_MODE_BF16, tl.TL_OUT_F32)) == tl.TL_ERR_SHAPE
     assert enc(*args(1, 7, tl.TL_OUT_F32)) == tl.TL_ERR_MODE
+    assert enc(*args(1, tl.TL_MODE_I8_FUSED, tl.TL_OUT_F32)) == tl.TL_ERR_MODE  # chains: A, B
     assert enc(*args(1, tl.TL_MODE_BF16, tl.TL_OUT_I32_RAW)) == tl.TL_ERR_MODE
     assert enc(None, 1, 1, 0, 0, None, 0, 0x100000, 1 << 20,
                img.ctypes.data_as(C.c_void_p), img.size) == tl.TL_ERR_NULL
