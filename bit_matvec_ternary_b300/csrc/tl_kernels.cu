@@ -65,10 +65,10 @@
 
 namespace {
 
-constexpr int kWarps = 8;             // warps per CTA of the N <= 8 kernel
-constexpr int kCtasPerSm = 2;         // resident CTAs per SM (registers and shared memory allow 2)
+constexpr int kWarps = 16;            // warps per CTA of the N <= 8 kernel
+constexpr int kCtasPerSm = 1;         // resident CTAs per SM (registers allow 1)
 // CTAs per SM in a launch's grid.
-constexpr int kGridPerSm = 2;
+constexpr int kGridPerSm = 1;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 2;             // bulk copies in flight per warp
 // Tiles (512 B each) per bulk copy: 8, or 4 at eight tokens, where the
@@ -79,7 +79,7 @@ __host__ __device__ constexpr int ring_bytes(int nt) { return kWarps * kSlots * 
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSlice = 32;         // 128-column blocks per K slice (64 KB of X at 8 tokens)
-constexpr int kMaxCtaRows = 16;       // row tiles one CTA may touch in one slice
+constexpr int kMaxCtaRows = 32;       // row tiles one CTA may touch in one slice (kThreads / 16)
 // 16-byte activation loads in flight per thread while staging a slice: all
 // of a slice at once, up to 8 (4 at eight tokens, where more registers spill).
 __host__ __device__ constexpr int stage_batch(int nt, bool mode_a) {
@@ -949,6 +949,8 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
     // the token scales the epilogue of an integer mode uses
     const float *ts = kQ ? sh.qs : a.s;
     const int32_t *tz = kQ ? sh.qz : a.z;
+    uint4 xv[SB];
+    bool xv_loaded = false;
     if (kQ) {
         // Fused quantisation: every CTA reduces each token's whole row to its
         // minimum and maximum (widened to include 0; exact in any order, so
@@ -962,7 +964,33 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
 #pragma unroll
         for (int n = 0; n < NT; ++n) lo[n] = hi[n] = 0.f;
         const uint16_t *x0 = reinterpret_cast<const uint16_t *>(a.X);
-        if (a.xvec) {
+        if (a.NS == 1 && !(kAsyncX && a.xvec) && N * P.kw * LB <= kThreads * SB) {
+            // One slice, staged from registers in one batch: that batch is
+            // every token's whole row, so it gives the minimum and maximum.
+            stage_load<kBf, SB, kChain>(a, P, 0, xv);
+            xv_loaded = true;
+            const int total = N * P.kw * LB;
+#pragma unroll
+            for (int i = 0; i < SB; ++i) {
+                const int idx = i * kThreads + (int)threadIdx.x;
+                if (idx >= total) break;
+                const int n = fdiv(idx / LB, a.dKWL);
+                const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+                float l = 0.f, h = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float e0 = __uint_as_float(w4[j] << 16), e1 = __uint_as_float(w4[j] & 0xFFFF0000u);
+                    l = fminf(l, fminf(e0, e1));
+                    h = fmaxf(h, fmaxf(e0, e1));
+                }
+#pragma unroll
+                for (int nn = 0; nn < NT; ++nn)
+                    if (nn == n) {
+                        lo[nn] = fminf(lo[nn], l);
+                        hi[nn] = fmaxf(hi[nn], h);
+                    }
+            }
+        } else if (a.xvec) {
             const int nv = a.K / 8;
             for (int i0 = threadIdx.x; i0 < nv; i0 += kThreads * R) {
                 uint4 u[R][NT];
@@ -1049,8 +1077,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
         }
         __syncthreads();
     }
-    uint4 xv[SB];
-    if (!(kAsyncX && a.xvec)) stage_load<kBf, SB, kChain>(a, P, 0, xv);
+    if (!(kAsyncX && a.xvec) && !xv_loaded) stage_load<kBf, SB, kChain>(a, P, 0, xv);
 
     Cursor cc;
     cc.sigma = sig0;
@@ -1482,9 +1509,9 @@ inline int padded_tokens(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 
 constexpr int kQThreads = 256;
 constexpr int kQChunk = 4096;          // activations quantised per CTA
 
-// Token n, chunk c (kQThreads threads).  kLaunch: a launch of its own, which
+// Token n, chunk c (kQT threads).  kLaunch: a launch of its own, which
 // waits for the previous kernel on the stream and lets the next one start.
-template <bool kLaunch>
+template <bool kLaunch, int kQT = kQThreads>
 __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int K, int vec,
                                             int8_t *__restrict__ Q, float *__restrict__ s_out,
                                             int32_t *__restrict__ z_out, int symmetric, int n,
@@ -1497,7 +1524,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     float lo = 0.f, hi = 0.f;
     if (vec) {
         const uint4 *xv = reinterpret_cast<const uint4 *>(x);
-        for (int i = threadIdx.x; i < K / 8; i += kQThreads) {
+        for (int i = threadIdx.x; i < K / 8; i += kQT) {
             const uint4 u = __ldcg(xv + i);
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -1512,7 +1539,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
             }
         }
     } else {
-        for (int k = threadIdx.x; k < K; k += kQThreads) {
+        for (int k = threadIdx.x; k < K; k += kQT) {
             const float v = __uint_as_float((uint32_t)__ldcg(x + k) << 16);
             if (symmetric) {
                 hi = fmaxf(hi, fabsf(v));
@@ -1522,7 +1549,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
             }
         }
     }
-    __shared__ float slo[kQThreads / 32], shi[kQThreads / 32];
+    __shared__ float slo[kQT / 32], shi[kQT / 32];
     __shared__ float s_sh;
     __shared__ int z_sh;
     for (int o = 16; o > 0; o >>= 1) {
@@ -1533,7 +1560,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     if (ln == 0) { slo[wid] = lo; shi[wid] = hi; }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kQThreads / 32; ++w) {
+        for (int w = 1; w < kQT / 32; ++w) {
             lo = fminf(lo, slo[w]);
             hi = fmaxf(hi, shi[w]);
         }
@@ -1572,7 +1599,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     if (vec) {
         // 8 activations per step: one 16-byte load, one 8-byte store
         const uint4 *xv = reinterpret_cast<const uint4 *>(x);
-        for (int i = k0 / 8 + threadIdx.x; i < k1 / 8; i += kQThreads) {
+        for (int i = k0 / 8 + threadIdx.x; i < k1 / 8; i += kQT) {
             const uint4 u = __ldcg(xv + i);
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
             uint32_t o[2] = {0u, 0u};
@@ -1585,7 +1612,7 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
             reinterpret_cast<uint2 *>(q)[i] = make_uint2(o[0], o[1]);
         }
     } else {
-        for (int k = k0 + threadIdx.x; k < k1; k += kQThreads)
+        for (int k = k0 + threadIdx.x; k < k1; k += kQT)
             q[k] = (int8_t)one(__uint_as_float((uint32_t)__ldcg(x + k) << 16));
     }
 }
@@ -1650,7 +1677,7 @@ tl_chain_kernel(const ChainHeader *__restrict__ ch, const GroupArgs *__restrict_
             ok = sh.go != 0;
             if (ok) {
                 const int chunks = (sa.K + kQChunk - 1) / kQChunk;
-                quant_chunk<false>(reinterpret_cast<const uint16_t *>(sa.X), sa.K, sa.xvec, sa.qout,
+                quant_chunk<false, kThreads>(reinterpret_cast<const uint16_t *>(sa.X), sa.K, sa.xvec, sa.qout,
                                    sa.sout, sa.zout, sa.sym, cta / chunks, cta % chunks);
             }
         }
