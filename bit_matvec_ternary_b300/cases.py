@@ -6,7 +6,8 @@ Cases are the launch groups of one 8B-shaped decoder layer: qkv (q/k/v
 grouped, K = 4096), o, gate_up (gate/up grouped), down (K = 12288), quant
 (the activation quantiser, K = 12288), chain (the first `--layers`
 layers of the 8B stack as one persistent chain launch), stack (the same
-layers as the benchmark's CUDA graph of per-group launches), and head (the
+layers as the benchmark's CUDA graph of per-group launches; `--mode f`
+quantises inside each linear launch), and head (the
 151,936 x 4,096 int8 head with its fused argmax).  Each is built from the same seeded
 synthetic inputs as the benchmark and launched `reps` times back to back
 after `warmup` launches, then the process checks nothing and exits 0.
@@ -27,7 +28,8 @@ def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant", "chain", "stack", "head"])
     ap.add_argument("--n", type=int, default=1)
-    ap.add_argument("--mode", default="a", choices=["a", "b"])
+    ap.add_argument("--mode", default="a", choices=["a", "b", "f"],
+                    help="a: bf16, b: int8 from the quantiser, f: int8 quantised in the launch")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--layer", type=int, default=5)
@@ -41,7 +43,9 @@ def main() -> None:
 
     shape = synth.NEUTRINO_8B
     shp = shape.linear_shapes()
-    mode = tl.TL_MODE_BF16 if args.mode == "a" else tl.TL_MODE_I8
+    mode = {"a": tl.TL_MODE_BF16, "b": tl.TL_MODE_I8, "f": tl.TL_MODE_I8_FUSED}[args.mode]
+    if mode == tl.TL_MODE_I8_FUSED and args.case in ("chain", "quant", "head"):
+        raise SystemExit("mode f applies to the per-launch cases and the stack")
     if args.case == "stack":
         from .stack import LinearStack
         st = LinearStack(shape, N=args.n, mode=mode, layers=args.layers)
@@ -99,9 +103,9 @@ def main() -> None:
         for _ in range(args.warmup + args.reps):
             tl.tl_linear_group(ws, q, s, z, outs=outs, mode=mode, workspace=work)
     else:
-        outs = tl.tl_linear_group(ws, xt, workspace=work)
+        outs = tl.tl_linear_group(ws, xt, mode=mode, workspace=work)
         for _ in range(args.warmup + args.reps):
-            tl.tl_linear_group(ws, xt, outs=outs, workspace=work)
+            tl.tl_linear_group(ws, xt, outs=outs, mode=mode, workspace=work)
     torch.cuda.synchronize()
 
 
