@@ -555,20 +555,30 @@ __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const u
         sum = (float)isum;
     } else if (kModeA) {
         const int m = o >> 1, qd = m >> 1;
-        const uint32_t ex = (uint32_t)(kT - 2 * (m & 3)) * 0x00800080u;
+        // 2^(kT - 2q) in both halves: an exact bf16 product for values in the
+        // window (and zero stays zero)
+        const uint32_t e2 = (uint32_t)(kT - 2 * (m & 3) + 127) * 0x00800080u;
+        const __nv_bfloat162 sc2 = *reinterpret_cast<const __nv_bfloat162 *>(&e2);
         uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1) + (o & 1);
         uint32_t st[4];
+        // Per 16-bit half, with mag = |bits|: bit 15 of mag + kUp is set when
+        // the exponent field is above kWinHi, bit 15 of kLo - mag when mag is
+        // below the window, bit 15 of mag + 0x7FFF when mag is not zero (no
+        // carry or borrow crosses the halves).
+        constexpr uint32_t kUp = (0x8000u - ((uint32_t)(kWinHi + 1) << 7)) * 0x00010001u;
+        constexpr uint32_t kLo = (0x8000u + ((uint32_t)kWinLo << 7) - 1u) * 0x00010001u;
+        uint32_t flags = 0u;
 #pragma unroll
         for (int tt = 0; tt < 4; ++tt) {
             const uint32_t v = wd[tt];
             sum = __fadd_rn(__fadd_rn(sum, __uint_as_float(v << 16)),
                             __uint_as_float(v & 0xFFFF0000u));
-            // per half: nonzero, and exponent outside [kWinLo, kWinHi]
-            const uint32_t nz = __vcmpne2(v & 0x7FFF7FFFu, 0u);
-            const uint32_t off = __vsub2(v & 0x7F807F80u, (uint32_t)kWinLo * 0x00800080u);
-            bad |= __vcmpgtu2(off, (uint32_t)(kWinHi - kWinLo) * 0x00800080u) & nz;
-            st[tt] = v + (ex & nz);
+            const uint32_t mag = v & 0x7FFF7FFFu;
+            flags |= (mag + kUp) | ((kLo - mag) & (mag + 0x7FFF7FFFu));
+            const __nv_bfloat162 p2 = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v), sc2);
+            st[tt] = *reinterpret_cast<const uint32_t *>(&p2);
         }
+        bad = flags & 0x80008000u;
         // store word tt = (it + qd) % 4 at step it: the lanes of one block
         // quarter apart then write different banks
         store_rotated(dst, st, qd);
@@ -850,6 +860,38 @@ struct StepSmem {
 };
 
 // ------------------------------------------------------------ one linear step
+// Fused quantisation, threads n < NT: token n's step, its reciprocal and
+// its zero point from the per-warp minima and maxima in red[w][0 / 1][n]
+// (each range includes 0), formed as the quantiser kernel forms them.
+// Columns past the batch get step 1 and zero point 0, so they stage zeros.
+template <int NT, int W>
+__device__ __forceinline__ void quant_params(const float (&red)[W][2][16 * NT], int sym, float *qs,
+                                             float *qr, int *qz) {
+    if (threadIdx.x >= NT) return;
+    const int n = threadIdx.x;
+    float l = 0.f, h = 0.f;
+    for (int w = 0; w < W; ++w) {
+        l = fminf(l, red[w][0][n]);
+        h = fmaxf(h, red[w][1][n]);
+    }
+    float sv;
+    int zv;
+    if (sym) {
+        const float m = fmaxf(-l, h);   // max |x|, the row's range including 0
+        sv = m == 0.f ? 1.f : __fdiv_rn(m, 127.f);
+        zv = 0;
+    } else if (h == l) {
+        sv = 1.f;
+        zv = 0;
+    } else {
+        sv = __fdiv_rn(__fsub_rn(h, l), 255.f);
+        zv = -128 - (int)rintf(__fdiv_rn(l, sv));
+    }
+    qs[n] = sv;
+    qr[n] = __frcp_rn(sv);
+    qz[n] = zv;
+}
+
 // kModeA: bf16 activations (else int8 from the quantiser).  kQ (with
 // !kModeA): bf16 activations quantised per token by the step itself, as the
 // quantiser kernel would, then mode B's arithmetic.  NT: token columns
@@ -951,7 +993,10 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
     const int32_t *tz = kQ ? sh.qz : a.z;
     uint4 xv[SB];
     bool xv_loaded = false;
-    if (kQ) {
+    // fused quantisation with one slice copied whole by cp.async: the range
+    // comes from the copied slice (below) instead of a pass of its own
+    const bool q_late = kQ && kAsyncX && a.xvec && a.NS == 1;
+    if (kQ && !q_late) {
         // Fused quantisation: every CTA reduces each token's whole row to its
         // minimum and maximum (widened to include 0; exact in any order, so
         // every CTA derives the same step and zero point) and forms them as
@@ -1050,31 +1095,7 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
             }
         }
         __syncthreads();
-        if (threadIdx.x < NT) {
-            // columns past the batch: step 1, zero point 0, so they stage zeros
-            const int n = threadIdx.x;
-            float l = 0.f, h = 0.f;
-            for (int w = 0; w < kWarps; ++w) {
-                l = fminf(l, bslot[w][0][n]);
-                h = fmaxf(h, bslot[w][1][n]);
-            }
-            float sv;
-            int zv;
-            if (a.sym) {
-                const float m = fmaxf(-l, h);   // max |x|, the row's range including 0
-                sv = m == 0.f ? 1.f : __fdiv_rn(m, 127.f);
-                zv = 0;
-            } else if (h == l) {
-                sv = 1.f;
-                zv = 0;
-            } else {
-                sv = __fdiv_rn(__fsub_rn(h, l), 255.f);
-                zv = -128 - (int)rintf(__fdiv_rn(l, sv));
-            }
-            sh.qs[n] = sv;
-            sh.qr[n] = __frcp_rn(sv);
-            sh.qz[n] = zv;
-        }
+        quant_params<NT>(bslot, a.sym, sh.qs, sh.qr, sh.qz);
         __syncthreads();
     }
     if (!(kAsyncX && a.xvec) && !xv_loaded) stage_load<kBf, SB, kChain>(a, P, 0, xv);
@@ -1124,6 +1145,42 @@ __device__ __forceinline__ bool run_step(const GroupArgs &a, int cta, uint8_t *s
                 }
                 asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
                 __syncthreads();
+                if (q_late) {
+                    // Every token's whole row is in the slice: thread t reads
+                    // token (t / 16) % NT only (kThreads is a multiple of 16 NT),
+                    // each half warp reduces its token, and warp w leaves its two
+                    // tokens' ranges (zero elsewhere) in the boundary slots.
+                    static_assert(kThreads % (16 * NT) == 0, "one token per thread");
+                    const int n = (threadIdx.x >> 4) % NT;
+                    float l = 0.f, h = 0.f;
+                    if (n < N) {
+                        for (int u = threadIdx.x; u < P.kw * NT * 16; u += kThreads) {
+                            const uint4 v = xs[u];
+                            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float e0 = __uint_as_float(w4[j] << 16),
+                                            e1 = __uint_as_float(w4[j] & 0xFFFF0000u);
+                                l = fminf(l, fminf(e0, e1));
+                                h = fmaxf(h, fmaxf(e0, e1));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) {
+                        l = fminf(l, __shfl_xor_sync(0xffffffffu, l, off));
+                        h = fmaxf(h, __shfl_xor_sync(0xffffffffu, h, off));
+                    }
+                    if (lane < NT) bslot[warp][0][lane] = bslot[warp][1][lane] = 0.f;
+                    __syncwarp();
+                    if ((lane & 15) == 0) {
+                        bslot[warp][0][n] = l;
+                        bslot[warp][1][n] = h;
+                    }
+                    __syncthreads();
+                    quant_params<NT>(bslot, a.sym, sh.qs, sh.qr, sh.qz);
+                    __syncthreads();
+                }
                 constexpr int J = NT * LB / 32 > 0 ? NT * LB / 32 : 1;   // groups per lane in one block
                 for (int jb = warp; jb < P.kw; jb += kWarps) {
                     uint32_t *blk = xw + jb * NT * 64;
