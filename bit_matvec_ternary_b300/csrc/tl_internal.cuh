@@ -17,11 +17,13 @@ namespace tl_internal {
 // v * r is within three units in the last place of the IEEE quotient
 // fl(v / s), so it rounds to the same integer unless it lies that close to
 // a half-integer (or is not finite); only then is the quotient formed.
+// With q = rint(t), t - q is exact (q is within 0.5 of t) and 0.5 - |t - q|
+// is t's distance to the nearest half-integer; the fast path asks for more
+// than |t| * 2^-20 of it.
 __device__ __forceinline__ float quant_round(float v, float s, float r) {
     const float t = __fmul_rn(v, r);
-    const float d = fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f));
-    // |t| < 512 on the fast path, so t - floor(t) is exact
-    if (d > __fmul_rn(fabsf(t), 0x1p-20f) && fabsf(t) < 512.f) return rintf(t);
+    const float q = rintf(t);
+    if (fabsf(__fsub_rn(t, q)) < __fmaf_rn(-fabsf(t), 0x1p-20f, 0.5f)) return q;
     return rintf(__fdiv_rn(v, s));
 }
 #endif

@@ -71,10 +71,9 @@ constexpr int kCtasPerSm = 1;         // resident CTAs per SM (registers allow 1
 constexpr int kGridPerSm = 1;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 2;             // bulk copies in flight per warp
-// Tiles (512 B each) per bulk copy: 8, or 4 at eight tokens, where the
-// staged activations take 64 KB (two CTAs still fit in one SM's shared
-// memory for plans of up to 8 row tiles per CTA).
-__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 4 ? 8 : 4; }
+// Tiles (512 B each) per bulk copy: 8, or 6 at eight tokens, where the
+// staged activations take 64 KB of the CTA's shared memory.
+__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 4 ? 8 : 6; }
 __host__ __device__ constexpr int ring_bytes(int nt) { return kWarps * kSlots * chunk_tiles(nt) * 512; }
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
@@ -541,18 +540,16 @@ __device__ __forceinline__ void stage_group(uint32_t *blk, int n, int o, const u
         const float sv = qs[n], rv = qr[n], zf = (float)qz[n], qlo = sym ? -127.f : -128.f;
         uint32_t *dst = blk + (qd * NT + n) * 16 + 2 * (m & 1) + (o & 1);
         uint32_t st[4];
-        int isum = 0;
 #pragma unroll
         for (int tt = 0; tt < 4; ++tt) {
             const float x0 = __uint_as_float(wd[tt] << 16), x1 = __uint_as_float(wd[tt] & 0xFFFF0000u);
             const float q0 = fminf(fmaxf(__fadd_rn(tl_internal::quant_round(x0, sv, rv), zf), qlo), 127.f);
             const float q1 = fminf(fmaxf(__fadd_rn(tl_internal::quant_round(x1, sv, rv), zf), qlo), 127.f);
-            isum += (int)q0 + (int)q1;
+            sum = __fadd_rn(sum, __fadd_rn(q0, q1));   // integers: exact
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(q0, f), __fmul_rn(q1, f));
             st[tt] = *reinterpret_cast<const uint32_t *>(&b2);
         }
         store_rotated(dst, st, qd);
-        sum = (float)isum;
     } else if (kModeA) {
         const int m = o >> 1, qd = m >> 1;
         // 2^(kT - 2q) in both halves: an exact bf16 product for values in the
