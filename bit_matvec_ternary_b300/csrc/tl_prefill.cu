@@ -12,8 +12,10 @@
 // One CTA computes a 128-row x 256-token tile of Y:
 //   warp 0      TMA producer: activation tiles X[256 tokens][64 k] (bf16)
 //   warp 1      TMEM owner and MMA issuer (one elected lane)
-//   warps 2..5  weight decoders during the K loop, then the epilogue
-//               (TMEM -> registers -> scale -> global)
+//   warps 2..9  weight decoders during the K loop (one 16-row tile of the
+//               CTA's eight each, two warps per SM sub-partition), then the
+//               epilogue (TMEM -> registers -> scale -> global; the two warps
+//               of a TMEM lane quarter take half of the tokens each)
 // STAGES-deep ring of (A, B) shared-memory stages guarded by mbarriers.
 // Every wait is bounded: after ~2^31 SM cycles the CTA records
 // TL_DEVERR_TIMEOUT in the workspace status word, stops issuing work, waits
@@ -43,8 +45,11 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
-constexpr int DEC_WARPS = 4;
+constexpr int DEC_WARPS = 8;
+constexpr int THREADS = 64 + 32 * DEC_WARPS;
+constexpr int RPW = BM / 16 / DEC_WARPS;            // row tiles decoded per warp
+constexpr int EPI_COLS = BN / (DEC_WARPS / 4);      // tokens per epilogue warp
+static_assert(RPW * DEC_WARPS * 16 == BM && DEC_WARPS % 4 == 0, "decoder split");
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr long long WAIT_LIMIT = 1ll << 31;   // SM cycles
 
@@ -279,26 +284,26 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         }
     } else {
         // ---------------- weight decoders, then the epilogue
-        const int dw = warp - 2;            // row tiles 2dw, 2dw+1 of the 8 in the CTA tile
+        const int dw = warp - 2;            // row tiles RPW dw .. RPW dw + RPW - 1 of the CTA's 8
         const int g = lane >> 2, t = lane & 3;
-        const int rt_base = mt * 8 + 2 * dw;
+        const int rt_base = mt * 8 + RPW * dw;
         const int rts = (a.M[gi] + 15) / 16;
         const char *pk = a.packed[gi];
         // The weights do not depend on the previous kernel: bring this warp's
         // two row tiles' whole K range into L2 first (their tiles are
         // contiguous along K), so the loads below find them there.
-        if (lane < 2 && rt_base + lane < rts && NKB > 0)
+        if (lane < RPW && rt_base + lane < rts && NKB > 0)
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
                              pk + ((long long)(rt_base + lane) * a.KB + kb_lo) * 512),
                          "r"((uint32_t)NKB * 512u)
                          : "memory");
-        // two TL2P tiles (one per row tile) per 128 columns; prefetch ring of 4
+        // RPW TL2P tiles (one per row tile) per 128 columns; prefetch ring of 4
         constexpr int RING = 4;
-        uint4 ring[RING][2];
+        uint4 ring[RING][RPW];
 #pragma unroll
         for (int i = 0; i < RING; ++i)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
+            for (int r = 0; r < RPW; ++r) {
                 ring[i][r] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // zero weights
                 if (i < NKB && rt_base + r < rts)
                     ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + kb_lo + i) * 512 + lane * 16);
@@ -308,10 +313,12 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             for (int i = 0; i < RING; ++i) {
                 const int kb = kb0 + i;       // block index within this split
                 if (kb < NKB) {
-                    const uint4 cur0 = ring[i][0], cur1 = ring[i][1];
+                    uint4 cur[RPW];
+#pragma unroll
+                    for (int r = 0; r < RPW; ++r) cur[r] = ring[i][r];
                     const int nb = kb + RING;
 #pragma unroll
-                    for (int r = 0; r < 2; ++r)
+                    for (int r = 0; r < RPW; ++r)
                         if (nb < NKB && rt_base + r < rts)
                             ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + kb_lo + nb) * 512 + lane * 16);
 #pragma unroll
@@ -323,8 +330,8 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                         ok = __all_sync(0xffffffffu, ok && mbar_wait(empty(s), ph ^ 1u, a.status));
                         if (ok) {
                             uint8_t *a_stage = smem + s * STAGE_BYTES;
-                            store_half(a_stage, 2 * dw, g, t, cur0, h);
-                            store_half(a_stage, 2 * dw + 1, g, t, cur1, h);
+#pragma unroll
+                            for (int r = 0; r < RPW; ++r) store_half(a_stage, RPW * dw + r, g, t, cur[r], h);
                             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                             __syncwarp();
                             if (lane == 0) mbar_arrive(full_a(s));
@@ -338,6 +345,7 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         const bool got = __all_sync(0xffffffffu, ok && mbar_wait(tmem_full, 0u, a.status));
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const int q = warp & 3;
+        const int c_lo = (dw / 4) * EPI_COLS, c_hi = c_lo + EPI_COLS;   // this warp's tokens
         const int row_local = 32 * q + lane;
         const int row = mt * BM + row_local;
         const bool row_ok = row < a.M[gi];
@@ -367,7 +375,7 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
         if (got && a.S == 1) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
                 if (!row_ok) continue;
@@ -387,7 +395,7 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             float *mine = a.part + (tile * a.S + split) * BN * BM;
             if (got) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
 #pragma unroll
@@ -408,7 +416,7 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                 if (row_ok) {
                     // 32 tokens at a time: each split's 32 loads are issued together
 #pragma unroll 1
-                    for (int c0 = 0; c0 < BN && nt * BN + c0 < a.N; c0 += 32) {
+                    for (int c0 = c_lo; c0 < c_hi && nt * BN + c0 < a.N; c0 += 32) {
                         float acc2[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) acc2[j] = 0.f;
@@ -475,11 +483,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 namespace tl_internal {
 
 namespace {
-// K splits for a group: enough CTAs to cover the SMs when the tiles alone
-// do not, each split at least 4 blocks of 128 columns.
+// K splits for a group whose tiles alone do not cover the SMs: the count
+// (each split at least 4 blocks of 128 columns) with the fewest blocks on
+// the busiest SM -- waves of CTAs times blocks per split -- counting each
+// partial tile the completing CTA reads back as one block more.
 int prefill_splits(int tiles, int KB, int sms) {
     if (tiles >= sms) return 1;
-    return std::max(1, std::min(sms / tiles, KB / 4));
+    int best = 1;
+    long long cost = (long long)KB;
+    for (int S = 2; S <= KB / 4; ++S) {
+        const long long waves = ((long long)tiles * S + sms - 1) / sms;
+        const long long c = waves * ((KB + S - 1) / S) + (S - 1);
+        if (c < cost) {
+            best = S;
+            cost = c;
+        }
+    }
+    return best;
 }
 
 // Workspace of a prefill call: the status word at the front, nothing else
