@@ -56,6 +56,12 @@ tl_status device_sms(int *sms);
 tl_status head_init_device();
 tl_status fused_init_device();
 
+// The per-token quantiser (as tl_quantize_act) over bf16 X [N][K]: Q as int8,
+// or with bf16_out the same integers held exactly in bf16; launched with the
+// programmatic-dependent-launch attribute.
+tl_status launch_quant(const void *X_bf16, int N, int K, void *Q, bool bf16_out, float *s,
+                       int32_t *z, int symmetric, cudaStream_t stream);
+
 size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms);
 bool prefill_supported(int N, int K);
 tl_status prefill_init_device();

@@ -1565,14 +1565,15 @@ constexpr int kQChunk = 4096;          // activations quantised per CTA
 
 // Token n, chunk c (kQT threads).  kLaunch: a launch of its own, which
 // waits for the previous kernel on the stream and lets the next one start.
-template <bool kLaunch, int kQT = kQThreads>
+template <bool kLaunch, int kQT = kQThreads, bool kBfOut = false>
 __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int K, int vec,
-                                            int8_t *__restrict__ Q, float *__restrict__ s_out,
+                                            void *__restrict__ Q, float *__restrict__ s_out,
                                             int32_t *__restrict__ z_out, int symmetric, int n,
                                             int c) {
     const int k0 = c * kQChunk;
     const uint16_t *x = X + (long long)n * K;
-    int8_t *q = Q + (long long)n * K;
+    int8_t *q = static_cast<int8_t *>(Q) + (long long)n * K;
+    __nv_bfloat16 *qb = static_cast<__nv_bfloat16 *>(Q) + (long long)n * K;   // (kBfOut)
     // the previous kernel on the stream may still be writing X
     if (kLaunch) griddep_wait();
     float lo = 0.f, hi = 0.f;
@@ -1646,10 +1647,32 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     const float zf = (float)z_sh;
     const float qlo = symmetric ? -127.f : -128.f;
     const int k1 = min(K, k0 + kQChunk);
-    auto one = [&](float v) {
-        const float t = fminf(fmaxf(__fadd_rn(tl_internal::quant_round(v, s, r), zf), qlo), 127.f);
-        return (uint32_t)(uint8_t)(int8_t)(int)t;
+    auto qv = [&](float v) {
+        return fminf(fmaxf(__fadd_rn(tl_internal::quant_round(v, s, r), zf), qlo), 127.f);
     };
+    auto one = [&](float v) { return (uint32_t)(uint8_t)(int8_t)(int)qv(v); };
+    if (kBfOut) {
+        // the integers as bf16 (exact): 8 per 16-byte store
+        if (vec) {
+            const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+            for (int i = k0 / 8 + threadIdx.x; i < k1 / 8; i += kQT) {
+                const uint4 u = __ldcg(xv + i);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(qv(__uint_as_float(w[j] << 16)),
+                                                                    qv(__uint_as_float(w[j] & 0xFFFF0000u)));
+                    o[j] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                reinterpret_cast<uint4 *>(qb)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            for (int k = k0 + threadIdx.x; k < k1; k += kQT)
+                qb[k] = __float2bfloat16_rn(qv(__uint_as_float((uint32_t)__ldcg(x + k) << 16)));
+        }
+        return;
+    }
     if (vec) {
         // 8 activations per step: one 16-byte load, one 8-byte store
         const uint4 *xv = reinterpret_cast<const uint4 *>(x);
@@ -1671,10 +1694,11 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     }
 }
 
+template <bool kBfOut>
 __global__ void __launch_bounds__(kQThreads)
-tl_quant_kernel(const uint16_t *__restrict__ X, int K, int vec, int8_t *__restrict__ Q,
+tl_quant_kernel(const uint16_t *__restrict__ X, int K, int vec, void *__restrict__ Q,
                 float *__restrict__ s_out, int32_t *__restrict__ z_out, int symmetric) {
-    quant_chunk<true>(X, K, vec, Q, s_out, z_out, symmetric, blockIdx.y, blockIdx.x);
+    quant_chunk<true, kQThreads, kBfOut>(X, K, vec, Q, s_out, z_out, symmetric, blockIdx.y, blockIdx.x);
 }
 
 // ------------------------------------------------------------------ chains
@@ -1915,10 +1939,10 @@ size_t workspace_bytes_for(const tl_weight *Ws, int G, int N, int sms) {
     const int K = Ws[0].K;
     Plan p;
     if (make_plan(Ms, G, K, N, sms, &p) != TL_OK) return 0;
-    if (tl_internal::prefill_supported(N, K))   // the fused mode runs these N in chunks of 8
+    if (tl_internal::prefill_supported(N, K))
         return std::max({tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_BF16, sms),
                          tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_I8, sms),
-                         p.ws_bytes});
+                         tl_internal::prefill_workspace_bytes(Ws, G, N, K, TL_MODE_I8_FUSED, sms)});
     return p.ws_bytes;
 }
 
@@ -2099,6 +2123,28 @@ tl_status decode_scratch_bytes(const tl_weight *Ws, int G, size_t *need, size_t 
     return TL_OK;
 }
 
+tl_status launch_quant(const void *X_bf16, int N, int K, void *Q, bool bf16_out, float *s,
+                       int32_t *z, int symmetric, cudaStream_t stream) {
+    // 16-byte rows: vector loads of X, 8-byte (int8) or 16-byte (bf16) stores of Q
+    const int vec = aligned(X_bf16, 16) && aligned(Q, bf16_out ? 16 : 8) && (K % 8) == 0;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((K + kQChunk - 1) / kQChunk), (unsigned)N);
+    cfg.blockDim = dim3(kQThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le =
+        bf16_out ? cudaLaunchKernelEx(&cfg, tl_quant_kernel<true>, static_cast<const uint16_t *>(X_bf16), K,
+                                      vec, Q, s, z, symmetric ? 1 : 0)
+                 : cudaLaunchKernelEx(&cfg, tl_quant_kernel<false>, static_cast<const uint16_t *>(X_bf16), K,
+                                      vec, Q, s, z, symmetric ? 1 : 0);
+    return le == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+}
+
 tl_status launch_decode(const tl_weight *Ws, int G, const void *X, const float *s,
                         const int32_t *z, void *const *Ys, int N, int mode, int out, void *ws,
                         size_t ws_bytes, unsigned flags, cudaStream_t stream) {
@@ -2158,22 +2204,8 @@ tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, float *s,
     const tl_status st = device_info(&dev);
     if (st != TL_OK) return st;
     if (N > 65535) return TL_ERR_SHAPE;
-    // 16-byte rows: vector loads of X and 8-byte stores of Q
-    const int vec = aligned(X_bf16, 16) && aligned(Q, 8) && (K % 8) == 0;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)((K + kQChunk - 1) / kQChunk), (unsigned)N);
-    cfg.blockDim = dim3(kQThreads);
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, tl_quant_kernel,
-                                              static_cast<const uint16_t *>(X_bf16), K, vec, Q, s, z,
-                                              symmetric ? 1 : 0);
-    return le == cudaSuccess ? TL_OK : TL_ERR_CUDA;
+    return tl_internal::launch_quant(X_bf16, N, K, Q, false, s, z, symmetric,
+                                     static_cast<cudaStream_t>(stream));
 }
 
 tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float *s,
@@ -2201,7 +2233,7 @@ tl_status tl_linear_group(const tl_weight *Ws, int G, const void *X, const float
     st = device_info(&dev);
     if (st != TL_OK) return st;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (mode != TL_MODE_I8_FUSED && tl_internal::prefill_supported(N, Ws[0].K)) {
+    if (tl_internal::prefill_supported(N, Ws[0].K)) {
         if (mode == TL_MODE_BF16 && !aligned(X, 16)) return TL_ERR_ALIGN;
         return tl_internal::launch_prefill(Ws, G, X, s, z, Ys, N, mode, out_dtype, workspace,
                                            workspace_bytes, flags, cs);

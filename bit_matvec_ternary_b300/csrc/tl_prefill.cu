@@ -505,19 +505,22 @@ int prefill_splits(int tiles, int KB, int sms) {
 // Workspace of a prefill call: the status word at the front, nothing else
 // kept zero; its scratch at the back, ending at the workspace's end:
 //   [arrival counter per tile, if K is split: cleared at the start of the call]
-//   [bf16 copy of the int8 activations, mode B]
+//   [bf16 copy of the int8 activations, mode B; the quantised activations as
+//    bf16 and their steps and zero points, TL_MODE_I8_FUSED]
 //   [fp32 partial tiles, if K is split]
 // (offsets below are from the start of that scratch), so prefill and decode
 // calls may share one workspace in any order.
 struct PrefillLayout {
-    size_t cnt, conv, part, back;
+    size_t cnt, conv, qs, qz, part, back;
 };
 PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S) {
     using tl_internal::round256;
     PrefillLayout L;
     L.cnt = 0;
     L.conv = L.cnt + (S > 1 ? round256((size_t)tiles * 8) : 0);
-    L.part = L.conv + (mode == TL_MODE_I8 ? round256((size_t)N * K * 2) : 0);
+    L.qs = L.conv + (mode != TL_MODE_BF16 ? round256((size_t)N * K * 2) : 0);
+    L.qz = L.qs + (mode == TL_MODE_I8_FUSED ? round256((size_t)N * 4) : 0);
+    L.part = L.qz + (mode == TL_MODE_I8_FUSED ? round256((size_t)N * 4) : 0);
     L.back = L.part + (S > 1 ? (size_t)tiles * S * tlp::BN * tlp::BM * 4 : 0);
     return L;
 }
@@ -572,7 +575,7 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     a.KBS = (a.KB + a.S - 1) / a.S;
     a.S = (a.KB + a.KBS - 1) / a.KBS;          // no empty split
     a.N = N;
-    a.mode = mode;
+    a.mode = mode == TL_MODE_BF16 ? TL_MODE_BF16 : TL_MODE_I8;   // the kernel's arithmetic
     a.out = out;
     a.s = s;
     a.z = z;
@@ -590,7 +593,18 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    if (mode == TL_MODE_I8) {
+    if (mode == TL_MODE_I8_FUSED) {
+        // quantise X per token straight into the bf16 operand, with its steps
+        // and zero points in the workspace
+        float *qs = reinterpret_cast<float *>(wsc + L.qs);
+        int32_t *qz = reinterpret_cast<int32_t *>(wsc + L.qz);
+        const tl_status qst = launch_quant(X, N, K, conv, true, qs, qz,
+                                           (flags & TL_FLAG_SYMMETRIC) ? 1 : 0, stream);
+        if (qst != TL_OK) return qst;
+        a.s = qs;
+        a.z = qz;
+        xb = conv;
+    } else if (mode == TL_MODE_I8) {
         cudaLaunchConfig_t cc;
         std::memset(&cc, 0, sizeof cc);
         cc.gridDim = dim3(592);
@@ -621,7 +635,8 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     cfg.blockDim = dim3(tlp::THREADS);
     cfg.dynamicSmemBytes = tlp::SMEM_BYTES;
     cfg.stream = stream;
-    // (mode B: the conversion kernel above, PDL-aware, is the one it follows)
+    // (mode B: the conversion or quantiser kernel above, PDL-aware, is the one
+    // it follows)
     cfg.attrs = pdl;
     cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map) != cudaSuccess) return TL_ERR_CUDA;

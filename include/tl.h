@@ -176,11 +176,12 @@ TL_API tl_status tl_quantize_act(const void *X_bf16, int N, int K, int8_t *Q, fl
  *   mode TL_MODE_I8:   X is int8 [N][K] from tl_quantize_act; s, z [N] required;
  *                      W->rowsum required.
  *   mode TL_MODE_I8_FUSED: X is bf16 [N][K]; s, z ignored (may be NULL);
- *                      W->rowsum required.  Every N runs on the decode
- *                      kernel (in chunks of 8 tokens, each CTA reducing
- *                      each token's whole row for its step and zero point):
- *                      meant for decode and verify batches; prefill-sized N
- *                      is faster as tl_quantize_act + TL_MODE_I8.
+ *                      W->rowsum required.  Up to 255 tokens run on the
+ *                      decode kernel (chunks of 8, each CTA reducing each
+ *                      token's whole row for its step and zero point); from
+ *                      256 tokens the quantiser writes the integers as bf16
+ *                      into the workspace and the tensor-core kernel reads
+ *                      them (two launches instead of three).
  *   out_dtype: TL_OUT_F32 (fp32 Y), TL_OUT_BF16 (bf16 Y, round to nearest
  *              even of the fp32 result), TL_OUT_I32_RAW (mode TL_MODE_I8
  *              only: the exact int32 acc = sum_k w*q, before any correction).

@@ -122,7 +122,8 @@ def test_fused_unaligned_rows_use_scalar_loads(oracle_mod):
 
 @pytest.mark.parametrize("N", [9, 20, 300])
 def test_fused_batches_above_eight(oracle_mod, N):
-    """Any N runs as chunks of 8 on the decode kernel (prefill-sized N too)."""
+    """Chunks of 8 on the decode kernel below 256 tokens; from 256 the
+    quantiser's bf16 integers feed the tensor-core kernel."""
     m = Mat(oracle_mod, 1024, 3072, seed=30)
     X = synth.activations(N, 3072, seed=31)
     Yr = oracle_y(oracle_mod, m, X)
@@ -178,3 +179,24 @@ def test_fused_pdl_chain_in_a_graph(oracle_mod):
     hb = h.cpu().view(torch.int16).numpy().view(np.uint16)
     Yr = oracle_y(oracle_mod, m2, hb)
     assert np.array_equal(first, Yr.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K,N", [(3072, 1024, 512), (1024, 12288, 256), (777, 4096, 300)])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_fused_prefill_sizes(oracle_mod, M, K, N, symmetric):
+    """Prefill-sized batches (the K-split path at K = 12,288, ragged M and N):
+    bit for bit the oracle's quantisation and integer linear, fp32 and bf16
+    out, and a group."""
+    m = Mat(oracle_mod, M, K, seed=M + K + N)
+    X = synth.activations(N, K, seed=N + 3, outlier_frac=0.01)
+    Yr = oracle_y(oracle_mod, m, X, symmetric)
+    Xd = bf16_tensor(X)
+    assert np.array_equal(bits(fused(m, Xd, symmetric)), Yr.view(np.uint32))
+    yb = fused(m, Xd, symmetric, out_dtype=tl.TL_OUT_BF16).cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(yb, oracle_mod.bf16_rne(Yr))
+    m2 = Mat(oracle_mod, 512, K, seed=7)
+    ys = tl.tl_linear_group([m.dev, m2.dev], Xd, mode=F,
+                            flags=tl.TL_FLAG_SYMMETRIC if symmetric else 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(ys[0]), Yr.view(np.uint32))
+    assert np.array_equal(bits(ys[1]), oracle_y(oracle_mod, m2, X, symmetric).view(np.uint32))
