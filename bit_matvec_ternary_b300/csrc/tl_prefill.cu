@@ -175,23 +175,31 @@ __device__ __forceinline__ void griddep_launch() {
 
 // Write the decoded half hh (columns 64hh .. 64hh+63, k-steps 4hh .. 4hh+3)
 // of one 16-row TL2P v2 tile into the A stage as bf16 +-2.0 / 0.  Word j of
-// the lane holds row g + 8(j&1), columns 16s + 8(j>>1) + 2t (+1) in the
+// lane (g, t) holds row g + 8(j&1), columns 16s + 8(j>>1) + 2t (+1) in the
 // fields at bits 2s (16 + 2s); a field holds 1 - w, so moving it to bits
 // 15..14 and flipping bit 14 gives 00 -> 0x4000 (+2), 01 -> 0, 10 -> 0xC000.
-__device__ __forceinline__ void store_half(uint8_t *a_stage, int rt, int g, int t, const uint4 &w,
+// For one k-step the four words are the mma A fragment of a 16 x 16 block,
+// i.e. four 8 x 8 matrices (rows +8 for j odd, columns +8 for j >= 2), which
+// one stmatrix.x4 writes: lane L gives the address of row L % 8 of matrix
+// L / 8.  In the 128-byte swizzle the eight rows of a matrix sit in eight
+// different 16-byte bank groups.
+__device__ __forceinline__ void store_half(uint32_t a_stage, int rt, int lane, const uint4 &w,
                                            int hh) {
     const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+    const int mi = lane >> 3, r = lane & 7;
+    const int row = rt * 16 + r + 8 * (mi & 1);             // row & 7 == r
+    const uint32_t row_addr = a_stage + (uint32_t)((row >> 3) * 1024 + r * 128);
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) {
         const int s = 4 * hh + s4;
+        uint32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t v = ((wd[j] << (14 - 2 * s)) & 0xC000C000u) ^ 0x40004000u;
-            const int row = rt * 16 + g + 8 * (j & 1);
-            const int chunk = 2 * s4 + (j >> 1);
-            const int off = (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4) + 4 * t;
-            *reinterpret_cast<uint32_t *>(a_stage + off) = v;
-        }
+        for (int j = 0; j < 4; ++j) v[j] = ((wd[j] << (14 - 2 * s)) & 0xC000C000u) ^ 0x40004000u;
+        const int chunk = 2 * s4 + (mi >> 1);
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                         row_addr + (uint32_t)((chunk ^ r) << 4)),
+                     "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                     : "memory");
     }
 }
 
@@ -285,7 +293,6 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     } else {
         // ---------------- weight decoders, then the epilogue
         const int dw = warp - 2;            // row tiles RPW dw .. RPW dw + RPW - 1 of the CTA's 8
-        const int g = lane >> 2, t = lane & 3;
         const int rt_base = mt * 8 + RPW * dw;
         const int rts = (a.M[gi] + 15) / 16;
         const char *pk = a.packed[gi];
@@ -329,9 +336,9 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                         // every lane waits; the warp continues only if all of them got through
                         ok = __all_sync(0xffffffffu, ok && mbar_wait(empty(s), ph ^ 1u, a.status));
                         if (ok) {
-                            uint8_t *a_stage = smem + s * STAGE_BYTES;
+                            const uint32_t a_stage = base + (uint32_t)(s * STAGE_BYTES);
 #pragma unroll
-                            for (int r = 0; r < RPW; ++r) store_half(a_stage, RPW * dw + r, g, t, cur[r], h);
+                            for (int r = 0; r < RPW; ++r) store_half(a_stage, RPW * dw + r, lane, cur[r], h);
                             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                             __syncwarp();
                             if (lane == 0) mbar_arrive(full_a(s));
