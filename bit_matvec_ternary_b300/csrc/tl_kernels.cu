@@ -1893,6 +1893,13 @@ tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     pps = std::min<long long>(pps, p->KW > 1 ? std::max<long long>(1, su / (p->KW - 1)) : su);
     pps = std::max<long long>(pps, ceil_div(p->R, kMaxCtaRows - 2));
     pps = std::max<long long>(1, pps);
+    // One slice: whole row tiles per CTA (the grid may leave a few SMs
+    // idle), so that no row tile is split between two CTAs and no CTA waits
+    // on another's exchange slot.
+    if (p->NS == 1) {
+        const long long rpc = ceil_div(p->R, pps);
+        pps = ceil_div(p->R, rpc);
+    }
     const long long Lc = ceil_div(su, pps), LcL = ceil_div(suL, pps);
     if ((p->KW > 1 && Lc < p->KW - 1) || (p->KWL > 1 && LcL < p->KWL - 1)) return TL_ERR_SHAPE;
     auto rows_for = [](long long L, long long kw) { return ceil_div(L + kw - 1, kw) + 1; };
