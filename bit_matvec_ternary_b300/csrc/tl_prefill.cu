@@ -71,7 +71,14 @@ struct PrefillArgs {
     int *status;                     // workspace status word
     unsigned long long *cnt;         // [tiles] splits arrived (S > 1); zero between launches
     float *part;                     // [tiles][S][BN][BM] partial sums (S > 1)
+    int ystore;                      // whole tiles leave by TMA stores (ymap below)
 };
+
+// Tensor maps of the group's outputs Y_g [N][M_g] for the TMA-store epilogue.
+struct YMaps {
+    CUtensorMap m[TL_MAX_GROUP];
+};
+constexpr int SZ_OFF = 128 * 1024;    // per-token steps and zero points, after the staged tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -204,7 +211,8 @@ __device__ __forceinline__ void store_half(uint32_t a_stage, int rt, int lane, c
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap xmap) {
+tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap xmap,
+                  const __grid_constant__ YMaps ym) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -380,7 +388,61 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         };
         const float sc = row_ok ? a.scale[gi][row] : 0.f;
         const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
-        if (got && a.S == 1) {
+        if (a.S == 1 && a.ystore) {
+            // The tile is assembled in the stage buffers (idle once the MMAs
+            // are done) in Y's own [token][row] layout and leaves by one TMA
+            // store; rows past M and tokens past N lie outside the tensor and
+            // are not written.  Every epilogue warp passes both named barriers
+            // whatever happened before.
+            const int esz = a.out == TL_OUT_BF16 ? 2 : 4;
+            float *s_sm = reinterpret_cast<float *>(smem + SZ_OFF);
+            int *z_sm = reinterpret_cast<int *>(smem + SZ_OFF + BN * 4);
+            if (a.mode != TL_MODE_BF16) {
+                const int et = threadIdx.x - 64, n = nt * BN + et;   // 256 epilogue threads
+                s_sm[et] = n < a.N ? a.s[n] : 0.f;
+                z_sm[et] = n < a.N ? a.z[n] : 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
+            if (got) {
+#pragma unroll 1
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int nl = c0 + j;
+                        uint8_t *dst = smem + ((size_t)nl * BM + row_local) * esz;
+                        const float half = __uint_as_float(r[j]) * 0.5f;
+                        float y;
+                        if (a.mode == TL_MODE_BF16) {
+                            y = __fmul_rn(half, sc);
+                        } else {
+                            const int iacc = __float2int_rn(half);
+                            if (a.out == TL_OUT_I32_RAW) {
+                                *reinterpret_cast<int32_t *>(dst) = iacc;
+                                continue;
+                            }
+                            y = __fmul_rn(__fmul_rn((float)(iacc - z_sm[nl] * rsum), s_sm[nl]), sc);
+                        }
+                        if (a.out == TL_OUT_F32)
+                            *reinterpret_cast<float *>(dst) = y;
+                        else
+                            *reinterpret_cast<__nv_bfloat16 *>(dst) = __float2bfloat16_rn(y);
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
+            if (warp == 2 && lane == 0 && got) {
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                        reinterpret_cast<uint64_t>(&ym.m[gi])),
+                    "r"(mt * BM), "r"(nt * BN), "r"(base)
+                    : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            }
+        } else if (got && a.S == 1) {
 #pragma unroll 1
             for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                 uint32_t r[32];
@@ -646,7 +708,29 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     // it follows)
     cfg.attrs = pdl;
     cfg.numAttrs = (flags & TL_FLAG_PDL) ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map) != cudaSuccess) return TL_ERR_CUDA;
+    // Outputs that TMA can write whole tiles of (16-byte aligned, rows of a
+    // multiple of 16 bytes) leave by TMA stores; otherwise by element stores.
+    tlp::YMaps ym;
+    std::memset(&ym, 0, sizeof ym);
+    a.ystore = a.S == 1 ? 1 : 0;
+    const size_t esz = out == TL_OUT_BF16 ? 2 : 4;
+    const CUtensorMapDataType ydt = out == TL_OUT_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : out == TL_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                        : CU_TENSOR_MAP_DATA_TYPE_INT32;
+    for (int g = 0; g < G && a.ystore; ++g) {
+        if (reinterpret_cast<uintptr_t>(Ys[g]) % 16 != 0 || ((size_t)Ws[g].M * esz) % 16 != 0) {
+            a.ystore = 0;
+            break;
+        }
+        const cuuint64_t ydims[2] = {(cuuint64_t)Ws[g].M, (cuuint64_t)N};
+        const cuuint64_t ystr[1] = {(cuuint64_t)Ws[g].M * esz};
+        const cuuint32_t ybox[2] = {(cuuint32_t)tlp::BM, (cuuint32_t)tlp::BN};
+        if (fn(&ym.m[g], ydt, 2, Ys[g], ydims, ystr, ybox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            a.ystore = 0;
+    }
+    if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map, ym) != cudaSuccess) return TL_ERR_CUDA;
     return TL_OK;
 }
 
