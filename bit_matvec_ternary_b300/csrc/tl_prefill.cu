@@ -46,11 +46,16 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DEC_WARPS = 8;
-constexpr int THREADS = 64 + 32 * DEC_WARPS;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI0 = 2 + DEC_WARPS;                 // first epilogue warp
+constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
 constexpr int RPW = BM / 16 / DEC_WARPS;            // row tiles decoded per warp
-constexpr int EPI_COLS = BN / (DEC_WARPS / 4);      // tokens per epilogue warp
-static_assert(RPW * DEC_WARPS * 16 == BM && DEC_WARPS % 4 == 0, "decoder split");
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int EPI_COLS = BN / (EPI_WARPS / 4);      // tokens per epilogue warp
+static_assert(RPW * DEC_WARPS * 16 == BM && EPI_WARPS % 4 == 0 && EPI0 % 4 == 2, "warp roles");
+constexpr int ACC_BUFS = 2;                         // TMEM accumulators (BN columns each)
+constexpr int EST_BYTES = 32 * 32 * 4;              // one epilogue warp's staging of 32 x 32 outputs
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EST_BYTES + 1024 /*align*/ +
+                           256 /*barriers*/;
 constexpr long long WAIT_LIMIT = 1ll << 31;   // SM cycles
 
 struct PrefillArgs {
@@ -62,8 +67,9 @@ struct PrefillArgs {
     int mt_off[TL_MAX_GROUP + 1];   // 128-row tiles, prefix over the group
     int G;
     int KB;                          // 128-column TL2P blocks
-    int KBS;                         // blocks per K split (grid z)
+    int KBS;                         // blocks per K split
     int S;                           // K splits
+    int MT, NTT;                     // 128-row tiles, 256-token tiles
     int N;
     int mode, out;
     const float *s;
@@ -74,11 +80,11 @@ struct PrefillArgs {
     int ystore;                      // whole tiles leave by TMA stores (ymap below)
 };
 
-// Tensor maps of the group's outputs Y_g [N][M_g] for the TMA-store epilogue.
+// Tensor maps of the group's outputs Y_g [N][M_g] (boxes of 32 rows x 32
+// tokens) for the TMA-store epilogue.
 struct YMaps {
     CUtensorMap m[TL_MAX_GROUP];
 };
-constexpr int SZ_OFF = 128 * 1024;    // per-token steps and zero points, after the staged tile
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -210,6 +216,27 @@ __device__ __forceinline__ void store_half(uint32_t a_stage, int rt, int lane, c
     }
 }
 
+// One work item: a 128-row x 256-token tile of one K split.
+struct Item {
+    int mt_global, nt, split, gi, mt, kb_lo, NKB;
+};
+__device__ __forceinline__ Item item_of(const PrefillArgs &a, int it) {
+    Item t;
+    t.mt_global = it % a.MT;
+    t.nt = (it / a.MT) % a.NTT;
+    t.split = it / (a.MT * a.NTT);
+    t.gi = 0;
+    while (t.gi + 1 < a.G && a.mt_off[t.gi + 1] <= t.mt_global) ++t.gi;
+    t.mt = t.mt_global - a.mt_off[t.gi];
+    t.kb_lo = t.split * a.KBS;
+    t.NKB = min(a.KB, t.kb_lo + a.KBS) - t.kb_lo;
+    return t;
+}
+
+// Persistent: CTA c takes items c, c + gridDim.x, ...  Every role walks the
+// same items in the same order; the stage ring and its barriers run on
+// across items, and the accumulator alternates between two TMEM buffers,
+// so the epilogue warps finish one item while the MMAs of the next run.
 __global__ void __launch_bounds__(THREADS, 1)
 tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap xmap,
                   const __grid_constant__ YMaps ym) {
@@ -217,27 +244,22 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    // bars: full_a[S], full_b[S], empty[S], tmem_full; then the TMEM address
+    uint8_t *est = smem + STAGES * STAGE_BYTES;                       // epilogue staging
+    uint64_t *bars = reinterpret_cast<uint64_t *>(est + EPI_WARPS * EST_BYTES);
+    // bars: full_a[S], full_b[S], empty[S], acc_full[2], acc_empty[2]; then the
+    // TMEM address and the split epilogue's flag
     const uint32_t bar0 = smem_u32(bars);
     auto full_a = [&](int s) { return bar0 + 8u * s; };
     auto full_b = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-    const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 1);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(bars + 3 * STAGES + 2);
+    auto acc_full = [&](int b) { return bar0 + 8u * (3 * STAGES + b); };
+    auto acc_empty = [&](int b) { return bar0 + 8u * (3 * STAGES + ACC_BUFS + b); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 2 * ACC_BUFS);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(bars + 3 * STAGES + 2 * ACC_BUFS + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt_global = blockIdx.x;
-    const int nt = blockIdx.y;
-    const int split = blockIdx.z;
-    int gi = 0;
-    while (gi + 1 < a.G && a.mt_off[gi + 1] <= mt_global) ++gi;
-    const int mt = mt_global - a.mt_off[gi];
-    // this CTA's K blocks [kb_lo, kb_hi)
-    const int kb_lo = split * a.KBS, kb_hi = min(a.KB, kb_lo + a.KBS);
-    const int NKB = kb_hi - kb_lo;
-    const int KSTEPS = NKB * 2;
+    const int n_items = a.MT * a.NTT * a.S;
+    const int my_items = blockIdx.x < n_items ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -245,13 +267,16 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(tmem_full, 1);
+        for (int b = 0; b < ACC_BUFS; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), EPI_WARPS);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
-                     "r"((uint32_t)BN));
+                     "r"((uint32_t)(ACC_BUFS * BN)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -264,259 +289,296 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         // ---------------- activation producer
         griddep_wait();
         if (lane == 0) {
-            for (int ks = 0; ks < KSTEPS && ok; ++ks) {
-                const int s = ks % STAGES;
-                const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-                if (!mbar_wait(empty(s), ph ^ 1u, a.status)) { ok = false; break; }
-                mbar_expect_tx(full_b(s), B_BYTES);
-                tma_load_2d(base + s * STAGE_BYTES + A_BYTES, &xmap, kb_lo * 128 + ks * BK, nt * BN,
-                            full_b(s));
+            int gs = 0;                                   // stages issued so far
+            for (int j = 0; j < my_items && ok; ++j) {
+                const Item t = item_of(a, blockIdx.x + j * gridDim.x);
+                for (int ks = 0; ks < 2 * t.NKB; ++ks, ++gs) {
+                    const int s = gs % STAGES;
+                    const uint32_t ph = (uint32_t)(gs / STAGES) & 1u;
+                    if (!mbar_wait(empty(s), ph ^ 1u, a.status)) { ok = false; break; }
+                    mbar_expect_tx(full_b(s), B_BYTES);
+                    tma_load_2d(base + s * STAGE_BYTES + A_BYTES, &xmap, t.kb_lo * 128 + ks * BK,
+                                t.nt * BN, full_b(s));
+                }
             }
             // drain: every copy this lane issued must land before the CTA exits
-            const int issued = ok ? KSTEPS : 0;
-            for (int ks = (issued > STAGES ? issued - STAGES : 0); ks < issued; ++ks)
-                mbar_wait(full_b(ks % STAGES), (uint32_t)(ks / STAGES) & 1u, a.status);
+            for (int g = (gs > STAGES ? gs - STAGES : 0); g < gs; ++g)
+                mbar_wait(full_b(g % STAGES), (uint32_t)(g / STAGES) & 1u, a.status);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            for (int ks = 0; ks < KSTEPS && ok; ++ks) {
-                const int s = ks % STAGES;
-                const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-                if (!mbar_wait(full_a(s), ph, a.status) || !mbar_wait(full_b(s), ph, a.status)) {
+            int gs = 0;
+            int done = 0;                                 // items whose accumulator was committed
+            for (int j = 0; j < my_items && ok; ++j) {
+                const Item t = item_of(a, blockIdx.x + j * gridDim.x);
+                const int b = j & 1;
+                // the epilogue of item j - 2 has read this accumulator
+                if (j >= ACC_BUFS && !mbar_wait(acc_empty(b), (uint32_t)((j >> 1) - 1) & 1u, a.status)) {
                     ok = false;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a_addr = base + s * STAGE_BYTES;
-                const uint32_t b_addr = a_addr + A_BYTES;
+                const uint32_t d = tmem + (uint32_t)(b * BN);
+                for (int ks = 0; ks < 2 * t.NKB; ++ks, ++gs) {
+                    const int s = gs % STAGES;
+                    const uint32_t ph = (uint32_t)(gs / STAGES) & 1u;
+                    if (!mbar_wait(full_a(s), ph, a.status) || !mbar_wait(full_b(s), ph, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a_addr = base + s * STAGE_BYTES;
+                    const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_f16(tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                            (ks | kk) != 0);
-                mma_commit(empty(s));
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                                (ks | kk) != 0);
+                    mma_commit(empty(s));
+                }
+                if (!ok) break;
+                mma_commit(acc_full(b));
+                done = j + 1;
             }
-            mma_commit(tmem_full);
+            // every MMA issued has retired before TMEM is freed
+            if (done > 0) mbar_wait(acc_full((done - 1) & 1), (uint32_t)((done - 1) >> 1) & 1u, a.status);
+        }
+    } else if (warp < EPI0) {
+        // ---------------- weight decoders
+        const int dw = warp - 2;            // row tiles RPW dw .. RPW dw + RPW - 1 of the item's 8
+        int gs = 0;
+        for (int j = 0; j < my_items && ok; ++j) {
+            const Item t = item_of(a, blockIdx.x + j * gridDim.x);
+            const int rt_base = t.mt * 8 + RPW * dw;
+            const int rts = (a.M[t.gi] + 15) / 16;
+            const char *pk = a.packed[t.gi];
+            const int NKB = t.NKB;
+            // The weights do not depend on the previous kernel: bring this
+            // warp's row tiles' K range into L2 first (their tiles are
+            // contiguous along K), so the loads below find them there.
+            if (lane < RPW && rt_base + lane < rts && NKB > 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 pk + ((long long)(rt_base + lane) * a.KB + t.kb_lo) * 512),
+                             "r"((uint32_t)NKB * 512u)
+                             : "memory");
+            // RPW TL2P tiles (one per row tile) per 128 columns; prefetch ring of 4
+            constexpr int RING = 4;
+            uint4 ring[RING][RPW];
+#pragma unroll
+            for (int i = 0; i < RING; ++i)
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    ring[i][r] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // zero weights
+                    if (i < NKB && rt_base + r < rts)
+                        ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + t.kb_lo + i) * 512 + lane * 16);
+                }
+            for (int kb0 = 0; kb0 < NKB && ok; kb0 += RING) {
+#pragma unroll
+                for (int i = 0; i < RING; ++i) {
+                    const int kb = kb0 + i;       // block index within this split
+                    if (kb < NKB) {
+                        uint4 cur[RPW];
+#pragma unroll
+                        for (int r = 0; r < RPW; ++r) cur[r] = ring[i][r];
+                        const int nb = kb + RING;
+#pragma unroll
+                        for (int r = 0; r < RPW; ++r)
+                            if (nb < NKB && rt_base + r < rts)
+                                ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + t.kb_lo + nb) * 512 + lane * 16);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int g = gs + 2 * kb + h;
+                            const int s = g % STAGES;
+                            const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+                            // every lane waits; the warp continues only if all of them got through
+                            ok = __all_sync(0xffffffffu, ok && mbar_wait(empty(s), ph ^ 1u, a.status));
+                            if (ok) {
+                                const uint32_t a_stage = base + (uint32_t)(s * STAGE_BYTES);
+#pragma unroll
+                                for (int r = 0; r < RPW; ++r) store_half(a_stage, RPW * dw + r, lane, cur[r], h);
+                                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(full_a(s));
+                            }
+                        }
+                    }
+                }
+            }
+            gs += 2 * NKB;
         }
     } else {
-        // ---------------- weight decoders, then the epilogue
-        const int dw = warp - 2;            // row tiles RPW dw .. RPW dw + RPW - 1 of the CTA's 8
-        const int rt_base = mt * 8 + RPW * dw;
-        const int rts = (a.M[gi] + 15) / 16;
-        const char *pk = a.packed[gi];
-        // The weights do not depend on the previous kernel: bring this warp's
-        // two row tiles' whole K range into L2 first (their tiles are
-        // contiguous along K), so the loads below find them there.
-        if (lane < RPW && rt_base + lane < rts && NKB > 0)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                             pk + ((long long)(rt_base + lane) * a.KB + kb_lo) * 512),
-                         "r"((uint32_t)NKB * 512u)
-                         : "memory");
-        // RPW TL2P tiles (one per row tile) per 128 columns; prefetch ring of 4
-        constexpr int RING = 4;
-        uint4 ring[RING][RPW];
-#pragma unroll
-        for (int i = 0; i < RING; ++i)
-#pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                ring[i][r] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);  // zero weights
-                if (i < NKB && rt_base + r < rts)
-                    ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + kb_lo + i) * 512 + lane * 16);
-            }
-        for (int kb0 = 0; kb0 < NKB; kb0 += RING) {
-#pragma unroll
-            for (int i = 0; i < RING; ++i) {
-                const int kb = kb0 + i;       // block index within this split
-                if (kb < NKB) {
-                    uint4 cur[RPW];
-#pragma unroll
-                    for (int r = 0; r < RPW; ++r) cur[r] = ring[i][r];
-                    const int nb = kb + RING;
-#pragma unroll
-                    for (int r = 0; r < RPW; ++r)
-                        if (nb < NKB && rt_base + r < rts)
-                            ring[i][r] = ldg_stream(pk + ((long long)(rt_base + r) * a.KB + kb_lo + nb) * 512 + lane * 16);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int ks = 2 * kb + h;
-                        const int s = ks % STAGES;
-                        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-                        // every lane waits; the warp continues only if all of them got through
-                        ok = __all_sync(0xffffffffu, ok && mbar_wait(empty(s), ph ^ 1u, a.status));
-                        if (ok) {
-                            const uint32_t a_stage = base + (uint32_t)(s * STAGE_BYTES);
-#pragma unroll
-                            for (int r = 0; r < RPW; ++r) store_half(a_stage, RPW * dw + r, lane, cur[r], h);
-                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(full_a(s));
-                        }
-                    }
-                }
-            }
-        }
-        // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows
-        griddep_wait();
-        const bool got = __all_sync(0xffffffffu, ok && mbar_wait(tmem_full, 0u, a.status));
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows
+        const int ew = warp - EPI0;
         const int q = warp & 3;
-        const int c_lo = (dw / 4) * EPI_COLS, c_hi = c_lo + EPI_COLS;   // this warp's tokens
+        const int c_lo = (ew / 4) * EPI_COLS, c_hi = c_lo + EPI_COLS;   // this warp's tokens
         const int row_local = 32 * q + lane;
-        const int row = mt * BM + row_local;
-        const bool row_ok = row < a.M[gi];
-        const int Mg = a.M[gi];
-        // one finished (row, token) value: the sum of +-2 weights, halved here
-        auto emit = [&](int n, float acc2, float sc, int rsum) {
-            const float half = acc2 * 0.5f;
-            float y;
-            if (a.mode == TL_MODE_BF16) {
-                y = __fmul_rn(half, sc);
-            } else {
+        uint8_t *stg = est + ew * EST_BYTES;
+        const uint32_t stg_s = smem_u32(stg);
+        griddep_wait();                      // outputs may still be read by the previous kernel
+        for (int j = 0; j < my_items; ++j) {
+            const Item t = item_of(a, blockIdx.x + j * gridDim.x);
+            const int b = j & 1;
+            const int gi = t.gi, nt = t.nt;
+            const bool got = __all_sync(0xffffffffu, ok && mbar_wait(acc_full(b), (uint32_t)(j >> 1) & 1u, a.status));
+            ok = got;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t acc_t = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN);
+            const int row = t.mt * BM + row_local;
+            const int Mg = a.M[gi];
+            const bool row_ok = row < Mg;
+            const float sc = row_ok ? a.scale[gi][row] : 0.f;
+            const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
+            // one finished (row, token) value from the sum of +-2 weights;
+            // mode B's step and zero point of token n come from lane n % 32
+            auto value = [&](float acc2, float sv, int zv) {
+                const float half = acc2 * 0.5f;
+                if (a.mode == TL_MODE_BF16) return __fmul_rn(half, sc);
                 const int iacc = __float2int_rn(half);
-                if (a.out == TL_OUT_I32_RAW) {
-                    reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * Mg + row] = iacc;
+                return __fmul_rn(__fmul_rn((float)(iacc - zv * rsum), sv), sc);
+            };
+            auto emit = [&](int n, float acc2, float sv, int zv) {
+                if (a.mode != TL_MODE_BF16 && a.out == TL_OUT_I32_RAW) {
+                    reinterpret_cast<int32_t *>(a.Y[gi])[(long long)n * Mg + row] = __float2int_rn(acc2 * 0.5f);
                     return;
                 }
-                const int corr = iacc - a.z[n] * rsum;
-                y = __fmul_rn(__fmul_rn((float)corr, a.s[n]), sc);
-            }
-            if (a.out == TL_OUT_F32)
-                reinterpret_cast<float *>(a.Y[gi])[(long long)n * Mg + row] = y;
-            else
-                reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * Mg + row] =
-                    __float2bfloat16_rn(y);
-        };
-        const float sc = row_ok ? a.scale[gi][row] : 0.f;
-        const int rsum = (row_ok && a.mode == TL_MODE_I8) ? a.rowsum[gi][row] : 0;
-        if (a.S == 1 && a.ystore) {
-            // The tile is assembled in the stage buffers (idle once the MMAs
-            // are done) in Y's own [token][row] layout and leaves by one TMA
-            // store; rows past M and tokens past N lie outside the tensor and
-            // are not written.  Every epilogue warp passes both named barriers
-            // whatever happened before.
-            const int esz = a.out == TL_OUT_BF16 ? 2 : 4;
-            float *s_sm = reinterpret_cast<float *>(smem + SZ_OFF);
-            int *z_sm = reinterpret_cast<int *>(smem + SZ_OFF + BN * 4);
-            if (a.mode != TL_MODE_BF16) {
-                const int et = threadIdx.x - 64, n = nt * BN + et;   // 256 epilogue threads
-                s_sm[et] = n < a.N ? a.s[n] : 0.f;
-                z_sm[et] = n < a.N ? a.z[n] : 0;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
-            if (got) {
+                const float y = value(acc2, sv, zv);
+                if (a.out == TL_OUT_F32)
+                    reinterpret_cast<float *>(a.Y[gi])[(long long)n * Mg + row] = y;
+                else
+                    reinterpret_cast<__nv_bfloat16 *>(a.Y[gi])[(long long)n * Mg + row] = __float2bfloat16_rn(y);
+            };
+            auto release_acc = [&]() {
+                // the accumulator is read: the next item's MMAs may use it
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty(b));
+            };
+            if (!got) {
+                release_acc();
+            } else if (a.S == 1) {
 #pragma unroll 1
                 for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+                    tmem_ld32(acc_t + (uint32_t)c0, r);
+                    if (c0 + 32 >= c_hi) release_acc();
+                    const int nl = nt * BN + c0 + lane;
+                    const float s_l = a.mode != TL_MODE_BF16 && nl < a.N ? a.s[nl] : 0.f;
+                    const int z_l = a.mode != TL_MODE_BF16 && nl < a.N ? a.z[nl] : 0;
+                    if (a.ystore) {
+                        // 32 tokens x this warp's 32 rows through the warp's staging
+                        // buffer and one TMA store (rows past M, tokens past N are
+                        // outside the tensor and not written)
+                        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        __syncwarp();
+                        const int esz = a.out == TL_OUT_BF16 ? 2 : 4;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int nl = c0 + j;
-                        uint8_t *dst = smem + ((size_t)nl * BM + row_local) * esz;
-                        const float half = __uint_as_float(r[j]) * 0.5f;
-                        float y;
-                        if (a.mode == TL_MODE_BF16) {
-                            y = __fmul_rn(half, sc);
-                        } else {
-                            const int iacc = __float2int_rn(half);
-                            if (a.out == TL_OUT_I32_RAW) {
-                                *reinterpret_cast<int32_t *>(dst) = iacc;
-                                continue;
-                            }
-                            y = __fmul_rn(__fmul_rn((float)(iacc - z_sm[nl] * rsum), s_sm[nl]), sc);
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const float sv = __shfl_sync(0xffffffffu, s_l, jj);
+                            const int zv = __shfl_sync(0xffffffffu, z_l, jj);
+                            uint8_t *dst = stg + (jj * 32 + lane) * esz;
+                            const float acc2 = __uint_as_float(r[jj]);
+                            if (a.mode != TL_MODE_BF16 && a.out == TL_OUT_I32_RAW)
+                                *reinterpret_cast<int32_t *>(dst) = __float2int_rn(acc2 * 0.5f);
+                            else if (a.out == TL_OUT_F32)
+                                *reinterpret_cast<float *>(dst) = value(acc2, sv, zv);
+                            else
+                                *reinterpret_cast<__nv_bfloat16 *>(dst) = __float2bfloat16_rn(value(acc2, sv, zv));
                         }
-                        if (a.out == TL_OUT_F32)
-                            *reinterpret_cast<float *>(dst) = y;
-                        else
-                            *reinterpret_cast<__nv_bfloat16 *>(dst) = __float2bfloat16_rn(y);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) {
+                            asm volatile(
+                                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                    reinterpret_cast<uint64_t>(&ym.m[gi])),
+                                "r"(t.mt * BM + 32 * q), "r"(nt * BN + c0), "r"(stg_s)
+                                : "memory");
+                            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                        }
+                    } else {
+                        // element stores (every lane takes part in the shuffles)
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const float sv = __shfl_sync(0xffffffffu, s_l, jj);
+                            const int zv = __shfl_sync(0xffffffffu, z_l, jj);
+                            const int n = nt * BN + c0 + jj;
+                            if (row_ok && n < a.N) emit(n, __uint_as_float(r[jj]), sv, zv);
+                        }
                     }
                 }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
-            if (warp == 2 && lane == 0 && got) {
-                asm volatile(
-                    "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                        reinterpret_cast<uint64_t>(&ym.m[gi])),
-                    "r"(mt * BM), "r"(nt * BN), "r"(base)
-                    : "memory");
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-            }
-        } else if (got && a.S == 1) {
-#pragma unroll 1
-            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
-                if (!row_ok) continue;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = nt * BN + c0 + j;
-                    if (n >= a.N) break;
-                    emit(n, __uint_as_float(r[j]), sc, rsum);
-                }
-            }
-        } else if (a.S > 1) {
-            // split K: this split's partial tile goes to the workspace; the CTA
-            // that completes the tile adds the splits in order and finishes it.
-            // All four epilogue warps pass both named barriers whatever
-            // happened before, so none can be left waiting.
-            const long long tile = (long long)mt_global * gridDim.y + nt;
-            float *mine = a.part + (tile * a.S + split) * BN * BM;
-            if (got) {
+            } else {
+                // split K: this split's partial tile goes to the workspace; the
+                // item that completes the tile adds the splits in split order
+                // and finishes it.  All epilogue warps pass the named barriers
+                // below whatever happened before, so none can be left waiting.
+                const long long tile = (long long)t.mt_global * a.NTT + nt;
+                float *mine = a.part + (tile * a.S + t.split) * BN * BM;
 #pragma unroll 1
                 for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+                    tmem_ld32(acc_t + (uint32_t)c0, r);
+                    if (c0 + 32 >= c_hi) release_acc();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        __stcg(mine + (long long)(c0 + j) * BM + row_local, __uint_as_float(r[j]));
+                    for (int jj = 0; jj < 32; ++jj)
+                        __stcg(mine + (long long)(c0 + jj) * BM + row_local, __uint_as_float(r[jj]));
                 }
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
-            if (warp == 2 && lane == 0) {
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                const unsigned long long before = atomicAdd(a.cnt + tile, 1ull);
-                *last_flag = before + 1 == (unsigned long long)a.S ? 1 : 0;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(DEC_WARPS * 32) : "memory");
-            if (*last_flag) {
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                const float *p0 = a.part + tile * a.S * BN * BM;
-                if (row_ok) {
+            if (a.S > 1) {
+                const long long tile = (long long)t.mt_global * a.NTT + nt;
+                asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory");
+                if (ew == 0 && lane == 0) {
+                    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                    const unsigned long long before = atomicAdd(a.cnt + tile, 1ull);
+                    *last_flag = before + 1 == (unsigned long long)a.S ? 1 : 0;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory");
+                const int last = *last_flag;
+                // (the flag is read by every warp before it can be written again)
+                asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory");
+                if (last) {
+                    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                    const float *p0 = a.part + tile * a.S * BN * BM;
                     // 32 tokens at a time: each split's 32 loads are issued together
 #pragma unroll 1
                     for (int c0 = c_lo; c0 < c_hi && nt * BN + c0 < a.N; c0 += 32) {
+                        const int nl = nt * BN + c0 + lane;
+                        const float s_l = a.mode != TL_MODE_BF16 && nl < a.N ? a.s[nl] : 0.f;
+                        const int z_l = a.mode != TL_MODE_BF16 && nl < a.N ? a.z[nl] : 0;
                         float acc2[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc2[j] = 0.f;
+                        for (int jj = 0; jj < 32; ++jj) acc2[jj] = 0.f;
+                        if (row_ok) {
 #pragma unroll 1
-                        for (int sp = 0; sp < a.S; ++sp) {
-                            const float *ps = p0 + ((long long)sp * BN + c0) * BM + row_local;
-                            float v[32];
+                            for (int sp = 0; sp < a.S; ++sp) {
+                                const float *ps = p0 + ((long long)sp * BN + c0) * BM + row_local;
+                                float v[32];
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = __ldcg(ps + (long long)j * BM);
+                                for (int jj = 0; jj < 32; ++jj) v[jj] = __ldcg(ps + (long long)jj * BM);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) acc2[j] = __fadd_rn(acc2[j], v[j]);
+                                for (int jj = 0; jj < 32; ++jj) acc2[jj] = __fadd_rn(acc2[jj], v[jj]);
+                            }
                         }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int n = nt * BN + c0 + j;
-                            if (n < a.N) emit(n, acc2[j], sc, rsum);
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const float sv = __shfl_sync(0xffffffffu, s_l, jj);
+                            const int zv = __shfl_sync(0xffffffffu, z_l, jj);
+                            const int n = nt * BN + c0 + jj;
+                            if (row_ok && n < a.N) emit(n, acc2[jj], sv, zv);
                         }
                     }
+                    if (ew == 0 && lane == 0) a.cnt[tile] = 0ull;
                 }
-                if (warp == 2 && lane == 0) a.cnt[tile] = 0ull;
             }
         }
+        // the last TMA stores have left shared memory and reached global memory
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
-    if (warp == 1 && lane == 0) mbar_wait(tmem_full, 0u, a.status);  // all MMAs retired
     griddep_launch();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 1) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"((uint32_t)BN));
+                     "r"((uint32_t)(ACC_BUFS * BN)));
     }
 }
 
@@ -700,7 +762,11 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)a.mt_off[G], (unsigned)((N + tlp::BN - 1) / tlp::BN), (unsigned)a.S);
+    a.MT = a.mt_off[G];
+    a.NTT = (N + tlp::BN - 1) / tlp::BN;
+    // persistent: one CTA per SM (shared memory allows one), each taking
+    // every gridDim-th item
+    cfg.gridDim = dim3((unsigned)std::min(a.MT * a.NTT * a.S, sms));
     cfg.blockDim = dim3(tlp::THREADS);
     cfg.dynamicSmemBytes = tlp::SMEM_BYTES;
     cfg.stream = stream;
@@ -724,7 +790,7 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
         }
         const cuuint64_t ydims[2] = {(cuuint64_t)Ws[g].M, (cuuint64_t)N};
         const cuuint64_t ystr[1] = {(cuuint64_t)Ws[g].M * esz};
-        const cuuint32_t ybox[2] = {(cuuint32_t)tlp::BM, (cuuint32_t)tlp::BN};
+        const cuuint32_t ybox[2] = {32, 32};
         if (fn(&ym.m[g], ydt, 2, Ys[g], ydims, ystr, ybox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
