@@ -616,15 +616,17 @@ namespace tl_internal {
 namespace {
 // K splits for a group whose tiles alone do not cover the SMs: the count
 // (each split at least 4 blocks of 128 columns) with the fewest blocks on
-// the busiest SM -- waves of CTAs times blocks per split -- counting each
-// partial tile the completing CTA reads back as one block more.
+// the busiest SM -- rounds of items times blocks per split -- counting each
+// extra split as 8 blocks more (its 128 KB partial tile written, then read
+// back by the item that completes the tile: measured on the 8B groups, a
+// third split of q/k/v cost more than it saved).
 int prefill_splits(int tiles, int KB, int sms) {
     if (tiles >= sms) return 1;
     int best = 1;
     long long cost = (long long)KB;
     for (int S = 2; S <= KB / 4; ++S) {
         const long long waves = ((long long)tiles * S + sms - 1) / sms;
-        const long long c = waves * ((KB + S - 1) / S) + (S - 1);
+        const long long c = waves * ((KB + S - 1) / S) + 8 * (S - 1);
         if (c < cost) {
             best = S;
             cost = c;
