@@ -71,9 +71,9 @@ constexpr int kCtasPerSm = 1;         // resident CTAs per SM (registers allow 1
 constexpr int kGridPerSm = 1;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 2;             // bulk copies in flight per warp
-// Tiles (512 B each) per bulk copy: 8, or 6 at eight tokens, where the
-// staged activations take 64 KB of the CTA's shared memory.
-__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 4 ? 8 : 6; }
+// Tiles (512 B each) per bulk copy: 10 at one or two tokens, 8 at four and
+// 6 at eight, as the staged activations (up to 64 KB) leave room.
+__host__ __device__ constexpr int chunk_tiles(int nt) { return nt <= 2 ? 10 : nt == 4 ? 8 : 6; }
 __host__ __device__ constexpr int ring_bytes(int nt) { return kWarps * kSlots * chunk_tiles(nt) * 512; }
 constexpr int kNMax = 8;              // tokens per launch (mma n = 8)
 constexpr int kMaxDevices = 64;
