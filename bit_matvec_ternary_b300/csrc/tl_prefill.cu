@@ -9,14 +9,18 @@
 // in the 128-byte-swizzled K-major layout the tensor core reads, so no
 // bf16 copy of a weight ever reaches global memory.
 //
-// One CTA computes a 128-row x 256-token tile of Y:
-//   warp 0      TMA producer: activation tiles X[256 tokens][64 k] (bf16)
-//   warp 1      TMEM owner and MMA issuer (one elected lane)
-//   warps 2..9  weight decoders during the K loop (one 16-row tile of the
-//               CTA's eight each, two warps per SM sub-partition), then the
-//               epilogue (TMEM -> registers -> scale -> global; the two warps
-//               of a TMEM lane quarter take half of the tokens each)
-// STAGES-deep ring of (A, B) shared-memory stages guarded by mbarriers.
+// The work is a list of 128-row x 256-token tiles of Y (of K splits, where a
+// group's tiles alone do not cover the SMs).  The launch is persistent: one
+// CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ...:
+//   warp 0       TMA producer: activation tiles X[256 tokens][64 k] (bf16)
+//   warp 1       TMEM owner and MMA issuer (one elected lane)
+//   warps 2..9   weight decoders (one 16-row tile of the item's eight each,
+//                two warps per SM sub-partition)
+//   warps 10..17 epilogue (TMEM -> registers -> scale -> shared -> TMA store;
+//                the two warps of a TMEM lane quarter take half of the tokens)
+// A STAGES-deep ring of (A, B) shared-memory stages guarded by mbarriers runs
+// on across items, and the accumulator alternates between two TMEM buffers,
+// so the epilogue of one item overlaps the MMAs of the next.
 // Every wait is bounded: after ~2^31 SM cycles the CTA records
 // TL_DEVERR_TIMEOUT in the workspace status word, stops issuing work, waits
 // (again bounded) for its own copies in flight, frees TMEM and exits.
