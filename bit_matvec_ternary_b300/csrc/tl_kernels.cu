@@ -20,9 +20,11 @@
 //   CTAs, and CTA c owns a contiguous range of Lc units of slice c / Pps, so
 //   the CTAs of a slice stream the same number of bytes, each stages the
 //   activations of one slice only, and a (row tile, slice) piece spans at
-//   most two CTAs.  The 8 warps split the CTA's units into contiguous ranges.
+//   most two CTAs; a one-slice launch gives each CTA whole row tiles.  One
+//   CTA of 16 warps per SM; the warps split the CTA's units into contiguous
+//   ranges.
 //   Weights.  Each warp streams its units with cp.async.bulk into its own
-//   ring of shared-memory slots (up to 8 tiles per copy, completing on the
+//   ring of shared-memory slots (up to 10 tiles per copy, completing on the
 //   slot's mbarrier), running ahead across slices.  A TL2P v2 tile is in
 //   mma.m16n8k16 A-fragment order and each 2-bit field holds 1 - w, so
 //   register j of k-step m is (word >> 8*(m/4)) & (0x00030003 << 2*(m%4)):
@@ -30,8 +32,9 @@
 //   subnormals (or, for field 10 at q == 3, the smallest normal), exactly
 //   linear in the field.  One AND per two weights, plus one shift per word.
 //   Activations.  Staged per slice in shared memory in B-fragment order; the
-//   k-steps of class q = m % 4 are multiplied by 2^(67 - 2q) (an exponent
-//   add, exact), so every product is (1 - w) * x * 2^-66, exact in fp32.
+//   k-steps of class q = m % 4 are multiplied by 2^(67 - 2q) (a bf16 product
+//   by a power of two, exact), so every product is (1 - w) * x * 2^-66,
+//   exact in fp32.
 //   The staging also sums x over each half block (64 columns).  A tile's
 //   k-steps 0..3 and 4..7 go to two accumulator chains, alternating, and the
 //   next tile to two others; before its MMAs each chain is given minus its
@@ -41,7 +44,8 @@
 //   Activations outside [2^-60, 2^61) in magnitude (mode A only) switch that
 //   token's slice to a scale chosen from its largest exponent.  Columns
 //   n >= N are zero and their results are discarded, so no lane is
-//   predicated off.
+//   predicated off.  The int8 mode that quantises inside the launch stages
+//   each token's quantised integers the same way (kQ).
 //   Reduction.  A warp that covers all of a row tile's units in a slice adds
 //   its sum straight into the CTA's row accumulator (shared memory); rows
 //   split between warps go through per-warp boundary slots that are added in
