@@ -1900,11 +1900,15 @@ tl_status make_plan(const int *Ms, int G, int K, int N, int sms, Plan *p) {
     // One slice: whole row tiles per CTA (the grid may leave a few SMs
     // idle), so that no row tile is split between two CTAs and no CTA waits
     // on another's exchange slot.
+    long long Lc = 0, LcL = 0;
     if (p->NS == 1) {
-        const long long rpc = ceil_div(p->R, pps);
+        const long long rpc = ceil_div(p->R, pps);   // row tiles per CTA
         pps = ceil_div(p->R, rpc);
+        Lc = LcL = rpc * p->KW;
+    } else {
+        Lc = ceil_div(su, pps);
+        LcL = ceil_div(suL, pps);
     }
-    const long long Lc = ceil_div(su, pps), LcL = ceil_div(suL, pps);
     if ((p->KW > 1 && Lc < p->KW - 1) || (p->KWL > 1 && LcL < p->KWL - 1)) return TL_ERR_SHAPE;
     auto rows_for = [](long long L, long long kw) { return ceil_div(L + kw - 1, kw) + 1; };
     const long long rows = std::max(rows_for(Lc, p->KW), rows_for(LcL, p->KWL));

@@ -12,6 +12,7 @@ runs that end a row tile or a warp's share.  It checks that
     accumulators hold;
   * a warp leaves at most two partial row tiles per slice (its two boundary
     slots), and a row tile it claims whole belongs to it alone;
+  * in a one-slice launch every CTA owns whole row tiles;
   * a (row tile, slice) piece spans one or two CTAs, and the kernel's test
     for "split" (piece_split) agrees; in a one-slice launch a split row tile
     has exactly the two pieces the exchange slots expect;
@@ -69,6 +70,8 @@ def walk(p):
             continue
         s, a0, a1 = rng                       # slice-local units [a0, a1)
         kw = _width(p, s)
+        if p["NS"] == 1:                      # one slice: whole row tiles per CTA
+            assert a0 % kw == 0 and a1 % kw == 0, (c, a0, a1, kw)
         rf, rl = a0 // kw, (a1 - 1) // kw
         lo_f, hi_l = a0 - rf * kw, a1 - rl * kw
         assert rl - rf + 1 <= p["rows"] <= p["max_cta_rows"]
