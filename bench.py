@@ -281,6 +281,90 @@ def flush_l2(torch, buf):
     buf.zero_()
 
 
+def _launch_times(torch, call, flush, reps=50, cold_reps=20):
+    """(warm us, cold us) per launch: `reps` launches replayed as one CUDA
+    graph, L2-warm; and the median of single launches with L2 flushed by a
+    256 MiB write before each."""
+    stream = torch.cuda.current_stream()
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(reps):
+            call()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    warm = e0.elapsed_time(e1) * 1e3 / reps
+    cold = []
+    for _ in range(cold_reps):
+        flush_l2(torch, flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        cold.append(a.elapsed_time(b) * 1e3)
+    return warm, statistics.median(cold)
+
+
+def bench_neighbours(args, torch, tl, hbm_peak):
+    """The rows beside the ternary linears, at the 8B shapes, one and eight
+    tokens: the block-scale linear (12288 x 4096, one scale per row and
+    128-column block, seeded normal float weights ternarised by absmean) and
+    the fused RMSNorm + quantisation (hidden 4096) and SwiGLU + quantisation
+    (12288).  Per launch: warm (a graph of 50 launches) and cold (L2 flushed)
+    microseconds; GB/s and the HBM fraction from the cold time and the
+    algorithmic bytes (inputs once, outputs once)."""
+    import numpy as np
+    from bit_matvec_ternary_b300 import synth
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def bf16(a):
+        return torch.from_numpy(synth.to_bf16_bits(a.astype(np.float32)).view(np.int16)).view(
+            torch.bfloat16).cuda()
+
+    def line(warm, cold, alg):
+        return {"warm_us": warm, "cold_us": cold, "algorithmic_bytes": alg,
+                "cold_gbs": alg / (cold * 1e3), "cold_frac_of_hbm": alg / (cold * 1e3) / hbm_peak}
+
+    out = {}
+    rng = np.random.default_rng(7)
+    M, K = 12288, 4096
+    bw = tl.BlockScaledWeight.from_float(rng.standard_normal((M, K), dtype=np.float32) * 0.02)
+    KB = (K + 127) // 128
+    bs = {"shape": "12288x4096, fp32 scale per (row, 128-column block), mode A, fp32 out"}
+    for N in (1, 8):
+        x = bf16(rng.standard_normal((N, K)))
+        y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+        warm, cold = _launch_times(torch, lambda: tl.tl_linear_blockscale(bw, x, out=y), flush)
+        bs[f"n{N}"] = line(warm, cold, tl.tl_packed_bytes(M, K) + 4 * M * KB + 2 * N * K + 4 * N * M)
+    out["blockscale_linear"] = bs
+    del bw
+    D, F = 4096, 12288
+    rq = {"shape": "RMSNorm over 4096 then per-token int8 quantisation (bf16 and int8 out)"}
+    sq = {"shape": "silu(gate) * up over 12288 then per-token int8 quantisation (bf16 and int8 out)"}
+    gamma = bf16(rng.uniform(0.8, 1.2, D))
+    for N in (1, 8):
+        x = bf16(rng.standard_normal((N, D)))
+        warm, cold = _launch_times(torch, lambda: tl.tl_rmsnorm_quant(x, gamma), flush)
+        rq[f"n{N}"] = line(warm, cold, 2 * N * D + 2 * D + 2 * N * D + N * D + 8 * N)
+        gt, ut = bf16(rng.standard_normal((N, F))), bf16(rng.standard_normal((N, F)))
+        warm, cold = _launch_times(torch, lambda: tl.tl_swiglu_quant(gt, ut), flush)
+        sq[f"n{N}"] = line(warm, cold, 4 * N * F + 2 * N * F + N * F + 8 * N)
+    out["rmsnorm_quant"] = rq
+    out["swiglu_quant"] = sq
+    return out
+
+
 def bench_single_linear(args, torch, tl, hbm_peak, cpu):
     """A single 2048 x 1024 ternary linear at one token, modes A and B:
     launch-to-launch latency (back to back, L2-warm: 200 launches replayed
@@ -552,6 +636,8 @@ def main():
                                                  torch, tl, hbm_peak, unit_rms=True)
         extra["single_linear_2048x1024"] = bench_single_linear(
             args, torch, tl, hbm_peak, cpu=rank == 0 and not args.no_cpu)
+        extra.update(bench_neighbours(args, torch, tl, hbm_peak))
+        torch.cuda.empty_cache()
 
     if not args.no_prefill:
         # prefill-sized batch: 512 tokens, int8 symmetric per-token activations,

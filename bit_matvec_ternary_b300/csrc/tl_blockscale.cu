@@ -8,14 +8,16 @@
 //     y[n, m] = sum_b scale[m, b] * sum_{k in b} w[m, k] * x[n, k]
 // on the same TL2P v2 codes, bf16 activations, fp32 sums.
 //
-// Kernel: one warp per 16-row tile, over all of K (no split, so no
-// workspace); lane (g, t) loads its 16 bytes of each tile (eight tiles in
-// flight), decodes the eight k-steps' A fragments to bf16 2w (the field
-// 1 - w moved to the sign and top exponent bits), multiplies them by the
-// tokens' bf16 activations on the tensor cores into fresh per-tile
-// accumulators (two chains), and folds each tile's sums into the row's
-// result with that block's scale (times 1/2).  Activations are read from
-// global memory through L1 (all warps of an SM read the same X).
+// Kernel: one CTA of kBWarps warps per 16-row tile, warp w taking the
+// blocks b = w, w + kBWarps, ... of K (no workspace); lane (g, t) loads its
+// 16 bytes of each of its tiles (up to eight in flight), decodes the eight
+// k-steps' A fragments to bf16 2w (the field 1 - w moved to the sign and
+// top exponent bits), multiplies them by the tokens' bf16 activations on the
+// tensor cores into fresh per-tile accumulators (two chains), and folds each
+// tile's sums into its running result with that block's scale (times 1/2).
+// The warps' results are added in warp order (shared memory), so the sum
+// is the same on every run.  Activations are read from global memory through
+// L1 (all warps of an SM read the same X).
 #include "tl.h"
 #include "tl_internal.cuh"
 
@@ -27,7 +29,7 @@
 
 namespace {
 
-constexpr int kBWarps = 4;
+constexpr int kBWarps = 8;        // warps per row tile (the K split)
 constexpr int kBUnroll = 8;       // tiles loaded ahead per warp
 
 struct BsArgs {
@@ -36,6 +38,7 @@ struct BsArgs {
     const uint16_t *X;            // bf16 [N][K]
     void *Y;
     int M, K, KB, N, out;
+    int x4;                       // X rows start on 4-byte boundaries (X aligned, K even)
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -57,6 +60,8 @@ __device__ __forceinline__ uint32_t dec2w(uint32_t word, int m) {
 __device__ __forceinline__ uint32_t xpair(const BsArgs &a, int n, int k) {
     if (n >= a.N) return 0u;
     const uint16_t *x = a.X + (long long)n * a.K;
+    // k is even: with 4-byte aligned rows the pair is one 32-bit load
+    if (a.x4 && k + 1 < a.K) return __ldg(reinterpret_cast<const unsigned int *>(x + k));
     const uint32_t lo = k < a.K ? __ldg(x + k) : 0u;
     const uint32_t hi = k + 1 < a.K ? __ldg(x + k + 1) : 0u;
     return lo | (hi << 16);
@@ -64,23 +69,25 @@ __device__ __forceinline__ uint32_t xpair(const BsArgs &a, int n, int k) {
 
 __global__ void __launch_bounds__(kBWarps * 32)
 tl_blockscale_kernel(const __grid_constant__ BsArgs a) {
+    __shared__ float part[kBWarps][32][4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int r = blockIdx.x * kBWarps + warp;           // row tile
-    const int R = (a.M + 15) / 16;
-    if (r >= R) return;
+    const int r = blockIdx.x;                            // row tile
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint4 *tiles = a.packed + (long long)r * a.KB * 32 + lane;
     const int m0 = r * 16 + g, m1 = m0 + 8;
     float y[4] = {0.f, 0.f, 0.f, 0.f};                   // rows g, g+8 x tokens 2t, 2t+1
-    for (int b0 = 0; b0 < a.KB; b0 += kBUnroll) {
+    // this warp's blocks: warp, warp + kBWarps, ...
+    for (int b0 = warp; b0 < a.KB; b0 += kBUnroll * kBWarps) {
         uint4 w[kBUnroll];
 #pragma unroll
-        for (int u = 0; u < kBUnroll; ++u)
-            w[u] = b0 + u < a.KB ? tiles[(long long)(b0 + u) * 32] : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kBUnroll; ++u) {
+            const int b = b0 + u * kBWarps;
+            w[u] = b < a.KB ? tiles[(long long)b * 32] : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
         for (int u = 0; u < kBUnroll; ++u) {
-            const int b = b0 + u;
+            const int b = b0 + u * kBWarps;
             if (b >= a.KB) break;
             float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -101,12 +108,19 @@ tl_blockscale_kernel(const __grid_constant__ BsArgs a) {
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #pragma unroll
+    for (int i = 0; i < 4; ++i) part[warp][lane][i] = y[i];
+    __syncthreads();
+    if (warp != 0) return;
+#pragma unroll
     for (int i = 0; i < 4; ++i) {
+        float v = part[0][lane][i];
+#pragma unroll
+        for (int w2 = 1; w2 < kBWarps; ++w2) v = __fadd_rn(v, part[w2][lane][i]);
         const int m = i < 2 ? m0 : m1, n = 2 * t + (i & 1);
         if (m >= a.M || n >= a.N) continue;
         const long long o = (long long)n * a.M + m;
-        if (a.out == TL_OUT_F32) static_cast<float *>(a.Y)[o] = y[i];
-        else static_cast<__nv_bfloat16 *>(a.Y)[o] = __float2bfloat16_rn(y[i]);
+        if (a.out == TL_OUT_F32) static_cast<float *>(a.Y)[o] = v;
+        else static_cast<__nv_bfloat16 *>(a.Y)[o] = __float2bfloat16_rn(v);
     }
 }
 
@@ -131,7 +145,7 @@ tl_status tl_linear_blockscale(const uint32_t *packed, const float *bscale, int 
     const int R = (M + 15) / 16;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)((R + kBWarps - 1) / kBWarps));
+    cfg.gridDim = dim3((unsigned)R);
     cfg.blockDim = dim3(kBWarps * 32);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -149,6 +163,7 @@ tl_status tl_linear_blockscale(const uint32_t *packed, const float *bscale, int 
         a.Y = static_cast<char *>(Y) + (size_t)n0 * M * esz;
         a.M = M; a.K = K; a.KB = (K + 127) / 128; a.N = N - n0 < 8 ? N - n0 : 8;
         a.out = out_dtype;
+        a.x4 = aligned(a.X, 4) && (K % 2) == 0 ? 1 : 0;
         if (cudaLaunchKernelEx(&cfg, tl_blockscale_kernel, a) != cudaSuccess) return TL_ERR_CUDA;
     }
     return TL_OK;
