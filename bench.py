@@ -281,39 +281,47 @@ def flush_l2(torch, buf):
     buf.zero_()
 
 
-def _launch_times(torch, call, flush, reps=50, cold_reps=20):
-    """(warm us, cold us) per launch: `reps` launches replayed as one CUDA
-    graph, L2-warm; and the median of single launches with L2 flushed by a
-    256 MiB write before each."""
+def _graph_us(torch, body, reps, replays=5):
+    """Median device time of one replay of a CUDA graph of `reps` calls of
+    `body`, in microseconds (events on the launching stream)."""
     stream = torch.cuda.current_stream()
-    for _ in range(5):
-        call()
-    torch.cuda.synchronize()
     cs = torch.cuda.Stream()
     cs.wait_stream(stream)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cs):
         for _ in range(reps):
-            call()
-    for _ in range(3):
+            body()
+    for _ in range(2):
         g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    warm = e0.elapsed_time(e1) * 1e3 / reps
-    cold = []
-    for _ in range(cold_reps):
-        flush_l2(torch, flush)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        b.record(stream)
+    t = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
         torch.cuda.synchronize()
-        cold.append(a.elapsed_time(b) * 1e3)
-    return warm, statistics.median(cold)
+        t.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(t)
+
+
+def _cold_us(torch, call, flush, reps=20):
+    """Launch-to-launch microseconds of `call` with L2 flushed before it and
+    no host time inside: a graph of (256 MiB write, call) pairs less a graph
+    of the writes alone, per pair."""
+    both = _graph_us(torch, lambda: (flush_l2(torch, flush), call()), reps)
+    alone = _graph_us(torch, lambda: flush_l2(torch, flush), reps)
+    return (both - alone) / reps
+
+
+def _launch_times(torch, call, flush, reps=50, cold_reps=20):
+    """(warm us, cold us) per launch: `reps` launches replayed as one CUDA
+    graph, L2-warm; and `_cold_us` (L2 flushed before each launch)."""
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    warm = _graph_us(torch, call, reps) / reps
+    return warm, _cold_us(torch, call, flush, cold_reps)
 
 
 def bench_neighbours(args, torch, tl, hbm_peak):
@@ -415,16 +423,7 @@ def bench_single_linear(args, torch, tl, hbm_peak, cpu):
         e1.record(stream)
         torch.cuda.synchronize()
         lat_us = e0.elapsed_time(e1) * 1e3 / reps
-        cold = []
-        for _ in range(20):
-            flush_l2(torch, flush)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            call()
-            b.record(stream)
-            torch.cuda.synchronize()
-            cold.append(a.elapsed_time(b) * 1e3)
-        cold_us = statistics.median(cold)
+        cold_us = _cold_us(torch, call, flush)
         alg = tl.tl_packed_bytes(M, K) + 4 * M + 2 * K + 4 * M + (4 * M + 8 if mode else 0)
         out[name] = {"latency_us": lat_us, "host_loop_us": host_us, "cold_us": cold_us,
                      "algorithmic_bytes": alg,

@@ -52,9 +52,11 @@ inline size_t scratch_offset(size_t ws_bytes, size_t back) {
 
 // SM count of the current device (its attributes set up on first use).
 tl_status device_sms(int *sms);
-// Raise the head and fused kernels' shared-memory limits on the current device.
+// Raise the head, fused and block-scale kernels' shared-memory limits on the
+// current device.
 tl_status head_init_device();
 tl_status fused_init_device();
+tl_status blockscale_init_device();
 
 // The per-token quantiser (as tl_quantize_act) over bf16 X [N][K]: Q as int8,
 // or with bf16_out the same integers held exactly in bf16; launched with the

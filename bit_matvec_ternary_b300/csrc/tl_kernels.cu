@@ -1828,6 +1828,8 @@ tl_status init_device(int dev, DeviceInfo &d) {
     if (pst != TL_OK) return pst;
     pst = tl_internal::fused_init_device();
     if (pst != TL_OK) return pst;
+    pst = tl_internal::blockscale_init_device();
+    if (pst != TL_OK) return pst;
     d.sms = sms;
     d.init.store(1, std::memory_order_release);
     return TL_OK;
