@@ -9,10 +9,11 @@
 // in the 128-byte-swizzled K-major layout the tensor core reads, so no
 // bf16 copy of a weight ever reaches global memory.
 //
-// The work is a list of 128-row x 256-token tiles of Y (of K splits, where a
-// group's tiles alone do not cover the SMs).  The launch is persistent: one
-// CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ...:
-//   warp 0       TMA producer: activation tiles X[256 tokens][64 k] (bf16)
+// The work is a list of 128-row x BN-token tiles of Y (of K splits, where a
+// group's tiles alone do not cover the SMs), BN = 256 or 128 as the host's
+// planner finds faster for the shapes.  The launch is persistent: one CTA per
+// SM walks items blockIdx.x, blockIdx.x + gridDim.x, ...:
+//   warp 0       TMA producer: activation tiles X[BN tokens][64 k] (bf16)
 //   warp 1       TMEM owner and MMA issuer (one elected lane)
 //   warps 2..9   weight decoders (one 16-row tile of the item's eight each,
 //                two warps per SM sub-partition)
@@ -43,23 +44,27 @@
 namespace tlp {
 
 constexpr int BM = 128;               // weight rows per CTA (TMEM lanes)
-constexpr int BN = 256;               // tokens per CTA (TMEM columns)
 constexpr int BK = 64;                // k per stage (one 128-byte swizzle row)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DEC_WARPS = 8;
 constexpr int EPI_WARPS = 8;
 constexpr int EPI0 = 2 + DEC_WARPS;                 // first epilogue warp
 constexpr int THREADS = 32 * (EPI0 + EPI_WARPS);
 constexpr int RPW = BM / 16 / DEC_WARPS;            // row tiles decoded per warp
-constexpr int EPI_COLS = BN / (EPI_WARPS / 4);      // tokens per epilogue warp
 static_assert(RPW * DEC_WARPS * 16 == BM && EPI_WARPS % 4 == 0 && EPI0 % 4 == 2, "warp roles");
 constexpr int ACC_BUFS = 2;                         // TMEM accumulators (BN columns each)
 constexpr int EST_BYTES = 32 * 32 * 4;              // one epilogue warp's staging of 32 x 32 outputs
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_WARPS * EST_BYTES + 1024 /*align*/ +
-                           256 /*barriers*/;
+// Per token-tile width BN (tokens per item, TMEM columns per accumulator):
+// 256 -> four stages of 48 KB, 128 -> six stages of 32 KB; the same shared
+// memory either way.
+__host__ __device__ constexpr int stages_for(int bn) { return bn == 256 ? 4 : 6; }
+__host__ __device__ constexpr int stage_bytes_for(int bn) { return A_BYTES + bn * BK * 2; }
+__host__ __device__ constexpr int smem_for(int bn) {
+    return stages_for(bn) * stage_bytes_for(bn) + EPI_WARPS * EST_BYTES + 1024 /*align*/ +
+           256 /*barriers*/;
+}
+static_assert(smem_for(256) <= 232448 && smem_for(128) <= 232448, "shared memory per CTA");
+static_assert((3 * stages_for(128) + 2 * ACC_BUFS + 2) * 8 <= 256, "barrier area");
 constexpr long long WAIT_LIMIT = 1ll << 31;   // SM cycles
 
 struct PrefillArgs {
@@ -146,15 +151,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
-// kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = 256.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+// kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t idesc_for(int bn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accum) {
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accum) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(IDESC), "r"(accum));
+        "l"(a), "l"(b), "r"(idesc), "r"(accum));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -220,7 +228,7 @@ __device__ __forceinline__ void store_half(uint32_t a_stage, int rt, int lane, c
     }
 }
 
-// One work item: a 128-row x 256-token tile of one K split.
+// One work item: a 128-row x BN-token tile of one K split.
 struct Item {
     int mt_global, nt, split, gi, mt, kb_lo, NKB;
 };
@@ -241,9 +249,15 @@ __device__ __forceinline__ Item item_of(const PrefillArgs &a, int it) {
 // same items in the same order; the stage ring and its barriers run on
 // across items, and the accumulator alternates between two TMEM buffers,
 // so the epilogue warps finish one item while the MMAs of the next run.
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap xmap,
                   const __grid_constant__ YMaps ym) {
+    constexpr int STAGES = stages_for(BN);
+    constexpr int STAGE_BYTES = stage_bytes_for(BN);
+    constexpr int B_BYTES = BN * BK * 2;
+    constexpr int EPI_COLS = BN / (EPI_WARPS / 4);      // tokens per epilogue warp
+    constexpr uint32_t IDESC = idesc_for(BN);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -336,7 +350,7 @@ tl_prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                     const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                        mma_f16(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), IDESC,
                                 (ks | kk) != 0);
                     mma_commit(empty(s));
                 }
@@ -618,22 +632,43 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 namespace tl_internal {
 
 namespace {
-// K splits for a group whose tiles alone do not cover the SMs: the count
-// (each split at least 4 blocks of 128 columns) with the fewest blocks on
-// the busiest SM -- rounds of items times blocks per split -- counting each
-// extra split as 8 blocks more (its 128 KB partial tile written, then read
-// back by the item that completes the tile: measured on the 8B groups, a
-// third split of q/k/v cost more than it saved).
-int prefill_splits(int tiles, int KB, int sms) {
-    if (tiles >= sms) return 1;
-    int best = 1;
-    long long cost = (long long)KB;
-    for (int S = 2; S <= KB / 4; ++S) {
-        const long long waves = ((long long)tiles * S + sms - 1) / sms;
-        const long long c = waves * ((KB + S - 1) / S) + 8 * (S - 1);
-        if (c < cost) {
-            best = S;
-            cost = c;
+// Time of one 128-column block of a 128-token item, in blocks of a 256-token
+// item, and of each extra K split (its partial tile written, then read back
+// by the item that completes the tile), in blocks of a 256-token item; both
+// fitted to the 8B groups at 512 tokens on B300: a 256-token block took
+// 0.76 us, a 128-token block 0.70 us (the tensor cores do half the work, the
+// stage ring and the weight decode do not shrink), and a second split added
+// 14.5 us to o, 16.8 us to down.
+constexpr double kHalfTileBlock = 0.92;
+constexpr double kSplitBlocks = 19.0;
+
+// The plan of one launch: the token-tile width BN, the K splits S (each at
+// least 4 blocks of 128 columns) and blocks per split KBS, chosen for the
+// fewest block-times on the busiest SM -- rounds of items times blocks per
+// split times the block time, plus the splits' cost.  Ties keep BN = 256 and
+// fewer splits.
+struct PrefillPlan {
+    int BN, S, KBS, tiles;
+};
+PrefillPlan prefill_plan(const tl_weight *Ws, int G, int N, int K, int sms) {
+    int mt = 0;
+    for (int g = 0; g < G; ++g) mt += (Ws[g].M + tlp::BM - 1) / tlp::BM;
+    const int KB = (K + 127) / 128;
+    PrefillPlan best{256, 1, KB, 0};
+    double best_cost = -1.0;
+    for (int bn : {256, 128}) {
+        const long long tiles = (long long)mt * ((N + bn - 1) / bn);
+        const double blk = bn == 256 ? 1.0 : kHalfTileBlock;
+        for (int S = 1; S == 1 || S <= KB / 4; ++S) {
+            const int KBS = (KB + S - 1) / S;
+            const int Se = (KB + KBS - 1) / KBS;            // no empty split
+            if (Se != S) continue;
+            const long long waves = (tiles * S + sms - 1) / sms;
+            const double c = (double)waves * KBS * blk + kSplitBlocks * blk * (S - 1);
+            if (best_cost < 0.0 || c < best_cost) {
+                best = PrefillPlan{bn, S, KBS, (int)tiles};
+                best_cost = c;
+            }
         }
     }
     return best;
@@ -650,7 +685,7 @@ int prefill_splits(int tiles, int KB, int sms) {
 struct PrefillLayout {
     size_t cnt, conv, qs, qz, part, back;
 };
-PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S) {
+PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S, int BN) {
     using tl_internal::round256;
     PrefillLayout L;
     L.cnt = 0;
@@ -658,29 +693,23 @@ PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S) {
     L.qs = L.conv + (mode != TL_MODE_BF16 ? round256((size_t)N * K * 2) : 0);
     L.qz = L.qs + (mode == TL_MODE_I8_FUSED ? round256((size_t)N * 4) : 0);
     L.part = L.qz + (mode == TL_MODE_I8_FUSED ? round256((size_t)N * 4) : 0);
-    L.back = L.part + (S > 1 ? (size_t)tiles * S * tlp::BN * tlp::BM * 4 : 0);
+    L.back = L.part + (S > 1 ? (size_t)tiles * S * BN * tlp::BM * 4 : 0);
     return L;
-}
-int prefill_tiles(const tl_weight *Ws, int G, int N) {
-    int mt = 0;
-    for (int g = 0; g < G; ++g) mt += (Ws[g].M + tlp::BM - 1) / tlp::BM;
-    return mt * ((N + tlp::BN - 1) / tlp::BN);
 }
 }  // namespace
 
 size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms) {
-    const int tiles = prefill_tiles(Ws, G, N);
-    int S = prefill_splits(tiles, (K + 127) / 128, sms);
-    const int KBS = ((K + 127) / 128 + S - 1) / S;
-    S = ((K + 127) / 128 + KBS - 1) / KBS;
-    return workspace_need(kStatusBytes, prefill_layout(N, K, mode, tiles, S).back);
+    const PrefillPlan pl = prefill_plan(Ws, G, N, K, sms);
+    return workspace_need(kStatusBytes, prefill_layout(N, K, mode, pl.tiles, pl.S, pl.BN).back);
 }
 
 bool prefill_supported(int N, int K) { return N >= kPrefillMinN && (K % 8) == 0; }
 
 tl_status prefill_init_device() {
-    if (cudaFuncSetAttribute(tlp::tl_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tlp::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(tlp::tl_prefill_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tlp::smem_for(256)) != cudaSuccess ||
+        cudaFuncSetAttribute(tlp::tl_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tlp::smem_for(128)) != cudaSuccess)
         return TL_ERR_CUDA;
     return tlp::encode_fn() ? TL_OK : TL_ERR_UNSUPPORTED;
 }
@@ -707,10 +736,10 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
         a.mt_off[g + 1] = a.mt_off[g] + (Ws[g].M + tlp::BM - 1) / tlp::BM;
     }
     a.KB = (K + 127) / 128;
-    const int tiles = a.mt_off[G] * ((N + tlp::BN - 1) / tlp::BN);
-    a.S = prefill_splits(tiles, a.KB, sms);
-    a.KBS = (a.KB + a.S - 1) / a.S;
-    a.S = (a.KB + a.KBS - 1) / a.KBS;          // no empty split
+    const PrefillPlan pl = prefill_plan(Ws, G, N, K, sms);
+    const int BN = pl.BN, tiles = pl.tiles;
+    a.S = pl.S;
+    a.KBS = pl.KBS;
     a.N = N;
     a.mode = mode == TL_MODE_BF16 ? TL_MODE_BF16 : TL_MODE_I8;   // the kernel's arithmetic
     a.out = out;
@@ -718,7 +747,7 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     a.z = z;
     a.status = static_cast<int *>(ws);
 
-    const PrefillLayout L = prefill_layout(N, K, mode, tiles, a.S);
+    const PrefillLayout L = prefill_layout(N, K, mode, tiles, a.S, BN);
     char *wsc = static_cast<char *>(ws) + scratch_offset(ws_bytes, L.back);
     const void *xb = X;
     __nv_bfloat16 *conv = reinterpret_cast<__nv_bfloat16 *>(wsc + L.conv);
@@ -757,7 +786,7 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)tlp::BK, (cuuint32_t)tlp::BN};
+    const cuuint32_t box[2] = {(cuuint32_t)tlp::BK, (cuuint32_t)BN};
     const cuuint32_t estr[2] = {1, 1};
     auto fn = tlp::encode_fn();
     if (!fn) return TL_ERR_UNSUPPORTED;
@@ -769,12 +798,12 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     a.MT = a.mt_off[G];
-    a.NTT = (N + tlp::BN - 1) / tlp::BN;
+    a.NTT = (N + BN - 1) / BN;
     // persistent: one CTA per SM (shared memory allows one), each taking
     // every gridDim-th item
     cfg.gridDim = dim3((unsigned)std::min(a.MT * a.NTT * a.S, sms));
     cfg.blockDim = dim3(tlp::THREADS);
-    cfg.dynamicSmemBytes = tlp::SMEM_BYTES;
+    cfg.dynamicSmemBytes = tlp::smem_for(BN);
     cfg.stream = stream;
     // (mode B: the conversion or quantiser kernel above, PDL-aware, is the one
     // it follows)
@@ -802,7 +831,9 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             a.ystore = 0;
     }
-    if (cudaLaunchKernelEx(&cfg, tlp::tl_prefill_kernel, a, map, ym) != cudaSuccess) return TL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, BN == 256 ? tlp::tl_prefill_kernel<256> : tlp::tl_prefill_kernel<128>,
+                           a, map, ym) != cudaSuccess)
+        return TL_ERR_CUDA;
     return TL_OK;
 }
 
