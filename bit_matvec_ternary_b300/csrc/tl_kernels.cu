@@ -1566,6 +1566,12 @@ inline int padded_tokens(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 
 // then is the IEEE division taken.
 constexpr int kQThreads = 256;
 constexpr int kQChunk = 4096;          // activations quantised per CTA
+constexpr int kQHeld = 8;              // 16-byte groups a thread keeps in registers
+// A launch of its own whose whole row fits in registers takes one CTA per
+// token (the CTA quantises all of the row); otherwise one CTA per chunk.
+__host__ __device__ __forceinline__ bool quant_held(int vec, int K) {
+    return vec && K / 8 <= kQHeld * kQThreads;
+}
 
 // Token n, chunk c (kQT threads).  kLaunch: a launch of its own, which
 // waits for the previous kernel on the stream and lets the next one start.
@@ -1581,7 +1587,34 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
     // the previous kernel on the stream may still be writing X
     if (kLaunch) griddep_wait();
     float lo = 0.f, hi = 0.f;
-    if (vec) {
+    // A launch of its own whose row fits in registers (thread i holds the
+    // 16-byte groups i, i + kQT, ...) is the token's only CTA: it quantises
+    // the whole row from them instead of reading it again.
+    const bool held = kLaunch && kQT == kQThreads && quant_held(vec, K);
+    uint4 hv[kLaunch ? kQHeld : 1];
+    if (held) {
+        const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+#pragma unroll
+        for (int j = 0; j < (kLaunch ? kQHeld : 1); ++j) {
+            const int i = threadIdx.x + j * kQT;
+            hv[j] = i < K / 8 ? __ldcg(xv + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < (kLaunch ? kQHeld : 1); ++j) {
+            // groups past K hold zeros, which the range includes anyway
+            const uint32_t w[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float a = __uint_as_float(w[e] << 16), b = __uint_as_float(w[e] & 0xFFFF0000u);
+                if (symmetric) {
+                    hi = fmaxf(hi, fmaxf(fabsf(a), fabsf(b)));
+                } else {
+                    lo = fminf(lo, fminf(a, b));
+                    hi = fmaxf(hi, fmaxf(a, b));
+                }
+            }
+        }
+    } else if (vec) {
         const uint4 *xv = reinterpret_cast<const uint4 *>(x);
         for (int i = threadIdx.x; i < K / 8; i += kQT) {
             const uint4 u = __ldcg(xv + i);
@@ -1655,6 +1688,34 @@ __device__ __forceinline__ void quant_chunk(const uint16_t *__restrict__ X, int 
         return fminf(fmaxf(__fadd_rn(tl_internal::quant_round(v, s, r), zf), qlo), 127.f);
     };
     auto one = [&](float v) { return (uint32_t)(uint8_t)(int8_t)(int)qv(v); };
+    if (held) {
+#pragma unroll
+        for (int j = 0; j < (kLaunch ? kQHeld : 1); ++j) {
+            const int i = threadIdx.x + j * kQT;
+            if (i >= K / 8) continue;
+            const uint32_t w[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+            if (kBfOut) {
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(qv(__uint_as_float(w[e] << 16)),
+                                                                    qv(__uint_as_float(w[e] & 0xFFFF0000u)));
+                    o[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                reinterpret_cast<uint4 *>(qb)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                uint32_t o[2] = {0u, 0u};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t lo8 = one(__uint_as_float(w[e] << 16));
+                    const uint32_t hi8 = one(__uint_as_float(w[e] & 0xFFFF0000u));
+                    o[e >> 1] |= (lo8 | (hi8 << 8)) << (16 * (e & 1));
+                }
+                reinterpret_cast<uint2 *>(q)[i] = make_uint2(o[0], o[1]);
+            }
+        }
+        return;
+    }
     if (kBfOut) {
         // the integers as bf16 (exact): 8 per 16-byte store
         if (vec) {
@@ -2146,7 +2207,7 @@ tl_status launch_quant(const void *X_bf16, int N, int K, void *Q, bool bf16_out,
     const int vec = aligned(X_bf16, 16) && aligned(Q, bf16_out ? 16 : 8) && (K % 8) == 0;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)((K + kQChunk - 1) / kQChunk), (unsigned)N);
+    cfg.gridDim = dim3(quant_held(vec, K) ? 1u : (unsigned)((K + kQChunk - 1) / kQChunk), (unsigned)N);
     cfg.blockDim = dim3(kQThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

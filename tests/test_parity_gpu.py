@@ -120,7 +120,7 @@ def test_mode_a_bf16_output(oracle_mod):
     assert rel_err(Y, ref) <= TOL_A + 2.0 ** -8
 
 
-@pytest.mark.parametrize("K", [1, 7, 128, 1000, 4096, 12288])
+@pytest.mark.parametrize("K", [1, 7, 128, 1000, 4096, 12288, 16384, 16392])
 @pytest.mark.parametrize("symmetric", [False, True])
 def test_quantizer_bit_exact(oracle_mod, K, symmetric):
     X = synth.activations(8, K, seed=K, outlier_frac=0.01 if K >= 100 else 0.0)
