@@ -498,9 +498,9 @@ def bench_head(args, torch, tl, hbm_peak):
         out[f"n{N}"] = {"us": ms * 1e3, "algorithmic_bytes": alg,
                         "gbs": alg / (ms / 1e3) / 1e9,
                         "frac_of_hbm": alg / (ms / 1e3) / 1e9 / hbm_peak,
-                        "tokens_s": N / (ms / 1e3)}
+                        "tokens_s": N / (ms / 1e3),
+                        "kernel": "tl_head_kernel" if N <= 2 else "tl_head_mma_kernel"}
     out["shape"] = f"int8 {V}x{D}, fp32 scale per row, argmax fused, logits not written"
-    out["kernel"] = "tl_head_kernel"
     return out
 
 

@@ -40,8 +40,8 @@ def _run(head, X):
             tok.cpu().numpy(), best.cpu().numpy(), tok2.cpu().numpy(), best2.cpu().numpy())
 
 
-@pytest.mark.parametrize("V,D", [(1000, 4096), (37, 16), (5003, 144), (300, 1024)])
-@pytest.mark.parametrize("N", [1, 3, 8])
+@pytest.mark.parametrize("V,D", [(1000, 4096), (37, 16), (5003, 144), (300, 1024), (2049, 512)])
+@pytest.mark.parametrize("N", [1, 3, 4, 5, 8])
 def test_head_matches_oracle_bit_for_bit(oracle_mod, V, D, N):
     H, scale = _table(V, D, V + D)
     head = tl.Head.from_host(H, scale)
@@ -70,6 +70,31 @@ def test_head_ties_and_extreme_positions(oracle_mod):
         _, _, tok_r, best_r = oracle_mod.head(Hc, sc, Q, s, z, return_logits=False)
         assert list(tok) == [a, a] == list(tok_r)
         assert np.array_equal(best.view(np.uint32), best_r.view(np.uint32))
+
+
+@pytest.mark.parametrize("N", [3, 7, 8])
+def test_tensor_core_head_ties_and_largest_sums(oracle_mod, N):
+    """Three to eight tokens (the tensor-core form): equal best rows give the
+    smaller index, and sums of the largest magnitude -- every product
+    -128 x -128, so each warp's fp32 partial sum reaches 2^23 and a row's
+    2^26 -- stay exact."""
+    V, D = 2000, 4096
+    H, scale = _table(V, D, 11)
+    H[5] = H[1500] = 127
+    scale[5] = scale[1500] = 1.0
+    H[7] = -128
+    scale[7] = 3.0
+    X = synth.to_bf16_bits(np.abs(synth.bf16_bits_to_f32(synth.activations(N, D, seed=12))) + 0.5)
+    X[N - 1] = synth.to_bf16_bits(np.full(D, -2.0, dtype=np.float32))   # quantises to -128
+    head = tl.Head.from_host(H, scale)
+    Q, s, z, lg, tok, best, tok2, best2 = _run(head, X)
+    assert (Q[N - 1] == -128).all()
+    acc_r, lg_r, tok_r, best_r = oracle_mod.head(H, scale, Q, s, z)
+    assert acc_r[N - 1, 7] == 128 * 128 * D
+    assert np.array_equal(lg.view(np.uint32), lg_r.view(np.uint32))
+    assert np.array_equal(tok, tok_r) and np.array_equal(tok2, tok_r)
+    assert list(tok[:N - 1]) == [5] * (N - 1)
+    assert np.array_equal(best.view(np.uint32), best_r.view(np.uint32))
 
 
 @pytest.mark.parametrize("N", [1, 8])
