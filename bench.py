@@ -235,7 +235,8 @@ class OracleSample:
                 break
         passes = done / self.shape.ternary_weights()
         desc = (f"layer 0's 7 linears x{done // per_layer} ({done / 1e9:.2f}e9 weights), "
-                f"N={self.N}, mode {'A' if mode == 0 else 'B'}, extrapolated to 252 linears")
+                f"N={self.N}, mode {'A' if mode == 0 else 'B'}, extrapolated to "
+                f"{len(self.order) * self.shape.layers} linears")
         return self.N * passes / el, desc
 
 
@@ -583,6 +584,7 @@ def main():
                   "kernel": "tl_chain_kernel"}
 
     cpu = None
+    host0 = stack.host                      # layer 0's matrices, for the oracle samples
     if rank == 0 and not args.no_cpu:
         sampler = OracleSample(stack.host, shape, 1)
         v, desc = sampler.run(seconds=10.0)
@@ -619,6 +621,12 @@ def main():
                                     "frac_of_hbm": a8 / (ms8c / 1e3) / 1e9 / hbm_peak}
             del st8
             torch.cuda.empty_cache()
+            if rank == 0 and not args.no_cpu:
+                # the oracle on the same eight tokens' work (a bounded sample)
+                s8 = OracleSample(host0, shape, 8)
+                v8, d8 = s8.run(seconds=3.0, mode=0 if mode == tl.TL_MODE_BF16 else 1)
+                extra[name]["cpu_oracle"] = {"value": v8, "unit": "tokens/s", "cores": s8.cores,
+                                             "kind": "oracle", "sample": d8}
 
     # N = 1 in mode B: quantisation inside each linear launch, and the
     # two-launch form (a quantiser launch in front of every linear launch)
@@ -633,6 +641,19 @@ def main():
         # the 0.6B-shaped stack (28 layers, hidden 1024), unit-RMS inputs
         extra["stack_06b_n1"] = bench_stack_line(synth.NEUTRINO_06B, 1, tl.TL_MODE_BF16, args,
                                                  torch, tl, hbm_peak, unit_rms=True)
+        if rank == 0 and not args.no_cpu:
+            # the oracle on layer 0 of the 0.6B-shaped stack (same seeds)
+            sh6, host6 = synth.NEUTRINO_06B, {}
+            for p in synth.PROJ_ORDER:
+                M6, K6 = sh6.linear_shapes()[p]
+                seed6 = synth.matrix_seed(0, 0, p)
+                host6[(0, p)] = (synth.ternary(M6, K6, synth.zero_fraction(sh6, 0, p), seed6),
+                                 synth.scales(M6, seed6))
+            s6 = OracleSample(host6, sh6, 1)
+            v6, d6 = s6.run(seconds=2.0)
+            extra["stack_06b_n1"]["cpu_oracle"] = {"value": v6, "unit": "tokens/s",
+                                                   "cores": s6.cores, "kind": "oracle",
+                                                   "sample": d6}
         extra["single_linear_2048x1024"] = bench_single_linear(
             args, torch, tl, hbm_peak, cpu=rank == 0 and not args.no_cpu)
         extra.update(bench_neighbours(args, torch, tl, hbm_peak))
