@@ -93,8 +93,10 @@ class LinearStack:
         self.X_flat = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=device)
         self.Y_flat = torch.empty(sum(y_sizes), dtype=odt, device=device)
         self.X, self.Q, self.S, self.Z, self.Y = [], [], [], [], []
+        self.x_span, self.y_span = [], []     # each layer's [lo, hi) in X_flat, Y_flat
         xo = yo = 0
         for l in range(self.layers):
+            x_lo, y_lo = xo, yo
             xs, qs, ss, zs, ys = [], [], [], [], []
             for gi, grp in enumerate(GROUPS):
                 K = shp[grp[0]][1]
@@ -116,6 +118,8 @@ class LinearStack:
                 ys.append(outs)
             self.X.append(xs); self.Q.append(qs); self.S.append(ss); self.Z.append(zs)
             self.Y.append(ys)
+            self.x_span.append((x_lo, xo))
+            self.y_span.append((y_lo, yo))
         groups = [[self.weights[l][p] for p in grp] for l in range(self.layers) for grp in GROUPS]
         self.workspace = tl.make_workspace(groups, N, device=device)
         self.graph = None
@@ -132,21 +136,24 @@ class LinearStack:
 
     def run(self, flags: int = tl.TL_FLAG_PDL, stream=None) -> None:
         for l in range(self.layers):
-            for gi, grp in enumerate(GROUPS):
-                ws = [self.weights[l][p] for p in grp]
-                x = self.X[l][gi]
-                if self.mode == tl.TL_MODE_I8:
-                    q, s, z = self.Q[l][gi], self.S[l][gi], self.Z[l][gi]
-                    tl.tl_quantize_act(x, symmetric=self.symmetric, Q=q, s=s, z=z, stream=stream)
-                    tl.tl_linear_group(ws, q, s, z, outs=self.Y[l][gi], mode=self.mode,
-                                       out_dtype=self.out_dtype, workspace=self.workspace,
-                                       flags=flags, stream=stream)
-                else:
-                    if self.mode == tl.TL_MODE_I8_FUSED and self.symmetric:
-                        flags |= tl.TL_FLAG_SYMMETRIC
-                    tl.tl_linear_group(ws, x, outs=self.Y[l][gi], mode=self.mode,
-                                       out_dtype=self.out_dtype, workspace=self.workspace,
-                                       flags=flags, stream=stream)
+            self.run_layer(l, flags, stream)
+
+    def run_layer(self, l: int, flags: int = tl.TL_FLAG_PDL, stream=None) -> None:
+        for gi, grp in enumerate(GROUPS):
+            ws = [self.weights[l][p] for p in grp]
+            x = self.X[l][gi]
+            if self.mode == tl.TL_MODE_I8:
+                q, s, z = self.Q[l][gi], self.S[l][gi], self.Z[l][gi]
+                tl.tl_quantize_act(x, symmetric=self.symmetric, Q=q, s=s, z=z, stream=stream)
+                tl.tl_linear_group(ws, q, s, z, outs=self.Y[l][gi], mode=self.mode,
+                                   out_dtype=self.out_dtype, workspace=self.workspace,
+                                   flags=flags, stream=stream)
+            else:
+                if self.mode == tl.TL_MODE_I8_FUSED and self.symmetric:
+                    flags |= tl.TL_FLAG_SYMMETRIC
+                tl.tl_linear_group(ws, x, outs=self.Y[l][gi], mode=self.mode,
+                                   out_dtype=self.out_dtype, workspace=self.workspace,
+                                   flags=flags, stream=stream)
 
     def chain(self, gate=None, wait_limit: int = 0) -> "tl.Chain":
         """The whole pass as one chain: every launch group of every layer, in
@@ -175,6 +182,64 @@ class LinearStack:
             self.run(flags=flags)
         torch.cuda.synchronize()
         self.graph = g
+        return g
+
+    def capture_e2e(self, hx, hy, flags: int = tl.TL_FLAG_PDL):
+        """Record one pass together with its host copies, as one CUDA graph:
+        pinned host inputs ``hx`` (shaped like ``X_flat``) come in on one copy
+        stream -- layer 0's first, then all the others -- and the outputs go
+        out to pinned ``hy`` (shaped like ``Y_flat``) on a second copy stream
+        in chunks of about a quarter of the layers, each as soon as its last
+        layer is done, with the last layer alone, so the copies overlap the
+        launches.  Each place where the launches wait for a copy or hand one
+        an event costs the pass about a microsecond, so the chunks are few:
+        measured on the 8B stack at one token, per-layer copies took 1.348 ms
+        per pass, these chunks 1.241 ms (1.172 ms without copies; 1.409 ms
+        with all inputs copied before the pass and all outputs after it).
+        Every replay copies all inputs in and all outputs out."""
+        torch = self.torch
+        if not (hx.is_pinned() and hy.is_pinned()):
+            raise ValueError("the host buffers must be pinned")
+        if hx.shape != self.X_flat.shape or hy.shape != self.Y_flat.shape:
+            raise ValueError("host buffers must match X_flat and Y_flat")
+        L = self.layers
+        ins = [(0, 1)] + ([(1, L)] if L > 1 else [])
+        every = max(1, (L - 1 + 3) // 4)
+        outs = [(lo, min(lo + every, L - 1)) for lo in range(0, L - 1, every)] + [(L - 1, L)]
+        main = torch.cuda.Stream()
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        main.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(main):
+            self.run(flags=flags)          # warm: device attributes cached before capture
+        torch.cuda.current_stream().wait_stream(main)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        ev_in = [torch.cuda.Event() for _ in ins]
+        ev_out = [torch.cuda.Event() for _ in outs]
+        with torch.cuda.graph(g, stream=main):
+            cin.wait_stream(main)
+            cout.wait_stream(main)
+            with torch.cuda.stream(cin):
+                for i, (l0, l1) in enumerate(ins):
+                    lo, hi = self.x_span[l0][0], self.x_span[l1 - 1][1]
+                    self.X_flat[lo:hi].copy_(hx[lo:hi], non_blocking=True)
+                    ev_in[i].record(cin)
+            for l in range(L):
+                for i, (l0, _) in enumerate(ins):
+                    if l0 == l:
+                        main.wait_event(ev_in[i])
+                self.run_layer(l, flags, stream=main)
+                for i, (l0, l1) in enumerate(outs):
+                    if l1 == l + 1:
+                        ev_out[i].record(main)
+                        with torch.cuda.stream(cout):
+                            cout.wait_event(ev_out[i])
+                            lo, hi = self.y_span[l0][0], self.y_span[l1 - 1][1]
+                            hy[lo:hi].copy_(self.Y_flat[lo:hi], non_blocking=True)
+            main.wait_stream(cin)
+            main.wait_stream(cout)
+        torch.cuda.synchronize()
+        self.graph_e2e = g
         return g
 
     # ------------------------------------------------------------ accounting

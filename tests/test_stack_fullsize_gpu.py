@@ -72,3 +72,47 @@ def test_full_stack_against_oracle_on_sampled_rows(oracle_mod, weights, N, mode)
     torch.cuda.synchronize()
     assert chain.status() == 0
     assert torch.equal(cs.Y_flat.view(torch.int32), graph_out.view(torch.int32))
+
+
+@pytest.mark.parametrize("N,mode", [(1, tl.TL_MODE_BF16), (8, tl.TL_MODE_I8_FUSED)])
+def test_host_copy_graph_equals_the_device_graph(oracle_mod, weights, N, mode):
+    """The pass with its host copies in the graph (each layer's inputs copied
+    in on one stream ahead of it, its outputs out on another after it): the
+    pinned host outputs equal the device graph's outputs bit for bit, and new
+    host inputs are picked up by the next replay (checked against the oracle
+    on sampled rows of the last layer)."""
+    st = LinearStack(SHAPE, N=N, mode=mode, out_dtype=tl.TL_OUT_F32, symmetric=False,
+                     weights=weights)
+    st.capture()
+    st.graph.replay()
+    torch.cuda.synchronize()
+    ref = st.Y_flat.cpu().numpy().view(np.uint32).copy()
+    hx = torch.empty(st.X_flat.shape, dtype=st.X_flat.dtype, pin_memory=True)
+    hx.copy_(st.X_flat.cpu())
+    hy = torch.zeros(st.Y_flat.shape, dtype=st.Y_flat.dtype, pin_memory=True)
+    g = st.capture_e2e(hx, hy)
+    st.Y_flat.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(hy.numpy().view(np.uint32), ref)
+    # new inputs for the last layer's down projection, from the host only
+    l = SHAPE.layers - 1
+    K = SHAPE.linear_shapes()["down"][1]
+    X = synth.activations(N, K, seed=991, outlier_frac=0.01)
+    lo = st.x_span[l][1] - N * K
+    hx[lo:].copy_(torch.from_numpy(X.view(np.int16).reshape(-1).copy()).view(torch.bfloat16))
+    g.replay()
+    torch.cuda.synchronize()
+    W, scale = weights.host[(l, "down")]
+    M = W.shape[0]
+    rows = _rows(M, 5)
+    Pr = oracle_mod.pack(W[rows])
+    y = hy.numpy()[st.y_span[l][1] - N * M:].reshape(N, M)[:, rows]
+    if mode == tl.TL_MODE_BF16:
+        yr = oracle_mod.linear_a(Pr, scale[rows], len(rows), K, X)
+        assert rel_err(y, yr) <= TOL_A
+    else:
+        Q, s, z = oracle_mod.quant(X)
+        _, yr = oracle_mod.linear_b(Pr, scale[rows], oracle_mod.rowsum(Pr, len(rows), K),
+                                    len(rows), K, Q, s, z)
+        assert np.array_equal(y.view(np.uint32), yr.view(np.uint32))
