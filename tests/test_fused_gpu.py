@@ -47,7 +47,10 @@ def _check_quant(oracle_mod, Y, Q, s, z, symmetric):
     assert torch.equal(Q2, Q) and torch.equal(s2.view(torch.int32), s.view(torch.int32))
 
 
-@pytest.mark.parametrize("N,K", [(1, 4096), (8, 4096), (3, 1024), (2, 333), (1, 12288)])
+# one token's row spans a cluster of up to eight CTAs: 1 (K <= 1024) ... 8,
+# ragged last slices (1025, 4100) and the largest row (32768)
+@pytest.mark.parametrize("N,K", [(1, 4096), (8, 4096), (3, 1024), (2, 333), (1, 12288),
+                                 (2, 4100), (1, 32768)])
 @pytest.mark.parametrize("symmetric", [False, True])
 def test_rmsnorm_quant(oracle_mod, N, K, symmetric):
     X = synth.activations(N, K, seed=K + N, outlier_frac=0.01)
@@ -64,7 +67,8 @@ def test_rmsnorm_quant(oracle_mod, N, K, symmetric):
     assert torch.equal(Q1, Q) and torch.equal(s1.view(torch.int32), s.view(torch.int32))
 
 
-@pytest.mark.parametrize("N,M", [(1, 12288), (8, 12288), (3, 3072), (2, 777)])
+@pytest.mark.parametrize("N,M", [(1, 12288), (8, 12288), (3, 3072), (2, 777), (1, 1025),
+                                 (4, 32768)])
 @pytest.mark.parametrize("symmetric", [False, True])
 def test_swiglu_quant(oracle_mod, N, M, symmetric):
     rng = np.random.default_rng(M + N)
