@@ -267,7 +267,9 @@ TL_API tl_status tl_embed(const int8_t *E, const float *scale, int64_t V, int D,
  * in one pass: the op's bf16 output (Y, may be NULL when Q is given) and/or
  * that output quantised per token (Q int8 [N][K], s, z [N]; NULL to skip),
  * Q, s and z being bit for bit what tl_quantize_act(Y, symmetric) gives.
- * One CTA per token row, K <= 32768.  The pages fix neither the rounding
+ * K <= 32768; a row runs on one CTA or, when long (SwiGLU beyond 1024
+ * columns, RMSNorm beyond 8192), on a cluster of up to eight CTAs that
+ * exchange their partial sums and ranges.  The pages fix neither the rounding
  * of these ops nor how their outputs are quantised; here the op is computed
  * in fp32 (IEEE division and square root; exp from the CUDA math library),
  * rounded once to bf16, and that bf16 row is quantised. */
