@@ -26,7 +26,9 @@ CASE_GROUPS = {"qkv": 0, "o": 1, "gate_up": 2, "down": 3}
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", default="gate_up", choices=sorted(CASE_GROUPS) + ["quant", "chain", "stack", "head"])
+    ap.add_argument("--case", default="gate_up",
+                    choices=sorted(CASE_GROUPS) + ["quant", "chain", "stack", "head", "blockscale",
+                                                   "rmsnorm", "swiglu"])
     ap.add_argument("--n", type=int, default=1)
     ap.add_argument("--mode", default="a", choices=["a", "b", "f"],
                     help="a: bf16, b: int8 from the quantiser, f: int8 quantised in the launch")
@@ -77,6 +79,36 @@ def main() -> None:
         torch.cuda.synchronize()
         if chain.status() != 0:
             raise SystemExit(f"chain status {chain.status()}")
+        return
+    if args.case == "blockscale":
+        # the gate-shaped 12288 x 4096 matrix with one scale per (row, 128-column block)
+        M, K = shp["gate"]
+        rng = np.random.default_rng(7)
+        bw = tl.BlockScaledWeight.from_float(rng.standard_normal((M, K), dtype=np.float32) * 0.02)
+        x = synth.activations(args.n, K, seed=3)
+        xt = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        y = torch.empty((args.n, M), dtype=torch.float32, device="cuda")
+        for _ in range(args.warmup + args.reps):
+            tl.tl_linear_blockscale(bw, xt, out=y)
+        torch.cuda.synchronize()
+        return
+    if args.case in ("rmsnorm", "swiglu"):
+        # RMSNorm over the hidden size, SwiGLU over the feed-forward size, each
+        # with the per-token quantisation fused
+        rng = np.random.default_rng(5)
+        D = shp["q"][1] if args.case == "rmsnorm" else shp["gate"][0]
+
+        def bf16(arr):
+            return torch.from_numpy(synth.to_bf16_bits(arr.astype(np.float32)).view(np.int16)).view(
+                torch.bfloat16).cuda()
+        a1 = bf16(rng.standard_normal((args.n, D)))
+        a2 = bf16(rng.uniform(0.8, 1.2, D)) if args.case == "rmsnorm" else bf16(rng.standard_normal((args.n, D)))
+        for _ in range(args.warmup + args.reps):
+            if args.case == "rmsnorm":
+                tl.tl_rmsnorm_quant(a1, a2, 1e-6)
+            else:
+                tl.tl_swiglu_quant(a1, a2)
+        torch.cuda.synchronize()
         return
     if args.case == "quant":
         K = shp["down"][1]
