@@ -838,3 +838,22 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
 }
 
 }  // namespace tl_internal
+
+extern "C" {
+
+tl_status tl_prefill_plan(const tl_weight *Ws, int G, int N, int sms, int32_t *plan) {
+    if (!Ws || !plan) return TL_ERR_NULL;
+    if (G < 1 || G > TL_MAX_GROUP || N < 1 || sms < 1) return TL_ERR_SHAPE;
+    for (int g = 0; g < G; ++g)
+        if (Ws[g].M < 1 || Ws[g].K < 1 || Ws[g].M > TL_MAX_M || Ws[g].K > TL_MAX_K ||
+            Ws[g].K != Ws[0].K)
+            return TL_ERR_SHAPE;
+    const tl_internal::PrefillPlan p = tl_internal::prefill_plan(Ws, G, N, Ws[0].K, sms);
+    const long long items = (long long)p.tiles * p.S;
+    const int32_t v[TL_PREFILL_PLAN_FIELDS] = {p.BN, p.S, p.KBS, p.tiles,
+                                               (int32_t)(items < sms ? items : sms)};
+    for (int i = 0; i < TL_PREFILL_PLAN_FIELDS; ++i) plan[i] = v[i];
+    return TL_OK;
+}
+
+}  // extern "C"

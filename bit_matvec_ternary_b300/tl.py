@@ -34,7 +34,7 @@ TL_MAX_GROUP = 4
 
 # Every symbol include/tl.h declares.
 EXPORTS = ("tl_packed_bytes", "tl_pack", "tl_validate_packed", "tl_workspace_bytes",
-           "tl_decode_plan", "tl_quantize_act", "tl_linear", "tl_linear_group",
+           "tl_decode_plan", "tl_prefill_plan", "tl_quantize_act", "tl_linear", "tl_linear_group",
            "tl_head_workspace_bytes", "tl_head_argmax", "tl_embed",
            "tl_rmsnorm_quant", "tl_swiglu_quant", "tl_ternarize_absmean",
            "tl_linear_blockscale",
@@ -66,6 +66,8 @@ _lib.tl_workspace_bytes.argtypes = [C.POINTER(tl_weight), _int, _int]
 _lib.tl_workspace_bytes.restype = _sz
 _lib.tl_decode_plan.argtypes = [C.POINTER(tl_weight), _int, _int, _int, C.POINTER(C.c_int32)]
 _lib.tl_decode_plan.restype = _int
+_lib.tl_prefill_plan.argtypes = [C.POINTER(tl_weight), _int, _int, _int, C.POINTER(C.c_int32)]
+_lib.tl_prefill_plan.restype = _int
 _lib.tl_quantize_act.argtypes = [_p, _int, _int, _p, _p, _p, _int, _p]
 _lib.tl_quantize_act.restype = _int
 _lib.tl_linear.argtypes = [C.POINTER(tl_weight), _p, _p, _p, _p, _int, _int, _int, _p, _sz,
@@ -269,6 +271,18 @@ def decode_plan(weights, N: int, sms: int) -> dict:
     out = (C.c_int32 * len(PLAN_FIELDS))()
     _check(_lib.tl_decode_plan(_structs(ws), len(ws), N, sms, out), "tl_decode_plan")
     return dict(zip(PLAN_FIELDS, list(out)))
+
+
+PREFILL_PLAN_FIELDS = ("BN", "S", "KBS", "tiles", "grid")
+
+
+def prefill_plan(weights, N: int, sms: int) -> dict:
+    """The tensor-core kernel's tile width, K splits and grid for these
+    shapes (host only)."""
+    ws = weights if isinstance(weights, (list, tuple)) else [weights]
+    out = (C.c_int32 * len(PREFILL_PLAN_FIELDS))()
+    _check(_lib.tl_prefill_plan(_structs(ws), len(ws), N, sms, out), "tl_prefill_plan")
+    return dict(zip(PREFILL_PLAN_FIELDS, list(out)))
 
 
 def make_workspace(weights_lists, N: int, device="cuda"):

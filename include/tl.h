@@ -158,6 +158,18 @@ TL_API size_t tl_workspace_bytes(const tl_weight *Ws, int G, int N);
 #define TL_PLAN_FIELDS 14
 TL_API tl_status tl_decode_plan(const tl_weight *Ws, int G, int N, int sms, int32_t *plan);
 
+/* HOST.  The tensor-core kernel's plan for these shapes at batch N (used
+ * from N = 256 on) on a GPU with `sms` SMs; runs no GPU code and needs no
+ * GPU, for tests and tuning (the pages describe no such call).
+ * plan[TL_PREFILL_PLAN_FIELDS] receives: tokens per tile BN (256 or 128),
+ * K splits S, 128-column blocks per split KBS, output tiles (128 rows x BN
+ * tokens, over the group), and CTAs launched (one per SM at most).  The
+ * planner minimises rounds of items x blocks per split x the block time of
+ * BN, plus a cost per extra split.  Returns TL_ERR_NULL, TL_ERR_SHAPE or
+ * TL_OK. */
+#define TL_PREFILL_PLAN_FIELDS 5
+TL_API tl_status tl_prefill_plan(const tl_weight *Ws, int G, int N, int sms, int32_t *plan);
+
 /* DEVICE.  Per-token activation quantisation (bf16 -> int8).  X_bf16 [N][K]
  * (2-byte aligned), Q [N][K] int8, s [N] fp32, z [N] int32.
  *   symmetric == 0: lo = min(0, min x), hi = max(0, max x),

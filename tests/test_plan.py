@@ -148,3 +148,54 @@ def test_decode_plan_rejects_bad_arguments():
         tl.decode_plan([_w(16, 128), _w(16, 256)], 1, 148)     # K differs inside a group
     with pytest.raises(Exception):
         tl.decode_plan([_w(16, 128)], 1, 0)
+
+
+# ---------------------------------------------------------------- prefill plan
+# The 8B groups at 512 tokens, as measured on B300: q/k/v and gate+up in
+# 256-token tiles unsplit, o in 128-token tiles (128 items, no K split), down
+# in 256-token tiles with two K splits.
+PREFILL_8B = {
+    "qkv": ([4096, 1024, 1024], 4096, (256, 1)),
+    "o": ([4096], 4096, (128, 1)),
+    "gate_up": ([12288, 12288], 4096, (256, 1)),
+    "down": ([4096], 12288, (256, 2)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_8B))
+def test_prefill_plan_of_the_8b_groups(name):
+    Ms, K, (bn, s) = PREFILL_8B[name]
+    p = tl.prefill_plan([_w(M, K) for M in Ms], 512, 148)
+    assert (p["BN"], p["S"]) == (bn, s)
+    mt = sum(_cdiv(M, 128) for M in Ms)
+    assert p["tiles"] == mt * _cdiv(512, bn)
+    assert p["grid"] == min(p["tiles"] * p["S"], 148)
+
+
+@pytest.mark.parametrize("K", [128, 1000, 4096, 12288, 65536])
+@pytest.mark.parametrize("Ms", [[128], [777], [4096], [4096, 1024, 1024], [12288, 12288], [20000]])
+@pytest.mark.parametrize("N", [256, 300, 512, 1000, 4096])
+@pytest.mark.parametrize("sms", [1, 132, 148])
+def test_prefill_plan_invariants(K, Ms, N, sms):
+    """Whatever the shapes: a width the kernel has, splits of whole 128-column
+    blocks (at least four each when K is split) with none empty, the tile
+    count of that width, and no more CTAs than SMs or items."""
+    p = tl.prefill_plan([_w(M, K) for M in Ms], N, sms)
+    KB = _cdiv(K, 128)
+    assert p["BN"] in (128, 256)
+    assert p["S"] >= 1 and p["KBS"] >= 1
+    assert p["S"] == _cdiv(KB, p["KBS"])                 # no empty split
+    assert (p["S"] - 1) * p["KBS"] < KB <= p["S"] * p["KBS"]
+    if p["S"] > 1:
+        assert KB // p["S"] >= 4
+    assert p["tiles"] == sum(_cdiv(M, 128) for M in Ms) * _cdiv(N, p["BN"])
+    assert 1 <= p["grid"] == min(p["tiles"] * p["S"], sms)
+
+
+def test_prefill_plan_rejects_bad_arguments():
+    import ctypes
+    buf = (ctypes.c_int32 * len(tl.PREFILL_PLAN_FIELDS))()
+    assert tl._lib.tl_prefill_plan(None, 1, 512, 148, None) == tl.TL_ERR_NULL
+    ws = tl._structs([_w(4096, 4096), _w(1024, 2048)])
+    assert tl._lib.tl_prefill_plan(ws, 2, 512, 148, buf) == tl.TL_ERR_SHAPE   # K differs
+    assert tl._lib.tl_prefill_plan(tl._structs([_w(4096, 4096)]), 1, 0, 148, buf) == tl.TL_ERR_SHAPE
