@@ -674,22 +674,23 @@ PrefillPlan prefill_plan(const tl_weight *Ws, int G, int N, int K, int sms) {
     return best;
 }
 
-// Workspace of a prefill call: the status word at the front, nothing else
-// kept zero; its scratch at the back, ending at the workspace's end:
-//   [arrival counter per tile, if K is split: cleared at the start of the call]
+// Workspace of a prefill call.  At the front, kept zero between calls: the
+// status word, then (if K is split) one arrival counter per tile, which the
+// item completing a tile sets back to zero.  Its scratch at the back, ending
+// at the workspace's end:
 //   [bf16 copy of the int8 activations, mode B; the quantised activations as
 //    bf16 and their steps and zero points, TL_MODE_I8_FUSED]
 //   [fp32 partial tiles, if K is split]
 // (offsets below are from the start of that scratch), so prefill and decode
 // calls may share one workspace in any order.
 struct PrefillLayout {
-    size_t cnt, conv, qs, qz, part, back;
+    size_t front, conv, qs, qz, part, back;
 };
 PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S, int BN) {
     using tl_internal::round256;
     PrefillLayout L;
-    L.cnt = 0;
-    L.conv = L.cnt + (S > 1 ? round256((size_t)tiles * 8) : 0);
+    L.front = kStatusBytes + (S > 1 ? round256((size_t)tiles * 8) : 0);
+    L.conv = 0;
     L.qs = L.conv + (mode != TL_MODE_BF16 ? round256((size_t)N * K * 2) : 0);
     L.qz = L.qs + (mode == TL_MODE_I8_FUSED ? round256((size_t)N * 4) : 0);
     L.part = L.qz + (mode == TL_MODE_I8_FUSED ? round256((size_t)N * 4) : 0);
@@ -700,7 +701,8 @@ PrefillLayout prefill_layout(int N, int K, int mode, int tiles, int S, int BN) {
 
 size_t prefill_workspace_bytes(const tl_weight *Ws, int G, int N, int K, int mode, int sms) {
     const PrefillPlan pl = prefill_plan(Ws, G, N, K, sms);
-    return workspace_need(kStatusBytes, prefill_layout(N, K, mode, pl.tiles, pl.S, pl.BN).back);
+    const PrefillLayout L = prefill_layout(N, K, mode, pl.tiles, pl.S, pl.BN);
+    return workspace_need(L.front, L.back);
 }
 
 bool prefill_supported(int N, int K) { return N >= kPrefillMinN && (K % 8) == 0; }
@@ -752,10 +754,9 @@ tl_status launch_prefill(const tl_weight *Ws, int G, const void *X, const float 
     const void *xb = X;
     __nv_bfloat16 *conv = reinterpret_cast<__nv_bfloat16 *>(wsc + L.conv);
     const long long n = (long long)N * K;
-    a.cnt = reinterpret_cast<unsigned long long *>(wsc + L.cnt);
+    // the arrival counters sit in the front bytes, zero between calls
+    a.cnt = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kStatusBytes);
     a.part = reinterpret_cast<float *>(wsc + L.part);
-    if (a.S > 1 && cudaMemsetAsync(a.cnt, 0, (size_t)tiles * 8, stream) != cudaSuccess)
-        return TL_ERR_CUDA;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;

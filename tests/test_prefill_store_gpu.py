@@ -3,7 +3,8 @@ whole tiles leave by TMA stores when the output rows allow it (16-byte
 aligned, a multiple of 16 bytes) and by element stores otherwise.  Mode B
 bit for bit against the oracle (fp32, bf16 and raw int32 outputs, both
 quantiser variants, a group, ragged token counts), mode A within the
-tolerance."""
+tolerance.  And a K-split launch's arrival counters, kept in the
+workspace's front bytes."""
 import numpy as np
 import pytest
 
@@ -73,3 +74,35 @@ def test_unsplit_prefill_group(oracle_mod):
     for m, y in zip(mats, ys):
         _, Yr = _b(oracle_mod, m, X, False)
         assert np.array_equal(y.cpu().view(torch.int16).numpy().view(np.uint16), oracle_mod.bf16_rne(Yr))
+
+
+def test_split_prefill_leaves_the_front_zero(oracle_mod):
+    """A K-split launch keeps its per-tile arrival counters in the
+    workspace's front bytes (no clearing launch before it): after the call
+    they are zero again, and the same workspace then serves a decode call
+    and a second split call correctly."""
+    M, Kb, N = 1024, 12288, 300
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = tl.prefill_plan([tl.tl_weight(0x1000, 0x2000, 0x3000, M, Kb, tl.TL_LAYOUT_TL2P_V2)], N, sms)
+    assert p["S"] > 1
+    m = Mat(oracle_mod, M, Kb, seed=91)
+    X = synth.activations(N, Kb, seed=92)
+    Q, s, z = tl.tl_quantize_act(bf16_tensor(X))
+    need = max(tl.tl_workspace_bytes([m.dev], N), tl.tl_workspace_bytes([m.dev], 3))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    y1 = tl.tl_linear(m.dev, Q, s, z, mode=tl.TL_MODE_I8, workspace=ws)
+    torch.cuda.synchronize()
+    front = 256 + p["tiles"] * 8
+    assert int(ws[:front].count_nonzero()) == 0
+    _, Yr = _b(oracle_mod, m, X, False)
+    assert np.array_equal(y1.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+    # a decode call, then the split call again, on the same workspace
+    X1 = synth.activations(3, Kb, seed=93)
+    Q1, s1, z1 = tl.tl_quantize_act(bf16_tensor(X1))
+    y3 = tl.tl_linear(m.dev, Q1, s1, z1, mode=tl.TL_MODE_I8, workspace=ws)
+    y2 = tl.tl_linear(m.dev, Q, s, z, mode=tl.TL_MODE_I8, workspace=ws)
+    torch.cuda.synchronize()
+    _, Yr1 = _b(oracle_mod, m, X1, False)
+    assert np.array_equal(y3.cpu().numpy().view(np.uint32), Yr1.view(np.uint32))
+    assert np.array_equal(y2.cpu().numpy().view(np.uint32), Yr.view(np.uint32))
+    assert int(ws[:front].count_nonzero()) == 0
