@@ -26,6 +26,17 @@ from . import tl
 GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 
 
+def copy_chunks(layers: int):
+    """The host-copy chunks of ``LinearStack.capture_e2e`` as lists of
+    [first, last) layer ranges: inputs as layer 0, then all the others;
+    outputs in runs of about a quarter of the layers, the last layer alone."""
+    L = layers
+    ins = [(0, 1)] + ([(1, L)] if L > 1 else [])
+    every = max(1, (L - 1 + 3) // 4)
+    outs = [(lo, min(lo + every, L - 1)) for lo in range(0, L - 1, every)] + [(L - 1, L)]
+    return ins, outs
+
+
 class StackWeights:
     """The packed weights of every layer, resident on the device.
 
@@ -203,9 +214,7 @@ class LinearStack:
         if hx.shape != self.X_flat.shape or hy.shape != self.Y_flat.shape:
             raise ValueError("host buffers must match X_flat and Y_flat")
         L = self.layers
-        ins = [(0, 1)] + ([(1, L)] if L > 1 else [])
-        every = max(1, (L - 1 + 3) // 4)
-        outs = [(lo, min(lo + every, L - 1)) for lo in range(0, L - 1, every)] + [(L - 1, L)]
+        ins, outs = copy_chunks(L)
         main = torch.cuda.Stream()
         cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
         main.wait_stream(torch.cuda.current_stream())
