@@ -290,19 +290,23 @@ tl_head_mma_kernel(const __grid_constant__ HeadArgs a) {
     // this lane's 16 bytes of rows g and g + 8 of the group at v0, for each of
     // the warp's (at most eight) 64-column steps; zero past the CTA's rows
     uint4 wa[8], wb[8];
-    auto load_group = [&](long long v0) {
+    // steps 4h .. 4h + 3 (half h) of the group at v0
+    auto load_half = [&](long long v0, int h) {
         const long long ra = v0 + g, rb = v0 + g + 8;
         const int8_t *ha = a.H + ra * a.D + 16 * t;
         const int8_t *hb = a.H + rb * a.D + 16 * t;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 4 * h; u < 4 * h + 4; ++u) {
             const int cc = c_lo + u * kHMmaStep;
             const bool in = u * kHMmaStep < cols;
             wa[u] = in && ra < r1 ? ld_stream(reinterpret_cast<const uint4 *>(ha + cc)) : make_uint4(0u, 0u, 0u, 0u);
             wb[u] = in && rb < r1 ? ld_stream(reinterpret_cast<const uint4 *>(hb + cc)) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
-    if (r0 < r1) load_group(r0);
+    if (r0 < r1) {
+        load_half(r0, 0);
+        load_half(r0, 1);
+    }
     int pb = 0;
     for (long long v0 = r0, gi = 0; v0 < r1; v0 += kHMmaRows, ++gi) {
         const long long ra = v0 + g, rb = v0 + g + 8;
@@ -312,10 +316,18 @@ tl_head_mma_kernel(const __grid_constant__ HeadArgs a) {
         const float scb = epi && rb < r1 ? __ldg(a.scale + rb) : 0.f;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         int rs[2] = {0, 0};
+        const bool more = v0 + kHMmaRows < r1;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
+            if (u == 4) {
+                // the first half's registers are read: the next group's first
+                // half goes out now (the empty asm keeps the compiler from
+                // hoisting these loads above the MMAs that still read them)
+                asm volatile("" ::: "memory");
+                if (more) load_half(v0 + kHMmaRows, 0);
+            }
             const int cc = c_lo + u * kHMmaStep;
-            if (u * kHMmaStep >= cols) break;
+            if (u * kHMmaStep >= cols) continue;
             const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + cc);
             const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + cc + 8);
             const uint32_t A[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
@@ -331,8 +343,9 @@ tl_head_mma_kernel(const __grid_constant__ HeadArgs a) {
                 rs[1] = dp4(B[st], 0x01010101u, rs[1]);
             }
         }
-        // the next group's loads go out before the barrier and the epilogue
-        if (v0 + kHMmaRows < r1) load_group(v0 + kHMmaRows);
+        // and its second half, before the barrier and the epilogue
+        asm volatile("" ::: "memory");
+        if (more) load_half(v0 + kHMmaRows, 1);
         // this warp's exact integer sums for the group
         int *mine = part[pb][warp][lane];
 #pragma unroll
