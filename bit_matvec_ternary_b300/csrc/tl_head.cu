@@ -32,8 +32,9 @@
 // the products go to the tensor cores instead.  A CTA's eight warps work on
 // one 16-row group of H at a time, warp w taking columns [w D/8, (w+1) D/8):
 // lane (g, t) loads 16 bytes of rows g and g + 8 per 64 columns (all of the
-// warp's share in flight at once, the next group's issued before this one's
-// barrier and epilogue), turns each int8 pair into exact fp16 (a
+// warp's share in flight at once, in two halves: the next group's half is
+// issued as soon as this group's half has been read), turns each int8 pair
+// into exact fp16 (a
 // byte permute under a 2^10 exponent, then 1152 subtracted), and multiplies
 // them by the tokens' activations (staged once per CTA as exact fp16) with
 // mma.m16n8k16 into fp32.  Products are integers of at most 2^14 and a warp
