@@ -72,3 +72,35 @@ def test_certificate():
 def test_draft_length_is_checked():
     with pytest.raises(ValueError):
         speculative_decode(Affine(7, 1, 1), Affine(7, 1, 1), 0, 5, k=8)
+
+
+@pytest.mark.parametrize("n", [0, 1, 2])
+def test_short_runs_return_exactly_n_tokens(n):
+    target = Affine(1009, 17, 5)
+    seq, st = speculative_decode(target, Affine(1009, 17, 5), 4, n, k=7)
+    assert seq == greedy_decode(target, 4, n) and len(seq) == n + 1
+    assert st.rounds == (0 if n == 0 else 1)
+
+
+@pytest.mark.parametrize("k", range(1, 8))
+def test_every_draft_length_gives_greedy_and_consistent_counts(k):
+    V = 997
+    target = Affine(V, 31, 7)
+    rng = np.random.default_rng(k)
+    bad = {int(t): int((t + 1) % V) for t in rng.choice(V, size=V // 4, replace=False)}
+    seq, st = speculative_decode(target, Affine(V, 31, 7, override=bad), 2, 150, k=k)
+    assert seq == greedy_decode(target, 2, 150)
+    assert st.drafted == k * st.rounds and 0 <= st.accepted <= st.drafted
+    # every round appends its accepted proposals and one token of the target's
+    assert st.accepted + st.rounds >= 150
+    assert all(len(b) == k + 1 for b, _ in st.verify_batches)
+    assert st.tokens_per_round == pytest.approx((st.accepted + st.rounds) / st.rounds)
+
+
+def test_certificate_rejects_a_sequence_that_differs_from_greedy():
+    target = Affine(1009, 17, 5)
+    seq, st = speculative_decode(target, Affine(1009, 17, 5), 3, 20, k=4)
+    wrong = greedy_decode(target, 3, 20)
+    wrong[7] = (wrong[7] + 1) % 1009
+    cert = certify(target, seq, st, wrong)
+    assert cert.batch_invariant and not cert.identical_to_greedy and not cert.ok
