@@ -195,6 +195,50 @@ def test_head_arguments_checked_without_a_gpu():
     assert tl._lib.tl_embed(None, p, 10, 64, p, 1, p, None) == tl.TL_ERR_NULL
 
 
+def test_blockscale_arguments_checked_without_a_gpu():
+    f = tl._lib.tl_linear_blockscale
+    p = 0x10000
+    ok = dict(packed=p, bscale=p, M=64, K=256, X=p, N=1, Y=p, out=tl.TL_OUT_F32)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["packed"], a["bscale"], a["M"], a["K"], a["X"], a["N"], a["Y"], a["out"], 0, None)
+
+    assert call(packed=None) == tl.TL_ERR_NULL
+    assert call(bscale=None) == tl.TL_ERR_NULL
+    assert call(X=None) == tl.TL_ERR_NULL
+    assert call(Y=None) == tl.TL_ERR_NULL
+    assert call(M=0) == tl.TL_ERR_SHAPE
+    assert call(K=0) == tl.TL_ERR_SHAPE
+    assert call(N=0) == tl.TL_ERR_SHAPE
+    assert call(K=(1 << 20) + 1) == tl.TL_ERR_SHAPE
+    assert call(out=tl.TL_OUT_I32_RAW) == tl.TL_ERR_MODE
+    assert call(packed=p + 8) == tl.TL_ERR_ALIGN          # 16-byte codes
+    assert call(bscale=p + 2) == tl.TL_ERR_ALIGN
+    assert call(X=p + 1) == tl.TL_ERR_ALIGN
+    assert call(Y=p + 2) == tl.TL_ERR_ALIGN               # fp32 out
+    assert call(Y=p + 2, out=tl.TL_OUT_BF16) != tl.TL_ERR_ALIGN   # bf16 out: 2 bytes suffice
+
+
+def test_fused_neighbour_arguments_checked_without_a_gpu():
+    rq, sq = tl._lib.tl_rmsnorm_quant, tl._lib.tl_swiglu_quant
+    p = 0x10000
+    # X, gamma, eps, N, K, Y, Q, s, z, symmetric
+    assert rq(None, p, 1e-6, 1, 64, p, p, p, p, 0, None) == tl.TL_ERR_NULL
+    assert rq(p, p, 1e-6, 1, 64, None, None, p, p, 0, None) == tl.TL_ERR_NULL   # no output asked
+    assert rq(p, p, 1e-6, 1, 64, p, p, None, p, 0, None) == tl.TL_ERR_NULL      # Q without s
+    assert rq(p, p, 1e-6, 0, 64, p, p, p, p, 0, None) == tl.TL_ERR_SHAPE
+    assert rq(p, p, 1e-6, 1, 32769, p, p, p, p, 0, None) == tl.TL_ERR_SHAPE     # longest row 32768
+    assert rq(p + 1, p, 1e-6, 1, 64, p, p, p, p, 0, None) == tl.TL_ERR_ALIGN
+    assert rq(p, p, 1e-6, 1, 64, p, p, p + 2, p, 0, None) == tl.TL_ERR_ALIGN
+    assert rq(p, p, -1.0, 1, 64, p, p, p, p, 0, None) == tl.TL_ERR_BAD_VALUE
+    assert rq(p, p, float("nan"), 1, 64, p, p, p, p, 0, None) == tl.TL_ERR_BAD_VALUE
+    # G, U, N, M, H, Q, s, z, symmetric
+    assert sq(p, None, 1, 64, p, p, p, p, 0, None) == tl.TL_ERR_NULL
+    assert sq(p, p, 65536, 64, p, p, p, p, 0, None) == tl.TL_ERR_SHAPE
+    assert sq(p, p, 1, 64, p, p, p, p + 1, 0, None) == tl.TL_ERR_ALIGN
+
+
 @pytest.mark.parametrize("M,K", [(7, 300), (64, 128), (33, 1000)])
 def test_absmean_ternarizer_matches_oracle(oracle_mod, M, K):
     """The library's host ternariser gives the oracle's codes and scales bit
